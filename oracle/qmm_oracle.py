@@ -242,8 +242,8 @@ def pack_b_int8(B, b_type: str):
 #     holds the 8 codes of block b at columns k = 32 b + 8 t + j, j = 0..7.
 #     Inside the word, code j = 2i sits in bits [4i, 4i+4) and code j = 2i+1
 #     in bits [16+4i, 16+4i+4), i = 0..3.
-#   bytes [4096, 5120): 256 (scale, min) pairs of bf16.  The pair of (block b,
-#     row r) is at byte 4096 + 4*(32 b + r): scale in the low 16 bits, min in
+#   bytes [4096, 5120): 256 (scale, min) pairs of bf16.  The pair of (row r,
+#     block b) is at byte 4096 + 4*(8 r + b): scale in the low 16 bits, min in
 #     the high 16 bits.
 #
 #   Decoded weight: w[32 tr + r][256 tc + k] = q * scale + min.
@@ -297,7 +297,7 @@ def q4_tiles_from_blocks(q, s, m):
     sb = bf16_bits(s).reshape(TR, TILE_ROWS, TC, 8)   # tr, r, tc, b
     mb = bf16_bits(m).reshape(TR, TILE_ROWS, TC, 8)
     pair = sb.astype(np.uint32) | (mb.astype(np.uint32) << 16)
-    pair = pair.transpose(0, 2, 3, 1)                 # tr, tc, b, r
+    pair = pair.transpose(0, 2, 1, 3)                 # tr, tc, r, b
     out[:, :, 4096:] = pair.reshape(TR, TC, 256).astype(np.uint32).view(np.uint8).reshape(TR, TC, 1024)
     return out.reshape(-1)
 
@@ -321,11 +321,11 @@ def q4_blocks_from_tiles(tiles, N, K):
         q[..., j] = ((w64 >> np.uint64(shift)) & np.uint64(0xF)).astype(np.int64)
     # k within tile = 32 b + 8 t + j
     q = q.transpose(0, 2, 1, 4, 3, 5).reshape(N, K)   # tr r tc b t j
-    pairs = t[:, :, 4096:].copy().view(np.uint32).reshape(TR, TC, 8, TILE_ROWS)  # tr tc b r
+    pairs = t[:, :, 4096:].copy().view(np.uint32).reshape(TR, TC, TILE_ROWS, 8)  # tr tc r b
     s = bf16_from_bits((pairs & 0xFFFF).astype(np.uint16))
     m = bf16_from_bits((pairs >> 16).astype(np.uint16))
-    s = s.transpose(0, 3, 1, 2).reshape(N, K // BLOCK)  # tr r tc b
-    m = m.transpose(0, 3, 1, 2).reshape(N, K // BLOCK)
+    s = s.transpose(0, 2, 1, 3).reshape(N, K // BLOCK)  # tr r tc b
+    m = m.transpose(0, 2, 1, 3).reshape(N, K // BLOCK)
     return q, s, m
 
 

@@ -45,7 +45,7 @@ def scalar_tile_writer(q, s, m):
             buf[byte] |= int(q[n, k]) << (bit % 8)
         for blk in range(K // 32):
             tc, b = divmod(blk, 8)
-            base = (tr * TC + tc) * 5120 + 4096 + 4 * (32 * b + r)
+            base = (tr * TC + tc) * 5120 + 4096 + 4 * (8 * r + b)
             buf[base:base + 2] = int(sb[n, blk]).to_bytes(2, "little")
             buf[base + 2:base + 4] = int(mb[n, blk]).to_bytes(2, "little")
     return np.frombuffer(bytes(buf), dtype=np.uint8)
