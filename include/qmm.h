@@ -1,0 +1,230 @@
+/*
+ * qmm.h -- C ABI of the quantized projection matmul library for one GB300 (sm_103a).
+ *
+ * Two halves:
+ *   (I)  an exact int8 GEMM with zero-point correction, per-column weight
+ *        scale, optional int32 bias and float or requantised output;
+ *   (II) a 4-bit block-weight GEMM/GEMV over 32x256 tiles of q4_1 blocks and
+ *        its MUL_MAT_ID (mixture-of-experts) variant.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * - Every pointer argument is a DEVICE pointer on the current CUDA device,
+ *   except the size outputs (size_t*) and the epilogue struct, which are host
+ *   pointers.
+ * - The caller allocates and owns every buffer.  No entry point allocates or
+ *   frees device memory, synchronises the stream, or keeps mutable state
+ *   between calls.  The one exception is a per-process cache of the driver
+ *   entry point used to build TMA descriptors.  Pointers are borrowed until
+ *   the work queued on `stream` has finished.
+ * - Work is queued on `stream` and runs asynchronously.  Argument errors are
+ *   found on the host and returned at once, and nothing is launched when a
+ *   check fails.
+ * - Errors found on the device go to `dev_status`, a device int32 that the
+ *   caller sets to 0 (it may be NULL).  These are a bounded wait that ran out
+ *   (QMM_ERR_TIMEOUT) and an expert id outside [0, n_expert)
+ *   (QMM_ERR_BAD_EXPERT_ID).  The library only ever replaces a 0 there with
+ *   an error code, so the caller reads it after synchronising.
+ * - Shapes the library has no kernel for return QMM_ERR_UNSUPPORTED.  There
+ *   is no fallback path.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QMM_OK = 0,
+  QMM_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size, type or zero point */
+  QMM_ERR_UNSUPPORTED = 2,     /* valid request the library has no kernel for */
+  QMM_ERR_OVERFLOW_BOUND = 3,  /* K*255*128 >= 2^31: int32 sums could overflow */
+  QMM_ERR_CUDA = 4,            /* a CUDA runtime call failed (e.g. launch) */
+  QMM_ERR_TIMEOUT = 5,         /* device: a bounded pipeline wait gave up */
+  QMM_ERR_BAD_EXPERT_ID = 6,   /* device: an expert id was outside [0, n_expert) */
+  QMM_ERR_WORKSPACE = 7        /* workspace pointer NULL, misaligned or smaller than required */
+} qmm_status;
+
+typedef enum {
+  QMM_U8 = 1,
+  QMM_S8 = 2,
+  QMM_S32 = 3,
+  QMM_F32 = 4,
+  QMM_BF16 = 5
+} qmm_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* qmm_status_string(qmm_status s);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int qmm_version(void);
+
+/* ========================================================================
+ * (I) int8 GEMM
+ *
+ * Defined by "int8 inference" (recursiveai.org/onemodel/docs/int8/),
+ * section "Product kernel (Int8Gemm)":
+ *     A' = A - 128 for uint8 A, A for int8 (B the same);
+ *     zA' = zA - 128 for uint8 A (zB' likewise);
+ *     S[m,n] = sum_k A'[m,k] B'[k,n]                        (exact int32)
+ *     Y[m,n] = S - zA' colSum[n] - zB' (rowSum[m] - K zA')   (= sum (A-zA)(B-zB))
+ * followed by the epilogue, in this order: optional int32 bias, then the
+ * output conversion.  "The ONNX pack: weights to Q4NX, matmuls to our
+ * kernels, no VitisAI", sections "The three layers of the pack" and "What
+ * works today", fixes packB's scale = amax/127, the float dequant
+ * C = Cm * s_x[m] * s_w[n], and the fused QuantizeLinear
+ * y_q = clamp(round_half_even(C * s_x s_w / s_y) + zp_y).
+ * ======================================================================== */
+
+/* Packed-weight size: N rows of Kp = K rounded up to 64 bytes. */
+qmm_status qmm_pack_b_int8_size(int64_t K, int64_t N, size_t* packed_bytes);
+
+/* packB: build the kernel's weight layout once per weight.
+ *
+ * B        [K][N] row-major, row stride `ldb` elements (ldb >= N).
+ * b_type   QMM_F32: quantise each column, s = amax/127 (fp32, IEEE division),
+ *                   q = clamp(round_half_even(W/s), -127, 127); a zero column
+ *                   gets s = 0 and q = 0.  Scales go to col_scale[N].
+ *          QMM_S8 / QMM_U8: integer weights, stored shifted (B' = B, or B-128
+ *                   for uint8); col_scale is not touched (may be NULL).
+ * packed   int8 [N][Kp], K-major (byte n*Kp + k holds B'[k][n]; bytes k >= K
+ *          are 0).  Base 16-byte aligned, `packed_bytes` >= qmm_pack_b_int8_size.
+ * col_sum  int32 [N]: colSum[n] = sum_k B'[k][n], kept beside the weight.
+ * Errors: QMM_ERR_INVALID_ARG for null/misaligned pointers, K < 1, N < 1,
+ * ldb < N or a bad type; QMM_ERR_OVERFLOW_BOUND when K*255*128 >= 2^31.
+ */
+qmm_status qmm_pack_b_int8(const void* B, qmm_dtype b_type, int64_t K, int64_t N, int64_t ldb,
+                           void* packed, size_t packed_bytes, float* col_scale, int32_t* col_sum,
+                           cudaStream_t stream);
+
+/* Epilogue of qmm_int8_gemm (all pointers device, [N] or [M] fp32/int32). */
+typedef struct {
+  qmm_dtype out_type;      /* QMM_S32 (Y + bias), QMM_F32, QMM_S8 or QMM_U8 */
+  const int32_t* bias;     /* [N] int32 added to Y before any conversion, or NULL */
+  const float* s_x;        /* activation scale: NULL means 1.0 */
+  int64_t s_x_stride;      /* 0: per-tensor s_x[0]; 1: per-row s_x[m] */
+  const float* s_w;        /* [N] per-column weight scale, or NULL for 1.0 */
+  float s_y;               /* output scale (S8/U8 only), > 0 */
+  int32_t zp_y;            /* output zero point (S8/U8 only), added after rounding */
+} qmm_epilogue;
+
+/* Workspace the int8 GEMM needs for an (M, K, N) call (0 when none). */
+qmm_status qmm_int8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes);
+
+/* Y = A (x) packB with zero points, bias and the chosen output.
+ *
+ * A        [M][K] uint8 or int8 (a_type), row stride lda bytes: lda >= K,
+ *          lda % 16 == 0, base 16-byte aligned.  zA in A's own domain.
+ * packedB  from qmm_pack_b_int8 with the same K and N; col_sum from the same call.
+ * b_orig_type  the b_type given to packB (QMM_U8, QMM_S8 or QMM_F32); zB is in
+ *          that domain and must be 0 for QMM_F32 weights (symmetric).
+ * ep       epilogue (host pointer to the struct; its arrays are device).
+ * out      [M][N] with row stride ldo elements of the output type (ldo >= N).
+ * workspace / ws_bytes  device scratch of at least
+ *          qmm_int8_gemm_workspace_size(M, K, N) bytes, 256-byte aligned
+ *          (may be NULL when that size is 0).
+ * Output conversions (fp32 IEEE, round-to-nearest-even, no contraction):
+ *   S32: Yb = Y + bias
+ *   F32: fl(fl(fl(Yb) * s_x[m]) * s_w[n])
+ *   S8/U8: Mq = fl(fl(s_x[m] * s_w[n]) / s_y); q = rint_even(fl(fl(Yb) * Mq)) + zp_y,
+ *          clamped to the output type's range.
+ * The result is bit-exact and independent of the kernel chosen.  The caller
+ * must keep |Y|, |Y + bias| < 2^31.
+ * Errors: as packB, plus QMM_ERR_OVERFLOW_BOUND for K*255*128 >= 2^31,
+ * QMM_ERR_INVALID_ARG for zero points outside the operand domain, and
+ * QMM_ERR_WORKSPACE.  Device status: QMM_ERR_TIMEOUT.
+ */
+qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int64_t lda,
+                         int32_t zA, const void* packedB, const int32_t* col_sum, int64_t N,
+                         qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out,
+                         int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                         cudaStream_t stream);
+
+/* ========================================================================
+ * (II) 4-bit block weights
+ *
+ * Tile geometry from "NPU engine: full ELFs, no xclbin", section "Q4NX
+ * chunks".  A weight of N rows (outputs) x K columns (inputs) is a grid of
+ * 32-row x 256-column tiles, 5120 bytes each, stored row-major over the grid
+ * ([N/32][K/256] tiles).  The q4_1 semantics come from "Zaya 8B Q4NX on the
+ * AMD NPU", round 26: w = q * scale + min, where q is a 4-bit code 0..15 and
+ * scale and min are bf16, one pair per (row, 32-column block).
+ *
+ * The byte map inside a tile is this library's own, because the pages do not
+ * print one:
+ *   bytes [0, 4096)    codes: row r owns bytes [128 r, 128 r + 128) as 32
+ *                      little-endian uint32 words; word 8 t + b (t = 0..3,
+ *                      b = 0..7) holds the codes of columns 32 b + 8 t + j,
+ *                      j = 0..7, with code j = 2i in bits [4i, 4i+4) and code
+ *                      j = 2i+1 in bits [16+4i, 16+4i+4).
+ *   bytes [4096, 5120) (scale, min) bf16 pairs: the pair of (row r, block b)
+ *                      sits at byte 4096 + 4 (8 r + b), scale in the low half.
+ * ======================================================================== */
+
+/* Tile bytes of an N x K weight: (N/32) * (K/256) * 5120. */
+qmm_status qmm_pack_q4_size(int64_t N, int64_t K, size_t* tile_bytes);
+
+/* Quantise fp32 W [N][K] (row stride ldw elements, ldw >= K) into tiles.
+ * Per block of 32 consecutive k of one row (fp32 IEEE steps):
+ *   s = bf16_rne((max - min) / 15), m = bf16_rne(min),
+ *   q = clamp(rint_even((x - m) / s), 0, 15), q = 0 where s == 0.
+ * Requires N % 32 == 0 and K % 256 == 0 (else QMM_ERR_UNSUPPORTED); tiles
+ * 16-byte aligned with tile_bytes >= qmm_pack_q4_size.
+ */
+qmm_status qmm_pack_q4(const float* W, int64_t N, int64_t K, int64_t ldw, void* tiles,
+                       size_t tile_bytes, cudaStream_t stream);
+
+/* Y[m][n] = sum_k X[m][k] * w[n][k] with fp32 accumulation.
+ *
+ * tiles  one N x K tile set (16-byte aligned).  N % 32 == 0, K % 256 == 0.
+ * X      bf16 [M][K], row stride ldx elements (ldx >= K, ldx % 8 == 0, base
+ *        16-byte aligned).
+ * Y      fp32 [M][N], row stride ldy elements (ldy >= N).
+ * Small M runs the decode GEMV kernel, larger M the tensor-core GEMM; both
+ * compute the same function, within the accuracy bound
+ * max |y - y_exact| <= 2e-3 * sum_k |x||w|.
+ */
+qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, int64_t M,
+                       int64_t ldx, float* Y, int64_t ldy, int32_t* dev_status,
+                       cudaStream_t stream);
+
+/* Workspace of qmm_q4_gemm_id: routing tables for n_expert experts and
+ * T*n_used (token, slot) pairs. */
+qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64_t T,
+                                         size_t* ws_bytes);
+
+/* MUL_MAT_ID over q4 experts ("Zaya 8B Q4NX on the AMD NPU": the new
+ * MUL_MAT_ID_Q4NX op; "The bugs that were the work"; the down-projection fix
+ * of the rounds 24-28 notes).
+ *
+ * tiles     n_expert consecutive N x K tile sets (expert e starts at byte
+ *           e * qmm_pack_q4_size(N, K)).
+ * X         bf16 activations.  Slot i of token t reads the row at element
+ *           offset t*ldx_token + i*ldx_slot: ldx_slot = 0 gives the shared src1
+ *           of gate/up ([T][K]); ldx_slot = K gives the per-slot src1 of down
+ *           ([T][n_used][K]).  ldx_token and ldx_slot % 8 == 0.
+ * ids       int32, a STRIDED view: the expert of (t, i) is ids[t*ld_ids + i]
+ *           (ld_ids >= n_used, e.g. 17 for the top-8 of 17 sorted ids).
+ * Y         fp32; row (t, i) starts at element t*ldy_token + i*ldy_slot.
+ * workspace device scratch of qmm_q4_gemm_id_workspace_size bytes (256-byte
+ *           aligned), rewritten on every call.
+ * Y[t][i][n] = sum_k x(t,i)[k] * w_{ids(t,i)}[n][k].  A pair whose id is
+ * outside [0, n_expert) is skipped (its output row is left untouched) and
+ * dev_status gets QMM_ERR_BAD_EXPERT_ID.
+ */
+qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_t K,
+                          const void* X, int64_t ldx_token, int64_t ldx_slot, const int32_t* ids,
+                          int64_t ld_ids, int64_t n_used, int64_t T, float* Y, int64_t ldy_token,
+                          int64_t ldy_slot, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -1,0 +1,233 @@
+// C-ABI entry points: argument validation, kernel choice, launch.
+//
+// Every check runs on the host before anything is queued.  Kernel choice is
+// by shape only: every route computes the same function (bit-exact for the
+// int8 half, within the stated bound for the 4-bit half).  A shape with no
+// kernel returns QMM_ERR_UNSUPPORTED.
+#include <cstdio>
+#include <cstdlib>
+
+#include "qmm_internal.h"
+
+using namespace qmm;
+
+namespace {
+
+qmm_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return QMM_OK;
+  if (std::getenv("QMM_LOG")) std::fprintf(stderr, "qmm: CUDA error %s\n", cudaGetErrorString(e));
+  return QMM_ERR_CUDA;
+}
+
+bool k_bound_ok(int64_t K) { return K * 255 * 128 < (int64_t(1) << 31); }
+
+bool zp_in_domain(int32_t z, qmm_dtype t) {
+  if (t == QMM_U8) return z >= 0 && z <= 255;
+  if (t == QMM_S8) return z >= -128 && z <= 127;
+  return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qmm_status_string(qmm_status s) {
+  switch (s) {
+    case QMM_OK: return "QMM_OK";
+    case QMM_ERR_INVALID_ARG: return "QMM_ERR_INVALID_ARG";
+    case QMM_ERR_UNSUPPORTED: return "QMM_ERR_UNSUPPORTED";
+    case QMM_ERR_OVERFLOW_BOUND: return "QMM_ERR_OVERFLOW_BOUND";
+    case QMM_ERR_CUDA: return "QMM_ERR_CUDA";
+    case QMM_ERR_TIMEOUT: return "QMM_ERR_TIMEOUT";
+    case QMM_ERR_BAD_EXPERT_ID: return "QMM_ERR_BAD_EXPERT_ID";
+    case QMM_ERR_WORKSPACE: return "QMM_ERR_WORKSPACE";
+  }
+  return "QMM_ERR_UNKNOWN";
+}
+
+int qmm_version(void) { return 100; }
+
+// ---------------------------------------------------------------------------
+// int8
+// ---------------------------------------------------------------------------
+
+qmm_status qmm_pack_b_int8_size(int64_t K, int64_t N, size_t* packed_bytes) {
+  if (packed_bytes == nullptr || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (!k_bound_ok(K)) return QMM_ERR_OVERFLOW_BOUND;
+  *packed_bytes = (size_t)(N * padded_k(K));
+  return QMM_OK;
+}
+
+qmm_status qmm_pack_b_int8(const void* B, qmm_dtype b_type, int64_t K, int64_t N, int64_t ldb,
+                           void* packed, size_t packed_bytes, float* col_scale, int32_t* col_sum,
+                           cudaStream_t stream) {
+  if (B == nullptr || packed == nullptr || col_sum == nullptr) return QMM_ERR_INVALID_ARG;
+  if (K < 1 || N < 1 || ldb < N) return QMM_ERR_INVALID_ARG;
+  if (b_type != QMM_F32 && b_type != QMM_S8 && b_type != QMM_U8) return QMM_ERR_INVALID_ARG;
+  if (b_type == QMM_F32 && col_scale == nullptr) return QMM_ERR_INVALID_ARG;
+  if (!k_bound_ok(K)) return QMM_ERR_OVERFLOW_BOUND;
+  if (!aligned(packed, 16) || !aligned(col_sum, 4)) return QMM_ERR_INVALID_ARG;
+  if (b_type == QMM_F32 && (!aligned(B, 4) || !aligned(col_scale, 4))) return QMM_ERR_INVALID_ARG;
+  if (packed_bytes < (size_t)(N * padded_k(K))) return QMM_ERR_INVALID_ARG;
+  if (N > (int64_t)1 << 30) return QMM_ERR_UNSUPPORTED;
+  return cuda_status(launch_pack_b_int8(B, b_type, K, N, ldb, static_cast<int8_t*>(packed),
+                                        padded_k(K), col_scale, col_sum, stream));
+}
+
+qmm_status qmm_int8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes) {
+  if (ws_bytes == nullptr || M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (!k_bound_ok(K)) return QMM_ERR_OVERFLOW_BOUND;
+  *ws_bytes = 0;
+  return QMM_OK;
+}
+
+qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int64_t lda,
+                         int32_t zA, const void* packedB, const int32_t* col_sum, int64_t N,
+                         qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out,
+                         int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                         cudaStream_t stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  (void)dev_status;
+  if (A == nullptr || packedB == nullptr || col_sum == nullptr || ep == nullptr || out == nullptr)
+    return QMM_ERR_INVALID_ARG;
+  if (M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (a_type != QMM_U8 && a_type != QMM_S8) return QMM_ERR_INVALID_ARG;
+  if (b_orig_type != QMM_U8 && b_orig_type != QMM_S8 && b_orig_type != QMM_F32)
+    return QMM_ERR_INVALID_ARG;
+  if (!k_bound_ok(K)) return QMM_ERR_OVERFLOW_BOUND;
+  if (lda < K || lda % 16 != 0 || !aligned(A, 16) || !aligned(packedB, 16)) return QMM_ERR_INVALID_ARG;
+  if (!zp_in_domain(zA, a_type)) return QMM_ERR_INVALID_ARG;
+  if (b_orig_type == QMM_F32 ? zB != 0 : !zp_in_domain(zB, b_orig_type)) return QMM_ERR_INVALID_ARG;
+  const qmm_dtype ot = ep->out_type;
+  if (ot != QMM_S32 && ot != QMM_F32 && ot != QMM_S8 && ot != QMM_U8) return QMM_ERR_INVALID_ARG;
+  if (ldo < N) return QMM_ERR_INVALID_ARG;
+  if (ep->s_x != nullptr && ep->s_x_stride != 0 && ep->s_x_stride != 1) return QMM_ERR_INVALID_ARG;
+  if ((ot == QMM_S8 || ot == QMM_U8) && !(ep->s_y > 0.0f)) return QMM_ERR_INVALID_ARG;
+  const size_t osz = (ot == QMM_S32 || ot == QMM_F32) ? 4 : 1;
+  if (!aligned(out, osz)) return QMM_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+
+  Int8GemmArgs a{};
+  a.A = static_cast<const int8_t*>(A);
+  a.a_u8 = (a_type == QMM_U8);
+  a.M = (int)M;
+  a.K = (int)K;
+  a.N = (int)N;
+  a.lda = lda;
+  a.B = static_cast<const int8_t*>(packedB);
+  a.Kp = padded_k(K);
+  const int32_t zAp = a_type == QMM_U8 ? zA - 128 : zA;
+  const int32_t zBp = b_orig_type == QMM_U8 ? zB - 128 : zB;
+  a.need_rowsum = (zBp != 0);
+  a.epi.out_type = (int)ot;
+  a.epi.bias = ep->bias;
+  a.epi.s_x = ep->s_x;
+  a.epi.s_x_stride = (int)ep->s_x_stride;
+  a.epi.s_w = ep->s_w;
+  a.epi.s_y = ep->s_y;
+  a.epi.zp_y = ep->zp_y;
+  a.epi.zAp = (uint32_t)zAp;
+  a.epi.zBp = (uint32_t)zBp;
+  a.epi.Kz = (uint32_t)((int64_t)K * zAp);
+  a.epi.col_sum = col_sum;
+  a.epi.out = out;
+  a.epi.ldo = ldo;
+  if ((M + 31) / 32 > 65535) return QMM_ERR_UNSUPPORTED;
+  return cuda_status(launch_int8_gemm_mma(a, stream));
+}
+
+// ---------------------------------------------------------------------------
+// 4-bit
+// ---------------------------------------------------------------------------
+
+qmm_status qmm_pack_q4_size(int64_t N, int64_t K, size_t* tile_bytes) {
+  if (tile_bytes == nullptr || N < 1 || K < 1) return QMM_ERR_INVALID_ARG;
+  if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+  *tile_bytes = (size_t)((N / kTileRows) * (K / kTileCols) * kTileBytes);
+  return QMM_OK;
+}
+
+qmm_status qmm_pack_q4(const float* W, int64_t N, int64_t K, int64_t ldw, void* tiles,
+                       size_t tile_bytes, cudaStream_t stream) {
+  if (W == nullptr || tiles == nullptr || N < 1 || K < 1 || ldw < K) return QMM_ERR_INVALID_ARG;
+  if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+  if (!aligned(W, 4) || !aligned(tiles, 16)) return QMM_ERR_INVALID_ARG;
+  if (tile_bytes < (size_t)((N / kTileRows) * (K / kTileCols) * kTileBytes)) return QMM_ERR_INVALID_ARG;
+  if (N * (K / 32) > (int64_t)INT32_MAX * 64) return QMM_ERR_UNSUPPORTED;
+  return cuda_status(launch_pack_q4(W, N, K, ldw, static_cast<uint8_t*>(tiles), stream));
+}
+
+qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, int64_t M,
+                       int64_t ldx, float* Y, int64_t ldy, int32_t* dev_status,
+                       cudaStream_t stream) {
+  (void)dev_status;
+  if (tiles == nullptr || X == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
+  if (N < 1 || K < 1 || M < 1 || ldx < K || ldy < N) return QMM_ERR_INVALID_ARG;
+  if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+  if (ldx % 8 != 0 || !aligned(X, 16) || !aligned(tiles, 16) || !aligned(Y, 4))
+    return QMM_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  Q4DenseArgs a{};
+  a.tiles = static_cast<const uint8_t*>(tiles);
+  a.N = (int)N;
+  a.K = (int)K;
+  a.M = (int)M;
+  a.X = static_cast<const __nv_bfloat16*>(X);
+  a.ldx = ldx;
+  a.Y = Y;
+  a.ldy = ldy;
+  return cuda_status(launch_q4_gemv(a, stream));
+}
+
+qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64_t T,
+                                         size_t* ws_bytes) {
+  if (ws_bytes == nullptr || n_expert < 1 || n_used < 1 || T < 1) return QMM_ERR_INVALID_ARG;
+  if (n_expert > kMaxExperts || T * n_used > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  *ws_bytes = q4_moe_workspace_bytes(n_expert, n_used, T);
+  return QMM_OK;
+}
+
+qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_t K,
+                          const void* X, int64_t ldx_token, int64_t ldx_slot, const int32_t* ids,
+                          int64_t ld_ids, int64_t n_used, int64_t T, float* Y, int64_t ldy_token,
+                          int64_t ldy_slot, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, cudaStream_t stream) {
+  if (tiles == nullptr || X == nullptr || ids == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
+  if (n_expert < 1 || N < 1 || K < 1 || n_used < 1 || T < 1 || ld_ids < n_used)
+    return QMM_ERR_INVALID_ARG;
+  if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+  if (n_expert > kMaxExperts || n_expert > 65535 || T * n_used > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  if (ldx_token < 0 || ldx_slot < 0 || ldx_token % 8 != 0 || ldx_slot % 8 != 0)
+    return QMM_ERR_INVALID_ARG;
+  if (ldx_slot == 0 ? ldx_token < K : (ldx_slot < K || ldx_token < ldx_slot * n_used))
+    return QMM_ERR_INVALID_ARG;
+  if (ldy_token < 0 || ldy_slot < 0) return QMM_ERR_INVALID_ARG;
+  if (!(ldy_slot >= N && ldy_token >= ldy_slot * n_used)) return QMM_ERR_INVALID_ARG;
+  if (!aligned(X, 16) || !aligned(tiles, 16) || !aligned(Y, 4) || !aligned(ids, 4))
+    return QMM_ERR_INVALID_ARG;
+  const size_t need = q4_moe_workspace_bytes(n_expert, n_used, T);
+  if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256)) return QMM_ERR_WORKSPACE;
+  Q4MoEArgs a{};
+  a.tiles = static_cast<const uint8_t*>(tiles);
+  a.n_expert = (int)n_expert;
+  a.N = (int)N;
+  a.K = (int)K;
+  a.X = static_cast<const __nv_bfloat16*>(X);
+  a.ldx_token = ldx_token;
+  a.ldx_slot = ldx_slot;
+  a.ids = ids;
+  a.ld_ids = ld_ids;
+  a.n_used = (int)n_used;
+  a.T = (int)T;
+  a.Y = Y;
+  a.ldy_token = ldy_token;
+  a.ldy_slot = ldy_slot;
+  char* ws = static_cast<char*>(workspace);
+  a.offsets = reinterpret_cast<int32_t*>(ws);
+  a.pairs = reinterpret_cast<int32_t*>(ws + (((size_t)(n_expert + 1) * 4 + 255) / 256 * 256));
+  a.dev_status = dev_status;
+  return cuda_status(launch_q4_moe(a, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+// Device-side helpers shared by the kernels: loads, legacy MMA wrappers, the
+// exact int8 epilogue and the error-status word.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "qmm.h"
+
+#define QMM_DEV __device__ __forceinline__
+
+namespace qmm {
+
+// First error wins: a 0 in the caller's status word becomes `code`.
+QMM_DEV void set_status(int32_t* st, int32_t code) {
+  if (st != nullptr) atomicCAS(st, 0, code);
+}
+
+QMM_DEV uint4 ldg128(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Read-once stream (weights): do not allocate in L1.
+QMM_DEV uint4 ldg128_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+QMM_DEV uint32_t u4_get(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// D = A(16x32 s8, row) * B(32x8 s8, col) + D, exact int32 accumulation.
+QMM_DEV void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D with fp32 accumulation.
+QMM_DEV void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                            uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+QMM_DEV float bf16lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
+QMM_DEV float bf16hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Two 4-bit codes of one q4 word as a bf16x2 pair (128 + q0, 128 + q1):
+// code 2i sits in bits [4i, 4i+4) and code 2i+1 in bits [16+4i, 16+4i+4).
+QMM_DEV uint32_t q4_pair_biased(uint32_t word, int i) {
+  uint32_t r;
+  const uint32_t w = word >> (4 * i);
+  // r = (w & 0x000F000F) | 0x43004300 in one lop3
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// int8 epilogue.  Integer steps run modulo 2^32 (uint32): the final Y is the
+// exact value whenever it fits in int32, which the API requires.
+// ---------------------------------------------------------------------------
+struct Int8Epi {
+  int out_type;            // qmm_dtype
+  const int32_t* bias;
+  const float* s_x;
+  int s_x_stride;          // 0 or 1
+  const float* s_w;
+  float s_y;
+  int zp_y;
+  uint32_t zAp;            // zA' (two's complement)
+  uint32_t zBp;            // zB'
+  uint32_t Kz;             // K * zA'
+  const int32_t* col_sum;
+  void* out;
+  int64_t ldo;
+};
+
+QMM_DEV int32_t zp_correct(int32_t S, int32_t colsum, int32_t rowsum, const Int8Epi& e) {
+  uint32_t y = (uint32_t)S - e.zAp * (uint32_t)colsum - e.zBp * ((uint32_t)rowsum - e.Kz);
+  return (int32_t)y;
+}
+
+// Output conversion of one element (fp32 steps with explicit IEEE rounding).
+QMM_DEV void int8_store(const Int8Epi& e, int m, int n, int32_t Y) {
+  const int32_t yb = (int32_t)((uint32_t)Y + (uint32_t)(e.bias ? e.bias[n] : 0));
+  if (e.out_type == QMM_S32) {
+    reinterpret_cast<int32_t*>(e.out)[(int64_t)m * e.ldo + n] = yb;
+    return;
+  }
+  const float sx = e.s_x ? e.s_x[e.s_x_stride ? m : 0] : 1.0f;
+  const float sw = e.s_w ? e.s_w[n] : 1.0f;
+  const float yf = __int2float_rn(yb);
+  if (e.out_type == QMM_F32) {
+    reinterpret_cast<float*>(e.out)[(int64_t)m * e.ldo + n] = __fmul_rn(__fmul_rn(yf, sx), sw);
+    return;
+  }
+  const float mq = __fdiv_rn(__fmul_rn(sx, sw), e.s_y);
+  float r = __fmul_rn(yf, mq);
+  r = fminf(fmaxf(r, -1.0e9f), 1.0e9f);   // keeps the integer conversion in range
+  int q = __float2int_rn(r) + e.zp_y;
+  if (e.out_type == QMM_S8) {
+    q = min(max(q, -128), 127);
+    reinterpret_cast<int8_t*>(e.out)[(int64_t)m * e.ldo + n] = (int8_t)q;
+  } else {
+    q = min(max(q, 0), 255);
+    reinterpret_cast<uint8_t*>(e.out)[(int64_t)m * e.ldo + n] = (uint8_t)q;
+  }
+}
+
+}  // namespace qmm

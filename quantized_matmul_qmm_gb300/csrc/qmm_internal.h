@@ -1,0 +1,76 @@
+// Host-side declarations shared between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qmm.h"
+#include "qmm_device.cuh"
+
+namespace qmm {
+
+constexpr int64_t kTileRows = 32;
+constexpr int64_t kTileCols = 256;
+constexpr int64_t kTileBytes = 5120;
+
+inline int64_t padded_k(int64_t K) { return (K + 63) / 64 * 64; }
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---- packs (pack.cu) ----
+cudaError_t launch_pack_b_int8(const void* B, qmm_dtype b_type, int64_t K, int64_t N, int64_t ldb,
+                               int8_t* packed, int64_t Kp, float* col_scale, int32_t* col_sum,
+                               cudaStream_t stream);
+cudaError_t launch_pack_q4(const float* W, int64_t N, int64_t K, int64_t ldw, uint8_t* tiles,
+                           cudaStream_t stream);
+
+// ---- int8 GEMM ----
+struct Int8GemmArgs {
+  const int8_t* A;         // [M][lda] bytes (uint8 or int8 codes)
+  bool a_u8;
+  int M, K, N;
+  int64_t lda;
+  const int8_t* B;         // packed [N][Kp]
+  int64_t Kp;
+  bool need_rowsum;        // zB' != 0
+  Int8Epi epi;
+};
+// legacy integer MMA route (int8_mma.cu)
+cudaError_t launch_int8_gemm_mma(const Int8GemmArgs& a, cudaStream_t stream);
+// tcgen05 route (int8_umma.cu)
+bool int8_umma_eligible(int64_t M, int64_t K, int64_t N);
+size_t int8_umma_workspace_bytes(int64_t M, int64_t K, int64_t N);
+cudaError_t launch_int8_gemm_umma(const Int8GemmArgs& a, void* workspace, int32_t* dev_status,
+                                  cudaStream_t stream);
+
+// ---- q4 kernels (q4_mma.cu, q4_umma.cu) ----
+struct Q4DenseArgs {
+  const uint8_t* tiles;
+  int N, K, M;
+  const __nv_bfloat16* X;
+  int64_t ldx;
+  float* Y;
+  int64_t ldy;
+};
+cudaError_t launch_q4_gemv(const Q4DenseArgs& a, cudaStream_t stream);
+bool q4_umma_eligible(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream);
+
+struct Q4MoEArgs {
+  const uint8_t* tiles;
+  int n_expert, N, K;
+  const __nv_bfloat16* X;
+  int64_t ldx_token, ldx_slot;
+  const int32_t* ids;
+  int64_t ld_ids;
+  int n_used, T;
+  float* Y;
+  int64_t ldy_token, ldy_slot;
+  int32_t* offsets;   // workspace: [n_expert + 1]
+  int32_t* pairs;     // workspace: [T * n_used]
+  int32_t* dev_status;
+};
+constexpr int64_t kMaxExperts = 4096;
+size_t q4_moe_workspace_bytes(int64_t n_expert, int64_t n_used, int64_t T);
+cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream);
+
+}  // namespace qmm

@@ -1,0 +1,194 @@
+"""Thin ctypes binding of libqmm (include/qmm.h).
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+library.  The functions take torch tensors for device memory and use torch's
+current CUDA stream.  Each one raises ``QmmError`` when the C entry point
+returns a status other than QMM_OK.  There is no Python fallback: if
+libqmm.so is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqmm.so")
+
+QMM_OK, QMM_ERR_INVALID_ARG, QMM_ERR_UNSUPPORTED, QMM_ERR_OVERFLOW_BOUND = 0, 1, 2, 3
+QMM_ERR_CUDA, QMM_ERR_TIMEOUT, QMM_ERR_BAD_EXPERT_ID, QMM_ERR_WORKSPACE = 4, 5, 6, 7
+QMM_U8, QMM_S8, QMM_S32, QMM_F32, QMM_BF16 = 1, 2, 3, 4, 5
+DTYPES = {"u8": QMM_U8, "s8": QMM_S8, "s32": QMM_S32, "f32": QMM_F32, "bf16": QMM_BF16}
+TORCH_OUT = {"s32": torch.int32, "f32": torch.float32, "s8": torch.int8, "u8": torch.uint8}
+
+# exported symbols and their C signatures (restype, argtypes)
+_c = ctypes
+_vp, _i64, _i32, _sz = _c.c_void_p, _c.c_int64, _c.c_int32, _c.c_size_t
+_szp = _c.POINTER(_c.c_size_t)
+
+
+class QmmEpilogue(ctypes.Structure):
+    _fields_ = [("out_type", _c.c_int), ("bias", _vp), ("s_x", _vp), ("s_x_stride", _i64),
+                ("s_w", _vp), ("s_y", _c.c_float), ("zp_y", _i32)]
+
+
+SIGNATURES = {
+    "qmm_status_string": (_c.c_char_p, [_c.c_int]),
+    "qmm_version": (_c.c_int, []),
+    "qmm_pack_b_int8_size": (_c.c_int, [_i64, _i64, _szp]),
+    "qmm_pack_b_int8": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _vp, _sz, _vp, _vp, _vp]),
+    "qmm_int8_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
+    "qmm_int8_gemm": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _c.c_int,
+                                 _i32, _c.POINTER(QmmEpilogue), _vp, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_pack_q4_size": (_c.c_int, [_i64, _i64, _szp]),
+    "qmm_pack_q4": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "qmm_q4_gemm": (_c.c_int, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "qmm_q4_gemm_id_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
+    "qmm_q4_gemm_id": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64, _i64,
+                                  _vp, _i64, _i64, _vp, _sz, _vp, _vp]),
+}
+
+
+class QmmError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} returned {status_string(status)} ({status})")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libqmm.so not built ({path}); run quantized_matmul_qmm_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+lib = load_library()
+
+
+def status_string(s: int) -> str:
+    return lib.qmm_status_string(int(s)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != QMM_OK:
+        raise QmmError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _size(fn, *args) -> int:
+    out = ctypes.c_size_t(0)
+    _check(fn, getattr(lib, fn)(*args, ctypes.byref(out)))
+    return int(out.value)
+
+
+# ---------------------------------------------------------------------------
+# int8
+# ---------------------------------------------------------------------------
+
+def pack_b_int8_size(K: int, N: int) -> int:
+    return _size("qmm_pack_b_int8_size", K, N)
+
+
+def pack_b_int8(B: torch.Tensor, b_type: str):
+    """B: device [K][N] (fp32, int8 or uint8).  Returns (packed [N][Kp] int8,
+    col_scale [N] fp32 or None, col_sum [N] int32)."""
+    K, N = B.shape
+    dev = B.device
+    nbytes = pack_b_int8_size(K, N)
+    packed = torch.empty(nbytes, dtype=torch.int8, device=dev).view(N, nbytes // N)
+    col_scale = torch.empty(N, dtype=torch.float32, device=dev) if b_type == "f32" else None
+    col_sum = torch.empty(N, dtype=torch.int32, device=dev)
+    _check("qmm_pack_b_int8", lib.qmm_pack_b_int8(
+        _ptr(B), DTYPES[b_type], K, N, B.stride(0), _ptr(packed), nbytes, _ptr(col_scale),
+        _ptr(col_sum), _stream()))
+    return packed, col_scale, col_sum
+
+
+def int8_gemm_workspace_size(M: int, K: int, N: int) -> int:
+    return _size("qmm_int8_gemm_workspace_size", M, K, N)
+
+
+def int8_gemm(A: torch.Tensor, a_type: str, zA: int, packed: torch.Tensor, col_sum: torch.Tensor,
+              N: int, b_orig_type: str, zB: int, out_type: str = "s32", bias=None, s_x=None,
+              s_x_stride: int = 0, s_w=None, s_y: float = 1.0, zp_y: int = 0, out=None,
+              workspace=None, dev_status=None):
+    """Y = A (x) packB through qmm_int8_gemm.  Returns the output tensor."""
+    M, K = A.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=TORCH_OUT[out_type], device=A.device)
+    ws_need = int8_gemm_workspace_size(M, K, N)
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=A.device)
+    ep = QmmEpilogue(DTYPES[out_type], _ptr(bias), _ptr(s_x), s_x_stride, _ptr(s_w),
+                     float(s_y), int(zp_y))
+    _check("qmm_int8_gemm", lib.qmm_int8_gemm(
+        _ptr(A), DTYPES[a_type], M, K, A.stride(0), int(zA), _ptr(packed), _ptr(col_sum), N,
+        DTYPES[b_orig_type], int(zB), ctypes.byref(ep), _ptr(out), out.stride(0), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream()))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# 4-bit
+# ---------------------------------------------------------------------------
+
+def pack_q4_size(N: int, K: int) -> int:
+    return _size("qmm_pack_q4_size", N, K)
+
+
+def pack_q4(W: torch.Tensor) -> torch.Tensor:
+    """W: device fp32 [N][K].  Returns the tile bytes (uint8)."""
+    N, K = W.shape
+    nbytes = pack_q4_size(N, K)
+    tiles = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    _check("qmm_pack_q4", lib.qmm_pack_q4(_ptr(W), N, K, W.stride(0), _ptr(tiles), nbytes,
+                                          _stream()))
+    return tiles
+
+
+def q4_gemm(tiles: torch.Tensor, N: int, K: int, X: torch.Tensor, Y=None, dev_status=None):
+    """Y[m][n] = sum_k X[m][k] w[n][k]; X bf16 [M][K] on the device."""
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    _check("qmm_q4_gemm", lib.qmm_q4_gemm(_ptr(tiles), N, K, _ptr(X), M, X.stride(0), _ptr(Y),
+                                          Y.stride(0), _ptr(dev_status), _stream()))
+    return Y
+
+
+def q4_gemm_id_workspace_size(n_expert: int, n_used: int, T: int) -> int:
+    return _size("qmm_q4_gemm_id_workspace_size", n_expert, n_used, T)
+
+
+def q4_gemm_id(tiles: torch.Tensor, n_expert: int, N: int, K: int, X: torch.Tensor,
+               ids: torch.Tensor, ld_ids: int, n_used: int, T: int, Y=None, workspace=None,
+               dev_status=None):
+    """MUL_MAT_ID.  X is [T][K] (shared src1) or [T][n_used][K] (per-slot src1);
+    ids a device int32 buffer read as ids[t*ld_ids + i].  Returns Y [T][n_used][N]."""
+    if X.dim() == 2:
+        ldx_token, ldx_slot = X.stride(0), 0
+    else:
+        ldx_token, ldx_slot = X.stride(0), X.stride(1)
+    if Y is None:
+        Y = torch.empty((T, n_used, N), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = torch.empty(q4_gemm_id_workspace_size(n_expert, n_used, T), dtype=torch.uint8,
+                                device=X.device)
+    _check("qmm_q4_gemm_id", lib.qmm_q4_gemm_id(
+        _ptr(tiles), n_expert, N, K, _ptr(X), ldx_token, ldx_slot, _ptr(ids), ld_ids, n_used, T,
+        _ptr(Y), Y.stride(0), Y.stride(1), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
+    return Y

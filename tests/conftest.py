@@ -30,3 +30,20 @@ def read_golden(name):
 @pytest.fixture
 def golden():
     return read_golden
+
+
+@pytest.fixture(scope="session")
+def qmm():
+    """Build libqmm.so (no-op when current) and return the Python binding."""
+    from quantized_matmul_qmm_gb300 import build as _build
+    _build.build()
+    import quantized_matmul_qmm_gb300.qmm as q
+    return q
+
+
+@pytest.fixture(scope="session")
+def cuda(qmm):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA GPU is required for tests marked gpu")
+    return torch.device("cuda:0")

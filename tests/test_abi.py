@@ -1,0 +1,101 @@
+"""CPU tests of the C ABI: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "qmm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(qmm):
+    names = declared_functions()
+    assert len(names) >= 11
+    lib = ctypes.CDLL(qmm.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(qmm.SIGNATURES)
+
+
+def test_status_strings(qmm):
+    assert qmm.status_string(0) == "QMM_OK"
+    assert qmm.status_string(6) == "QMM_ERR_BAD_EXPERT_ID"
+    assert qmm.status_string(99) == "QMM_ERR_UNKNOWN"
+
+
+def test_size_queries(qmm):
+    assert qmm.pack_b_int8_size(1, 1) == 64
+    assert qmm.pack_b_int8_size(1024, 3) == 3 * 1024
+    assert qmm.pack_b_int8_size(1025, 3) == 3 * 1088
+    assert qmm.pack_q4_size(32, 256) == 5120
+    assert qmm.pack_q4_size(151936, 1024) == 97239040
+    assert qmm.int8_gemm_workspace_size(16, 1024, 1024) >= 0
+
+
+def test_overflow_bound_rejected(qmm):
+    # int8 inference, "Product kernel": safe while K*255*128 < 2^31
+    kmax = (2 ** 31 - 1) // (255 * 128)
+    assert qmm.pack_b_int8_size(kmax, 1) > 0
+    with pytest.raises(qmm.QmmError) as e:
+        qmm.pack_b_int8_size(kmax + 1, 1)
+    assert e.value.status == qmm.QMM_ERR_OVERFLOW_BOUND
+
+
+def test_q4_unsupported_shapes(qmm):
+    for N, K in ((33, 256), (32, 255), (64, 300)):
+        with pytest.raises(qmm.QmmError) as e:
+            qmm.pack_q4_size(N, K)
+        assert e.value.status == qmm.QMM_ERR_UNSUPPORTED
+
+
+def _call(qmm, name, *args):
+    return getattr(qmm.lib, name)(*args)
+
+
+def test_host_validation_before_launch(qmm):
+    L = qmm.lib
+    P = ctypes.c_void_p(1 << 20)      # aligned fake device address: never dereferenced
+    U = ctypes.c_void_p((1 << 20) + 3)  # misaligned
+    ep = qmm.QmmEpilogue(qmm.QMM_S32, None, None, 0, None, 1.0, 0)
+    epb = ctypes.byref(ep)
+    g = lambda *a: L.qmm_int8_gemm(*a)
+    # null A
+    assert g(None, qmm.QMM_U8, 4, 16, 16, 0, P, P, 8, qmm.QMM_S8, 0, epb, P, 8, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    # misaligned A, lda not a multiple of 16
+    assert g(U, qmm.QMM_U8, 4, 16, 16, 0, P, P, 8, qmm.QMM_S8, 0, epb, P, 8, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, qmm.QMM_U8, 4, 16, 24, 0, P, P, 8, qmm.QMM_S8, 0, epb, P, 8, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    # zero point outside the operand domain; zB != 0 for fp32 weights
+    assert g(P, qmm.QMM_U8, 4, 16, 16, 256, P, P, 8, qmm.QMM_S8, 0, epb, P, 8, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, qmm.QMM_S8, 4, 16, 16, 0, P, P, 8, qmm.QMM_S8, 200, epb, P, 8, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, qmm.QMM_S8, 4, 16, 16, 0, P, P, 8, qmm.QMM_F32, 1, epb, P, 8, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    # K beyond the int32 bound
+    assert g(P, qmm.QMM_S8, 4, 70000, 70000, 0, P, P, 8, qmm.QMM_S8, 0, epb, P, 8, None, 0, None, None) == qmm.QMM_ERR_OVERFLOW_BOUND
+    # ldo < N, bad output type, requant without a positive s_y
+    assert g(P, qmm.QMM_S8, 4, 16, 16, 0, P, P, 8, qmm.QMM_S8, 0, epb, P, 7, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    bad = qmm.QmmEpilogue(qmm.QMM_BF16, None, None, 0, None, 1.0, 0)
+    assert g(P, qmm.QMM_S8, 4, 16, 16, 0, P, P, 8, qmm.QMM_S8, 0, ctypes.byref(bad), P, 8, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    rq = qmm.QmmEpilogue(qmm.QMM_S8, None, None, 0, None, 0.0, 0)
+    assert g(P, qmm.QMM_S8, 4, 16, 16, 0, P, P, 8, qmm.QMM_S8, 0, ctypes.byref(rq), P, 8, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    # q4: shapes off the tile grid, X row stride not a multiple of 8
+    assert L.qmm_q4_gemm(P, 33, 256, P, 1, 256, P, 33, None, None) == qmm.QMM_ERR_UNSUPPORTED
+    assert L.qmm_q4_gemm(P, 32, 256, P, 1, 260, P, 32, None, None) == qmm.QMM_ERR_INVALID_ARG
+    # MUL_MAT_ID: ld_ids < n_used, missing workspace
+    assert L.qmm_q4_gemm_id(P, 4, 32, 256, P, 256, 0, P, 2, 3, 5, P, 96, 32, P, 1 << 20, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_q4_gemm_id(P, 4, 32, 256, P, 256, 0, P, 17, 3, 5, P, 96, 32, None, 0, None, None) == qmm.QMM_ERR_WORKSPACE
+    # pack: fp32 weights need a scale output
+    assert L.qmm_pack_b_int8(P, qmm.QMM_F32, 16, 8, 8, P, 1 << 20, None, P, None) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_pack_q4(P, 32, 256, 100, P, 5120, None) == qmm.QMM_ERR_INVALID_ARG
+
+
+def test_binding_has_no_oracle_imports():
+    # the product path never imports the oracle
+    for f in ("qmm.py", "build.py", "__init__.py", "inputs.py"):
+        src = open(os.path.join(ROOT, "quantized_matmul_qmm_gb300", f)).read()
+        assert not re.search(r"^\s*(import|from)\s+oracle", src, flags=re.M), f
