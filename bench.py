@@ -1,0 +1,396 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized projection matmul hot path on GB300.
+
+One step is one pass over every row of the hot path, on seeded synthetic
+inputs that are already resident in HBM:
+  * int8 GEMM      uint8 x int8, M=4096 K=N=4608, zero points, bias, int8 out
+  * q4 GEMV        lm_head (K=1024, N=151936) and the 7 Qwen3-0.6B projections, M=1
+  * q4 prefill     the 7 projections and lm_head at M=512
+  * q4 MUL_MAT_ID  128 experts, top-8 of 17 strided ids, 512 tokens: gate, up, down
+Weight packing (packB, pack_q4) is done once, before timing, as the pages do it
+("once per (tensor, K, N)").  L2 is flushed (a 256 MiB write) before every step.
+
+The printed `value` is int8 GEMM TOPS on the M=4096 K=N=4608 GEMM (the first
+half of the metric).  The q4 GEMV weight bandwidth (its second half) is
+reported in `gemv`.  Every kernel's device time comes from CUDA events on the
+launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qmm|reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs an independent replica
+of the step.  The path has no exchange step, so there is no collective in the
+data path.  Timing is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "int8 GEMM TOPS (% tensor peak); 4-bit GEMV weight GB/s (% HBM) at 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+INT8_M, INT8_K, INT8_N = 4096, 4608, 4608
+WORKLOAD = ("qmm hot path: int8 GEMM u8xs8 M=4096 K=N=4608 (int8 out); q4 GEMV M=1 lm_head "
+            "K=1024 N=151936 + 7 Qwen3-0.6B projections; q4 prefill M=512 (same 8 weights); "
+            "q4 MUL_MAT_ID 128 experts top-8/17 T=512 gate/up/down")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class HotPath:
+    """All device buffers of one step, and the list of library calls."""
+
+    def __init__(self, q, I, dev):
+        import torch
+        self.q, self.dev = q, dev
+        self.calls = []          # (name, fn, launches, work dict)
+        # int8 GEMM
+        c = I.int8_gemm_large()
+        self.int8 = c
+        self.A = c.A.to(dev)
+        packed, _, col_sum = q.pack_b_int8(c.B.to(dev), c.b_type)
+        self.packed, self.col_sum = packed, col_sum
+        self.bias, self.s_w = c.bias.to(dev), c.s_w.to(dev)
+        self.s_x = torch.tensor([c.s_x], dtype=torch.float32, device=dev)
+        self.out8 = torch.empty((c.M, c.N), dtype=torch.int8, device=dev)
+        ws = q.int8_gemm_workspace_size(c.M, c.K, c.N)
+        self.ws8 = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.calls.append(("int8_gemm_m4096", self.run_int8, self.int8_launches(),
+                           {"ops": 2 * c.M * c.N * c.K,
+                            "bytes": c.M * c.K + c.N * q.pack_b_int8_size(c.K, 1) + 4 * c.N * 3 + c.M * c.N}))
+        # q4 dense weights (lm_head + 7 projections), M=1 and M=512
+        shapes = [I.QWEN3_06B_LM_HEAD] + list(I.QWEN3_06B_PROJ)
+        self.q4 = []
+        for name, K, N in shapes:
+            W = I.q4_weights(9 * 1000 + N % 997 + K, N, K).to(dev)
+            tiles = q.pack_q4(W)
+            del W
+            x1 = I.q4_activations(9 * 7919 + 1, 1, K).to(dev)
+            x512 = I.q4_activations(9 * 7919 + 512, 512, K).to(dev)
+            y1 = torch.empty((1, N), dtype=torch.float32, device=dev)
+            y512 = torch.empty((512, N), dtype=torch.float32, device=dev)
+            self.q4.append((name, K, N, tiles, x1, x512, y1, y512))
+        for name, K, N, tiles, x1, _, y1, _ in self.q4:
+            wb = tiles.numel()
+            self.calls.append((f"q4_gemv_{name}_m1", self._q4(tiles, N, K, x1, y1), 1,
+                               {"weight_bytes": wb, "bytes": wb + 2 * K + 4 * N, "flops": 2 * N * K}))
+        for name, K, N, tiles, _, x512, _, y512 in self.q4:
+            wb = tiles.numel()
+            self.calls.append((f"q4_gemm_{name}_m512", self._q4(tiles, N, K, x512, y512),
+                               self.q4_launches(512),
+                               {"flops": 2 * 512 * N * K, "weight_bytes": wb,
+                                "bytes": wb + 2 * 512 * K + 4 * 512 * N}))
+        # MoE
+        self.moe = []
+        for kind in ("gate", "up", "down"):
+            m = I.moe_case(kind)
+            tiles = torch.cat([q.pack_q4(m.W[e].to(dev)) for e in range(m.n_expert)])
+            X = m.X.to(dev)
+            ids = m.ids_buf.to(dev)
+            Y = torch.empty((m.T, m.n_used, m.N), dtype=torch.float32, device=dev)
+            wsb = torch.empty(q.q4_gemm_id_workspace_size(m.n_expert, m.n_used, m.T),
+                              dtype=torch.uint8, device=dev)
+            touched = int(torch.unique(m.ids_buf[:, :m.n_used]).numel())
+            per = tiles.numel() // m.n_expert
+            self.moe.append((kind, m, tiles, X, ids, Y, wsb))
+            self.calls.append((f"q4_moe_{kind}", self._moe(m, tiles, X, ids, Y, wsb), 2,
+                               {"flops": 2 * m.T * m.n_used * m.N * m.K, "weight_bytes": touched * per,
+                                "bytes": touched * per + X.numel() * 2 + Y.numel() * 4}))
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+
+    def int8_launches(self):
+        c = self.int8
+        return 3 if self.q.int8_gemm_workspace_size(c.M, c.K, c.N) > 0 else 1
+
+    def q4_launches(self, M):
+        return 1
+
+    def run_int8(self):
+        c = self.int8
+        self.q.int8_gemm(self.A, c.a_type, c.zA, self.packed, self.col_sum, c.N, c.b_type, c.zB,
+                         "s8", bias=self.bias, s_x=self.s_x, s_w=self.s_w, s_y=c.s_y, zp_y=c.zp_y,
+                         out=self.out8, workspace=self.ws8, dev_status=self.status)
+
+    def _q4(self, tiles, N, K, X, Y):
+        return lambda: self.q.q4_gemm(tiles, N, K, X, Y=Y, dev_status=self.status)
+
+    def _moe(self, m, tiles, X, ids, Y, ws):
+        return lambda: self.q.q4_gemm_id(tiles, m.n_expert, m.N, m.K, X, ids, m.ld_ids, m.n_used,
+                                         m.T, Y=Y, workspace=ws, dev_status=self.status)
+
+
+def run_ours(args, rank, world, dev):
+    import torch
+    import torch.distributed as dist
+    from quantized_matmul_qmm_gb300 import build as B
+    B.build()
+    import quantized_matmul_qmm_gb300.qmm as q
+    from quantized_matmul_qmm_gb300 import inputs as I
+
+    hp = HotPath(q, I, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ncalls = len(hp.calls)
+
+    def step(evs=None):
+        flush.zero_()
+        if evs is not None:
+            evs[0].record(stream)
+        for i, (_, fn, _, _) in enumerate(hp.calls):
+            fn()
+            if evs is not None:
+                evs[i + 1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(hp.status.item()) != 0:
+        raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))} in warm-up")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    all_evs = []
+    for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(ncalls + 1)]
+        step(evs)
+        all_evs.append(evs)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    per_call = [0.0] * ncalls
+    total = 0.0
+    for evs in all_evs:
+        for i in range(ncalls):
+            per_call[i] += evs[i].elapsed_time(evs[i + 1])
+        total += evs[0].elapsed_time(evs[-1])
+    t = torch.tensor(per_call + [total], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    per_call, total = t[:-1].tolist(), float(t[-1])
+
+    # end to end through the public API: pinned host A in, int8 result out
+    c = hp.int8
+    A_host = c.A.pin_memory()
+    out_host = torch.empty((c.M, c.N), dtype=torch.int8).pin_memory()
+    A_dev = torch.empty_like(hp.A)
+    e2e_times = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        A_dev.copy_(A_host, non_blocking=True)
+        q.int8_gemm(A_dev, c.a_type, c.zA, hp.packed, hp.col_sum, c.N, c.b_type, c.zB, "s8",
+                    bias=hp.bias, s_x=hp.s_x, s_w=hp.s_w, s_y=c.s_y, zp_y=c.zp_y, out=hp.out8,
+                    workspace=hp.ws8, dev_status=hp.status)
+        out_host.copy_(hp.out8, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_times.append(e0.elapsed_time(e1))
+    te = torch.tensor([sum(e2e_times)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_ms = float(te) / args.steps
+    if int(hp.status.item()) != 0:
+        raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
+    return hp, per_call, total, clk, e2e_ms
+
+
+def cpu_int8_sample(rows: int):
+    """The oracle (as it stands) on `rows` rows of the M=4096 K=N=4608 GEMM."""
+    import numpy as np
+    import oracle.qmm_oracle as O
+    from quantized_matmul_qmm_gb300 import inputs as I
+    c = I.int8_gemm_large()
+    A = c.A[:rows].numpy().astype(np.int64)
+    B = c.B.numpy().astype(np.int64)
+    t0 = time.perf_counter()
+    r = O.int8_gemm_y(A, c.a_type, c.zA, B, c.b_type, c.zB)
+    O.int8_epilogue(r["Y"], "s8", c.bias.numpy(), c.s_x, c.s_w.numpy(), c.s_y, c.zp_y)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * c.N * c.K / dt / 1e12, dt
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["qmm", "reference"], default="qmm")
+    ap.add_argument("--cpu-rows", type=int, default=8, help="rows of the oracle's CPU sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        # the CPU oracle as the reference arm: rank 0 alone, a bounded sample per step
+        if rank != 0:
+            return
+        rows = 2
+        for _ in range(args.warmup):
+            cpu_int8_sample(rows)
+        tops, secs = [], 0.0
+        for _ in range(args.steps):
+            v, dt = cpu_int8_sample(rows)
+            tops.append(v)
+            secs += dt
+        value = args.steps * 2.0 * rows * INT8_N * INT8_K / secs / 1e12
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "reference": "CPU oracle (numpy int64/fp64)"},
+                "cpu_baseline": {"value": value, "unit": "TOPS", "cores": 1, "kind": "oracle",
+                                 "sample": f"{rows} of 4096 rows of the int8 GEMM per step"},
+                "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hp, per_call, total, clk, e2e_ms = run_ours(args, rank, world, dev)
+    peaks, peak_kind = load_peaks()
+
+    names = [c[0] for c in hp.calls]
+    kern = {}
+    for (name, _, launches, work), ms in zip(hp.calls, per_call):
+        us = 1e3 * ms / args.steps
+        d = {"us": round(us, 3), "launches": launches}
+        if "ops" in work:
+            d["TOPS"] = work["ops"] / (us * 1e-6) / 1e12
+        if "flops" in work:
+            d["TFLOPS"] = work["flops"] / (us * 1e-6) / 1e12
+        if "weight_bytes" in work:
+            d["weight_GBs"] = work["weight_bytes"] / (us * 1e-6) / 1e9
+        d["GBs"] = work["bytes"] / (us * 1e-6) / 1e9
+        kern[name] = d
+    i8 = kern["int8_gemm_m4096"]
+    tensor_peak = peaks["bf16_tflops"]
+    hbm_peak = peaks["hbm_gbs"]
+    value = world * i8["TOPS"]
+    lm = kern["q4_gemv_lm_head_m1"]
+    roof = {"bound": "tensor", "achieved": i8["TOPS"], "peak": tensor_peak, "unit": "TFLOP/s",
+            "frac": i8["TOPS"] / tensor_peak, "traffic": None,
+            "kernel": "int8_gemm_m4096", "peak_source": f"{peak_kind} bf16 (dense 16-bit tensor pipe)"}
+    rooflines = {
+        "q4_gemv_lm_head_m1": {"bound": "hbm", "achieved": lm["GBs"], "peak": hbm_peak,
+                               "unit": "GB/s", "frac": lm["GBs"] / hbm_peak, "traffic": None},
+    }
+    c = hp.int8
+    launches = sum(l for (_, _, l, _) in hp.calls) * args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "int8": f"u8xs8 M={c.M} K={c.K} N={c.N} int8 out",
+                   "l2": "flushed before every step (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "rooflines": rooflines,
+        "gemv": {"value": world * lm["weight_GBs"], "unit": "GB/s", "kernel": "q4_gemv_lm_head_m1",
+                 "frac_hbm": lm["GBs"] / hbm_peak, "peak_source": peak_kind},
+        "kernels": kern,
+        "e2e": {"value": world * 2.0 * c.M * c.N * c.K / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+                "h2d_bytes_per_step": c.M * c.K, "d2h_bytes_per_step": c.M * c.N},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1:
+        v, dt = cpu_int8_sample(args.cpu_rows)
+        line["cpu_baseline"] = {"value": v, "unit": "TOPS", "cores": 1, "kind": "oracle",
+                                "sample": f"{args.cpu_rows} of 4096 rows of the int8 GEMM "
+                                          f"({dt:.1f} s, numpy int64 matmul, one thread)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

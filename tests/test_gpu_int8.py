@@ -1,0 +1,204 @@
+"""GPU parity of the int8 half against the CPU oracle: packs byte-exact, GEMM
+outputs bit-exact, on small odd shapes, on every workload at full size
+(sampled rows where the oracle is slow), with canaries around the output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.qmm_oracle as O
+from quantized_matmul_qmm_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+NP_IN = {"u8": np.uint8, "s8": np.int8}
+T_IN = {"u8": torch.uint8, "s8": torch.int8}
+
+
+def rand_codes(g, t, shape):
+    if t == "u8":
+        return torch.randint(0, 256, shape, generator=g, dtype=torch.int64).to(torch.uint8)
+    return torch.randint(-128, 128, shape, generator=g, dtype=torch.int64).to(torch.int8)
+
+
+def gpu_gemm(qmm, dev, A, a_type, zA, B, b_type, zB, out_type, bias=None, s_x=None,
+             s_x_stride=0, s_w=None, s_y=1.0, zp_y=0, pad_cols=5, lda_pad=0):
+    """Run pack + GEMM on the GPU with a canary-filled, padded output.
+    Returns (out [M][N] numpy, packB outputs)."""
+    M, K = A.shape
+    N = B.shape[1]
+    Bd = B.to(dev)
+    packed, col_scale, col_sum = qmm.pack_b_int8(Bd, b_type)
+    lda = (K + 15) // 16 * 16 + lda_pad
+    Ad = torch.zeros((M, lda), dtype=A.dtype, device=dev)
+    Ad[:, :K] = A.to(dev)
+    Av = Ad[:, :K]                       # row stride lda, K columns
+    ld = N + pad_cols
+    canary = {"s32": 0x5A5A5A5A, "f32": float("nan"), "s8": 77, "u8": 201}[out_type]
+    full = torch.full((M + 1, ld), canary if out_type != "f32" else 0.0,
+                      dtype=qmm.TORCH_OUT[out_type], device=dev)
+    if out_type == "f32":
+        full.view(torch.int32).fill_(0x7FC0DEAD)
+    out = full[:M, :N]
+    if s_w is None and b_type == "f32":
+        s_w = col_scale
+    sx = None if s_x is None else torch.as_tensor(s_x, dtype=torch.float32).reshape(-1).to(dev)
+    qmm.int8_gemm(Av, a_type, zA, packed, col_sum, N, b_type, zB, out_type,
+                  bias=None if bias is None else bias.to(dev), s_x=sx, s_x_stride=s_x_stride,
+                  s_w=None if s_w is None else s_w.to(dev), s_y=s_y, zp_y=zp_y, out=out)
+    torch.cuda.synchronize()
+    f = full.cpu()
+    # canaries: padding columns and the extra row are untouched
+    raw = f.view(torch.int32) if out_type == "f32" else f
+    want = 0x7FC0DEAD if out_type == "f32" else canary
+    assert torch.all(raw[:, N:] == want) and torch.all(raw[M, :] == want), "canary overwritten"
+    return f[:M, :N].numpy(), (packed.cpu().numpy(), None if col_scale is None else col_scale.cpu().numpy(),
+                                col_sum.cpu().numpy())
+
+
+def oracle_out(A, a_type, zA, B, b_type, zB, out_type, bias=None, s_x=None, s_w=None, s_y=1.0,
+               zp_y=0):
+    An = A.numpy().astype(np.int64)
+    Bn = B.numpy()
+    if b_type == "f32":
+        p = O.pack_b_int8(Bn, "f32")
+        codes, s_w_o = p["codes"], p["col_scale"]
+        r = O.int8_gemm_y(An, a_type, zA, codes, "s8", 0)
+        sw = s_w_o if s_w is None else s_w
+    else:
+        r = O.int8_gemm_y(An, a_type, zA, Bn.astype(np.int64), b_type, zB)
+        sw = s_w
+    sw = None if sw is None else np.asarray(sw)
+    return O.int8_epilogue(r["Y"], out_type, None if bias is None else bias.numpy(),
+                           None if s_x is None else np.asarray(s_x, np.float64), sw, s_y, zp_y)
+
+
+def assert_same(got, ref, out_type):
+    if out_type == "f32":
+        assert np.array_equal(got.astype(np.float32).view(np.int32),
+                              ref.astype(np.float32).view(np.int32)), \
+            f"max diff {np.abs(got - ref).max()}"
+    else:
+        bad = np.argwhere(got.astype(np.int64) != ref)
+        assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:3].tolist()}"
+
+
+@pytest.mark.parametrize("b_type", ["f32", "s8", "u8"])
+@pytest.mark.parametrize("K,N", [(1, 1), (15, 7), (64, 32), (100, 33), (1024, 96), (1000, 130)])
+def test_pack_b_int8_bytes(qmm, cuda, b_type, K, N):
+    g = torch.Generator().manual_seed(K * 7 + N)
+    if b_type == "f32":
+        B = torch.randn((K, N), generator=g) * 0.02
+        if N > 3:
+            B[:, 3] = 0.0
+    else:
+        B = rand_codes(g, b_type, (K, N))
+    packed, col_scale, col_sum = qmm.pack_b_int8(B.to(cuda), b_type)
+    torch.cuda.synchronize()
+    ref = O.pack_b_int8(B.numpy(), b_type)
+    assert np.array_equal(packed.cpu().numpy(), ref["packed"])
+    assert np.array_equal(col_sum.cpu().numpy().astype(np.int64), ref["col_sum"])
+    if b_type == "f32":
+        assert np.array_equal(col_scale.cpu().numpy().view(np.int32),
+                              ref["col_scale"].astype(np.float32).view(np.int32))
+
+
+SHAPES = [(1, 1, 1), (3, 15, 7), (16, 64, 32), (17, 65, 33), (33, 100, 40), (5, 1024, 96),
+          (64, 257, 64), (100, 1000, 130)]
+
+
+@pytest.mark.parametrize("a_type,b_type", [("u8", "s8"), ("s8", "s8"), ("u8", "u8"), ("s8", "u8"),
+                                           ("s8", "f32"), ("u8", "f32")])
+@pytest.mark.parametrize("M,K,N", SHAPES)
+def test_gemm_s32_exact(qmm, cuda, a_type, b_type, M, K, N):
+    g = torch.Generator().manual_seed(M * 1000 + K + N)
+    A = rand_codes(g, a_type, (M, K))
+    B = torch.randn((K, N), generator=g) * 0.02 if b_type == "f32" else rand_codes(g, b_type, (K, N))
+    lo = {"u8": 0, "s8": -128}
+    zA = int(torch.randint(lo[a_type], lo[a_type] + 256, (1,), generator=g))
+    zB = 0 if b_type == "f32" else int(torch.randint(lo[b_type], lo[b_type] + 256, (1,), generator=g))
+    got, _ = gpu_gemm(qmm, cuda, A, a_type, zA, B, b_type, zB, "s32")
+    assert_same(got, oracle_out(A, a_type, zA, B, b_type, zB, "s32"), "s32")
+
+
+@pytest.mark.parametrize("out_type", ["s32", "f32", "s8", "u8"])
+@pytest.mark.parametrize("per_row", [False, True])
+def test_gemm_epilogues_exact(qmm, cuda, out_type, per_row):
+    g = torch.Generator().manual_seed(11)
+    M, K, N = 37, 300, 70
+    A = rand_codes(g, "u8", (M, K))
+    B = rand_codes(g, "s8", (K, N))
+    zA, zB = 133, -5
+    bias = torch.randint(-20000, 20000, (N,), generator=g, dtype=torch.int32)
+    s_w = (torch.rand(N, generator=g) * 9e-3 + 1e-3).float()
+    s_x = (torch.rand(M, generator=g) * 0.02 + 0.01).float() if per_row else torch.tensor([1 / 64.0])
+    s_y = 0.37
+    zp = -7 if out_type == "s8" else 120
+    got, _ = gpu_gemm(qmm, cuda, A, "u8", zA, B, "s8", zB, out_type, bias=bias, s_x=s_x,
+                      s_x_stride=1 if per_row else 0, s_w=s_w, s_y=s_y, zp_y=zp)
+    ref = oracle_out(A, "u8", zA, B, "s8", zB, out_type, bias=bias,
+                     s_x=s_x.numpy() if per_row else float(s_x[0]), s_w=s_w.numpy(), s_y=s_y, zp_y=zp)
+    assert_same(got, ref, out_type)
+
+
+def test_page_zero_points(qmm, cuda, golden):
+    # "The ONNX pack", "What works today": zp_x=-40, zp_w=-25, zp_y=-7 on 8x16x6
+    c = golden("onnx_pack_qdq_constants.txt")
+    for (M, K, N) in (c["proof_shape"], c["large_shape"]):
+        g = torch.Generator().manual_seed(M + K + N)
+        A = rand_codes(g, "s8", (M, K))
+        B = rand_codes(g, "s8", (K, N))
+        s_w = (torch.rand(N, generator=g) * 9e-3 + 1e-3).float()
+        got, _ = gpu_gemm(qmm, cuda, A, "s8", c["zp_x"], B, "s8", c["zp_w"], "s8", s_x=[0.02],
+                          s_w=s_w, s_y=0.05, zp_y=c["zp_y"])
+        ref = oracle_out(A, "s8", c["zp_x"], B, "s8", c["zp_w"], "s8", s_x=0.02, s_w=s_w.numpy(),
+                         s_y=0.05, zp_y=c["zp_y"])
+        assert_same(got, ref, "s8")
+
+
+def test_extreme_codes_exact(qmm, cuda):
+    # every product -128 * -128 with K = 4608: |S| = 4608 * 16384, far beyond 2^24
+    M, K, N = 32, 4608, 64
+    A = torch.zeros((M, K), dtype=torch.uint8)             # A' = -128
+    B = torch.full((K, N), -128, dtype=torch.int8)
+    B[:, 1::2] = 127
+    got, _ = gpu_gemm(qmm, cuda, A, "u8", 0, B, "s8", 0, "s32")
+    assert_same(got, oracle_out(A, "u8", 0, B, "s8", 0, "s32"), "s32")
+
+
+def test_workload_int8_m16(qmm, cuda):
+    c = I.int8_gemm_small()
+    for out_type, s_w in (("s32", None), ("f32", c.s_w)):
+        got, _ = gpu_gemm(qmm, cuda, c.A, c.a_type, c.zA, c.B, c.b_type, c.zB, out_type, s_w=s_w)
+        assert_same(got, oracle_out(c.A, c.a_type, c.zA, c.B, c.b_type, c.zB, out_type,
+                                    s_w=None if s_w is None else s_w.numpy()), out_type)
+
+
+@pytest.mark.parametrize("idx", range(7))
+def test_workload_qwen_projection_m32(qmm, cuda, idx):
+    c = I.int8_qwen_projection(idx)
+    got, (packed, col_scale, col_sum) = gpu_gemm(qmm, cuda, c.A, c.a_type, c.zA, c.B, c.b_type,
+                                                 c.zB, "f32", s_x=[c.s_x])
+    ref = oracle_out(c.A, c.a_type, c.zA, c.B, c.b_type, c.zB, "f32", s_x=c.s_x)
+    assert_same(got, ref, "f32")
+
+
+def test_workload_large_sampled(qmm, cuda):
+    """M=4096 K=N=4608 uint8 x int8, int8 output: 24 sampled rows in full and
+    the column sums/scales exactly."""
+    c = I.int8_gemm_large()
+    dev = cuda
+    Bd = c.B.to(dev)
+    packed, _, col_sum = qmm.pack_b_int8(Bd, c.b_type)
+    out = qmm.int8_gemm(c.A.to(dev), c.a_type, c.zA, packed, col_sum, c.N, c.b_type, c.zB,
+                        "s8", bias=c.bias.to(dev), s_x=torch.tensor([c.s_x], device=dev),
+                        s_w=c.s_w.to(dev), s_y=c.s_y, zp_y=c.zp_y)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    rows = np.array([0, 1, 127, 128, 1000, 2047, 2048, 4095] +
+                    list(np.random.default_rng(8).choice(4096, 8, replace=False)))
+    ref = oracle_out(c.A[rows], c.a_type, c.zA, c.B, c.b_type, c.zB, "s8", bias=c.bias,
+                     s_x=c.s_x, s_w=c.s_w.numpy(), s_y=c.s_y, zp_y=c.zp_y)
+    assert_same(got[rows], ref, "s8")
+    # the workload exercises rounding and both clamps
+    assert (got == 127).mean() > 0.001 and (got == -128).mean() > 0.001
+    assert np.array_equal(col_sum.cpu().numpy().astype(np.int64), c.B.numpy().astype(np.int64).sum(0))

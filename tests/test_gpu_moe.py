@@ -1,0 +1,99 @@
+"""GPU parity of MUL_MAT_ID: strided ids, shared and per-slot src1, bad ids."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.qmm_oracle as O
+from quantized_matmul_qmm_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+def run_moe(qmm, dev, W, X, ids_buf, ld_ids, n_used, T, status=None):
+    E, N, K = W.shape
+    tiles = torch.cat([qmm.pack_q4(W[e].to(dev)) for e in range(E)])
+    full = torch.full((T, n_used, N + 4), float("nan"), dtype=torch.float32, device=dev)
+    Y = full[:, :, :N]
+    qmm.q4_gemm_id(tiles, E, N, K, X.to(dev), ids_buf.to(dev), ld_ids, n_used, T, Y=Y,
+                   dev_status=status)
+    torch.cuda.synchronize()
+    f = full.cpu()
+    assert torch.isnan(f[:, :, N:]).all(), "canary overwritten"
+    return tiles.cpu().numpy(), f[:, :, :N].numpy()
+
+
+@pytest.mark.parametrize("shared", [True, False])
+def test_moe_small_full(qmm, cuda, shared):
+    g = torch.Generator().manual_seed(5)
+    E, N, K, T, n_used, ld = 8, 64, 512, 37, 3, 5
+    W = torch.randn((E, N, K), generator=g) * 0.02
+    ids_buf = torch.randint(0, E, (T, ld), generator=g, dtype=torch.int32)
+    X = torch.randn((T, K) if shared else (T, n_used, K), generator=g).to(torch.bfloat16)
+    tiles, Y = run_moe(qmm, cuda, W, X, ids_buf, ld, n_used, T)
+    y, norm = O.q4_gemm_id(tiles, E, N, K, X.float().double().numpy(), shared,
+                           ids_buf.numpy(), ld, n_used, T)
+    assert O.normalized_error(Y, y, norm) <= TOL
+    assert O.normalized_error(Y, y, norm) <= 2e-5
+
+
+def test_moe_contiguous_read_would_differ(qmm, cuda):
+    # the ids view has row stride 17 while n_used = 8: reading 8 contiguous ids
+    # per token would hand token t the experts of other tokens
+    c = I.moe_case("gate", T=16, n_expert=16)
+    Wsmall = c.W[:, :64, :512].contiguous()
+    X = c.X[:, :512].contiguous()
+    ids = (c.ids_buf % 16).contiguous()
+    tiles, Y = run_moe(qmm, cuda, Wsmall, X, ids, 17, 8, 16)
+    y, norm = O.q4_gemm_id(tiles, 16, 64, 512, X.float().double().numpy(), True, ids.numpy(), 17, 8, 16)
+    assert O.normalized_error(Y, y, norm) <= TOL
+    wrong = ids.numpy().reshape(-1)[:16 * 8].reshape(16, 8)
+    y_wrong, _ = O.q4_gemm_id(tiles, 16, 64, 512, X.float().double().numpy(), True,
+                              wrong.reshape(-1), 8, 8, 16)
+    assert O.normalized_error(Y, y_wrong, norm) > 0.01
+
+
+def test_moe_bad_id_sets_status(qmm, cuda):
+    g = torch.Generator().manual_seed(6)
+    E, N, K, T, n_used, ld = 4, 32, 256, 6, 2, 3
+    W = torch.randn((E, N, K), generator=g) * 0.02
+    ids = torch.randint(0, E, (T, ld), generator=g, dtype=torch.int32)
+    ids[2, 1] = E          # out of range
+    ids[4, 0] = -1
+    X = torch.randn((T, K), generator=g).to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    tiles, Y = run_moe(qmm, cuda, W, X, ids, ld, n_used, T, status=status)
+    assert int(status.item()) == qmm.QMM_ERR_BAD_EXPERT_ID
+    assert np.isnan(Y[2, 1]).all() and np.isnan(Y[4, 0]).all()
+    good = ids.clone()
+    good[2, 1] = 0
+    good[4, 0] = 0
+    y, norm = O.q4_gemm_id(tiles, E, N, K, X.float().double().numpy(), True, good.numpy(), ld, n_used, T)
+    mask = np.ones((T, n_used), bool)
+    mask[2, 1] = mask[4, 0] = False
+    assert O.normalized_error(Y[mask], y[mask], norm[mask]) <= TOL
+
+
+@pytest.mark.parametrize("kind", ["gate", "down"])
+def test_workload_moe_sampled(qmm, cuda, kind):
+    """128 experts, top-8 of 17 stored ids, 512 tokens: all pairs computed on
+    the GPU, 24 sampled pairs checked against the oracle."""
+    c = I.moe_case(kind)
+    tiles, Y = run_moe(qmm, cuda, c.W, c.X, c.ids_buf, c.ld_ids, c.n_used, c.T)
+    rng = np.random.default_rng(10)
+    ids = O.moe_ids_view(c.ids_buf.numpy(), c.ld_ids, c.n_used, c.T)
+    per = (c.N // 32) * (c.K // 256) * 5120
+    Xn = c.X.float().double().numpy()
+    dense = {}
+    for _ in range(24):
+        t, i = int(rng.integers(c.T)), int(rng.integers(c.n_used))
+        e = int(ids[t, i])
+        if e not in dense:
+            et = tiles[e * per:(e + 1) * per]
+            assert np.array_equal(et, O.pack_q4(c.W[e].numpy()))
+            dense[e] = O.q4_decode(et, c.N, c.K)
+        x = Xn[t] if c.shared_src1 else Xn[t, i]
+        y = dense[e] @ x
+        norm = np.abs(dense[e]) @ np.abs(x)
+        assert O.normalized_error(Y[t, i], y, norm) <= TOL
+    assert np.isfinite(Y).all()

@@ -1,0 +1,95 @@
+"""GPU parity of the 4-bit dense path: tile packing byte-exact against the
+oracle, GEMV/GEMM within max |y - y_ref| <= 2e-3 * sum|x||w| (the oracle is the
+fp64 decode-then-dense "twin")."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.qmm_oracle as O
+from quantized_matmul_qmm_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+def gpu_q4(qmm, dev, W, X, pad=3):
+    N, K = W.shape
+    M = X.shape[0]
+    tiles = qmm.pack_q4(W.to(dev))
+    full = torch.full((M + 1, N + pad), float("nan"), dtype=torch.float32, device=dev)
+    Y = full[:M, :N]
+    qmm.q4_gemm(tiles, N, K, X.to(dev), Y=Y)
+    torch.cuda.synchronize()
+    f = full.cpu()
+    assert torch.isnan(f[:, N:]).all() and torch.isnan(f[M]).all(), "canary overwritten"
+    return tiles.cpu().numpy(), f[:M, :N].numpy()
+
+
+def xnp(X):
+    return X.float().double().numpy()
+
+
+@pytest.mark.parametrize("N,K", [(32, 256), (64, 512), (96, 768), (1024, 1024), (1024, 3072)])
+@pytest.mark.parametrize("M", [1, 2, 7, 8, 9, 16, 17, 33, 100])
+def test_q4_gemm_small_shapes(qmm, cuda, N, K, M):
+    g = torch.Generator().manual_seed(N + K + M)
+    W = torch.randn((N, K), generator=g) * 0.02
+    X = torch.randn((M, K), generator=g).to(torch.bfloat16)
+    tiles, Y = gpu_q4(qmm, cuda, W, X)
+    ref_tiles = O.pack_q4(W.numpy())
+    assert np.array_equal(tiles, ref_tiles)
+    y, norm = O.q4_gemm(ref_tiles, N, K, xnp(X))
+    err = O.normalized_error(Y, y, norm)
+    assert err <= TOL, err
+    assert err <= 2e-5, f"error {err} far above the fp32 accumulation level"
+
+
+def test_q4_special_weights(qmm, cuda):
+    # constant blocks (scale 0), a zero row, one-hot activations
+    N, K = 64, 512
+    g = torch.Generator().manual_seed(3)
+    W = torch.randn((N, K), generator=g) * 0.02
+    W[5, 32:64] = 0.125
+    W[7] = 0.0
+    X = torch.zeros((3, K)).to(torch.bfloat16)
+    X[0, 0] = 1
+    X[1, 300] = 1
+    X[2] = torch.randn(K, generator=g).to(torch.bfloat16)
+    tiles, Y = gpu_q4(qmm, cuda, W, X)
+    ref_tiles = O.pack_q4(W.numpy())
+    assert np.array_equal(tiles, ref_tiles)
+    y, norm = O.q4_gemm(ref_tiles, N, K, xnp(X))
+    assert O.normalized_error(Y, y, norm) <= TOL
+    dense = O.q4_decode(ref_tiles, N, K)
+    assert np.allclose(Y[0], dense[:, 0], rtol=1e-6, atol=1e-7)
+    assert np.allclose(Y[1], dense[:, 300], rtol=1e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("M", [1, 512])
+@pytest.mark.parametrize("idx", range(7))
+def test_workload_qwen_projection(qmm, cuda, idx, M):
+    name, K, N = I.QWEN3_06B_PROJ[idx]
+    c = I.q4_case(name, K, N, M)
+    tiles, Y = gpu_q4(qmm, cuda, c.W, c.X)
+    ref_tiles = O.pack_q4(c.W.numpy())
+    assert np.array_equal(tiles, ref_tiles)
+    y, norm = O.q4_gemm(ref_tiles, N, K, xnp(c.X))
+    err = O.normalized_error(Y, y, norm)
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("M", [1, 16, 512])
+def test_workload_lm_head_sampled(qmm, cuda, M):
+    name, K, N = I.QWEN3_06B_LM_HEAD
+    c = I.q4_case(name, K, N, M)
+    tiles, Y = gpu_q4(qmm, cuda, c.W, c.X, pad=0)
+    rng = np.random.default_rng(M)
+    trs = np.unique(np.concatenate([[0, 1, N // 32 - 1], rng.choice(N // 32, 40, replace=False)]))
+    per = (K // 256) * 5120
+    rows = np.concatenate([np.arange(32 * tr, 32 * tr + 32) for tr in trs])
+    Wn = c.W.numpy()
+    for tr in trs:   # packing of the sampled tile rows, byte for byte
+        assert np.array_equal(tiles[tr * per:(tr + 1) * per], O.pack_q4(Wn[32 * tr:32 * tr + 32]))
+    y, norm = O.q4_gemm_rows(tiles, N, K, xnp(c.X), rows)
+    err = O.normalized_error(Y[:, rows], y, norm)
+    assert err <= TOL, err
