@@ -40,15 +40,16 @@ def test_moe_small_full(qmm, cuda, shared):
 def test_moe_contiguous_read_would_differ(qmm, cuda):
     # the ids view has row stride 17 while n_used = 8: reading 8 contiguous ids
     # per token would hand token t the experts of other tokens
-    c = I.moe_case("gate", T=16, n_expert=16)
+    c = I.moe_case("gate", T=16, n_expert=32)
     Wsmall = c.W[:, :64, :512].contiguous()
     X = c.X[:, :512].contiguous()
-    ids = (c.ids_buf % 16).contiguous()
+    ids = c.ids_buf.contiguous()
+    assert ids.shape == (16, 17)
     tiles, Y = run_moe(qmm, cuda, Wsmall, X, ids, 17, 8, 16)
-    y, norm = O.q4_gemm_id(tiles, 16, 64, 512, X.float().double().numpy(), True, ids.numpy(), 17, 8, 16)
+    y, norm = O.q4_gemm_id(tiles, 32, 64, 512, X.float().double().numpy(), True, ids.numpy(), 17, 8, 16)
     assert O.normalized_error(Y, y, norm) <= TOL
     wrong = ids.numpy().reshape(-1)[:16 * 8].reshape(16, 8)
-    y_wrong, _ = O.q4_gemm_id(tiles, 16, 64, 512, X.float().double().numpy(), True,
+    y_wrong, _ = O.q4_gemm_id(tiles, 32, 64, 512, X.float().double().numpy(), True,
                               wrong.reshape(-1), 8, 8, 16)
     assert O.normalized_error(Y, y_wrong, norm) > 0.01
 
