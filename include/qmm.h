@@ -14,8 +14,9 @@
  *   pointers.
  * - The caller allocates and owns every buffer.  No entry point allocates or
  *   frees device memory, synchronises the stream, or keeps mutable state
- *   between calls.  The one exception is a per-process cache of the driver
- *   entry point used to build TMA descriptors.  Pointers are borrowed until
+ *   between calls.  There are two exceptions: a per-process cache of the
+ *   driver entry point used to build TMA descriptors, and the fixed scratch
+ *   array of qmm_q4_gemm_id_noalloc (see there).  Pointers are borrowed until
  *   the work queued on `stream` has finished.
  * - Work is queued on `stream` and runs asynchronously.  Argument errors are
  *   found on the host and returned at once, and nothing is launched when a
@@ -222,6 +223,33 @@ qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_
                           int64_t ld_ids, int64_t n_used, int64_t T, float* Y, int64_t ldy_token,
                           int64_t ldy_slot, void* workspace, size_t ws_bytes,
                           int32_t* dev_status, cudaStream_t stream);
+
+/* MUL_MAT_ID for callers that cannot allocate device memory.  No counterpart
+ * on the pages: this is a convenience of this library.
+ *
+ * Callers that cannot call cudaMalloc use this entry point.  Examples are a
+ * plugin whose host framework owns every device buffer and passes it only
+ * inputs and outputs, and a latency-critical path where an allocation (which
+ * may synchronise the device) is not allowed.  The call computes exactly what
+ * qmm_q4_gemm_id computes, with the same arguments minus the workspace.  The
+ * routing tables live in a fixed scratch array inside the library's own
+ * device memory (266,496 bytes, held on every GPU that loads the library
+ * until the process exits), so the call allocates nothing.
+ *
+ * Limits: n_expert <= 1024 and T * n_used <= 65536; larger requests return
+ * QMM_ERR_WORKSPACE.
+ * - The first call on each device looks up the scratch array's device
+ *   address and caches it.  Make that first call before any stream capture.
+ * - Every call on a device shares the one array.  Calls that overlap on the
+ *   GPU (other streams, other host threads) race on it, so serialise them.
+ *   The array keeps the last call's routing tables; nothing in it needs to
+ *   start at zero, because each call rewrites what it reads.
+ */
+qmm_status qmm_q4_gemm_id_noalloc(const void* tiles, int64_t n_expert, int64_t N, int64_t K,
+                                  const void* X, int64_t ldx_token, int64_t ldx_slot,
+                                  const int32_t* ids, int64_t ld_ids, int64_t n_used, int64_t T,
+                                  float* Y, int64_t ldy_token, int64_t ldy_slot,
+                                  int32_t* dev_status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

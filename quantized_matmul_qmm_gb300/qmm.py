@@ -47,6 +47,8 @@ SIGNATURES = {
     "qmm_q4_gemm_id_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
     "qmm_q4_gemm_id": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64, _i64,
                                   _vp, _i64, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_q4_gemm_id_noalloc": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
+                                          _i64, _vp, _i64, _i64, _vp, _vp]),
 }
 
 
@@ -191,4 +193,22 @@ def q4_gemm_id(tiles: torch.Tensor, n_expert: int, N: int, K: int, X: torch.Tens
         _ptr(tiles), n_expert, N, K, _ptr(X), ldx_token, ldx_slot, _ptr(ids), ld_ids, n_used, T,
         _ptr(Y), Y.stride(0), Y.stride(1), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
+    return Y
+
+
+def q4_gemm_id_noalloc(tiles: torch.Tensor, n_expert: int, N: int, K: int, X: torch.Tensor,
+                       ids: torch.Tensor, ld_ids: int, n_used: int, T: int, Y: torch.Tensor,
+                       dev_status=None):
+    """MUL_MAT_ID through qmm_q4_gemm_id_noalloc: the same result as
+    q4_gemm_id, for callers that cannot allocate device memory.  The library
+    keeps the routing tables in its own fixed device array, so the caller
+    passes only inputs and the output Y [T][n_used][N] (preallocated).
+    Limits: n_expert <= 1024, T * n_used <= 65536."""
+    if X.dim() == 2:
+        ldx_token, ldx_slot = X.stride(0), 0
+    else:
+        ldx_token, ldx_slot = X.stride(0), X.stride(1)
+    _check("qmm_q4_gemm_id_noalloc", lib.qmm_q4_gemm_id_noalloc(
+        _ptr(tiles), n_expert, N, K, _ptr(X), ldx_token, ldx_slot, _ptr(ids), ld_ids, n_used, T,
+        _ptr(Y), Y.stride(0), Y.stride(1), _ptr(dev_status), _stream()))
     return Y
