@@ -77,7 +77,7 @@ qmm_status qmm_pack_b_int8(const void* B, qmm_dtype b_type, int64_t K, int64_t N
 qmm_status qmm_int8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes) {
   if (ws_bytes == nullptr || M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
   if (!k_bound_ok(K)) return QMM_ERR_OVERFLOW_BOUND;
-  *ws_bytes = 0;
+  *ws_bytes = int8_umma_workspace_bytes(M, K, N);
   return QMM_OK;
 }
 
@@ -86,9 +86,6 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
                          qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out,
                          int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
                          cudaStream_t stream) {
-  (void)workspace;
-  (void)ws_bytes;
-  (void)dev_status;
   if (A == nullptr || packedB == nullptr || col_sum == nullptr || ep == nullptr || out == nullptr)
     return QMM_ERR_INVALID_ARG;
   if (M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
@@ -133,6 +130,13 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
   a.epi.col_sum = col_sum;
   a.epi.out = out;
   a.epi.ldo = ldo;
+  if (int8_umma_eligible(M, K, N)) {
+    // tensor-core route: needs the caller's workspace (never a silent switch)
+    const size_t need = int8_umma_workspace_bytes(M, K, N);
+    if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256)) return QMM_ERR_WORKSPACE;
+    if ((M + 127) / 128 > INT32_MAX || (N + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;
+    return cuda_status(launch_int8_gemm_umma(a, workspace, dev_status, stream));
+  }
   if ((M + 31) / 32 > 65535) return QMM_ERR_UNSUPPORTED;
   return cuda_status(launch_int8_gemm_mma(a, stream));
 }
@@ -161,7 +165,6 @@ qmm_status qmm_pack_q4(const float* W, int64_t N, int64_t K, int64_t ldw, void* 
 qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, int64_t M,
                        int64_t ldx, float* Y, int64_t ldy, int32_t* dev_status,
                        cudaStream_t stream) {
-  (void)dev_status;
   if (tiles == nullptr || X == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
   if (N < 1 || K < 1 || M < 1 || ldx < K || ldy < N) return QMM_ERR_INVALID_ARG;
   if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
@@ -177,6 +180,10 @@ qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, i
   a.ldx = ldx;
   a.Y = Y;
   a.ldy = ldy;
+  if (q4_umma_eligible(M, N, K)) {
+    if ((M + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;
+    return cuda_status(launch_q4_gemm_umma(a, dev_status, stream));
+  }
   return cuda_status(launch_q4_gemv(a, stream));
 }
 

@@ -1,6 +1,7 @@
 // Host-side declarations shared between the C-ABI layer and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,6 +16,11 @@ constexpr int64_t kTileBytes = 5120;
 
 inline int64_t padded_k(int64_t K) { return (K + 63) / 64 * 64; }
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---- TMA descriptors (tmap.cu): 2-byte elements, 128-byte swizzle, box
+// box_inner x box_rows (box_inner * 2 == 128 bytes) ----
+bool make_tmap_2d(CUtensorMap* map, bool is_bf16_or_f16, void* base, uint64_t inner, uint64_t rows,
+                  uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
 
 // ---- packs (pack.cu) ----
 cudaError_t launch_pack_b_int8(const void* B, qmm_dtype b_type, int64_t K, int64_t N, int64_t ldb,

@@ -202,3 +202,70 @@ def test_workload_large_sampled(qmm, cuda):
     # the workload exercises rounding and both clamps
     assert (got == 127).mean() > 0.001 and (got == -128).mean() > 0.001
     assert np.array_equal(col_sum.cpu().numpy().astype(np.int64), c.B.numpy().astype(np.int64).sum(0))
+
+
+# ---------------------------------------------------------------------------
+# tensor-core route (M >= 256): same function, bit-exact
+# ---------------------------------------------------------------------------
+UMMA_SHAPES = [(256, 64, 256), (300, 1000, 300), (257, 4608, 130), (512, 2048, 520)]
+
+
+@pytest.mark.parametrize("a_type,b_type", [("u8", "s8"), ("s8", "u8"), ("u8", "f32")])
+@pytest.mark.parametrize("M,K,N", UMMA_SHAPES)
+def test_umma_route_s32_exact(qmm, cuda, a_type, b_type, M, K, N):
+    assert qmm.int8_gemm_workspace_size(M, K, N) > 0
+    g = torch.Generator().manual_seed(M + 7 * K + N)
+    A = rand_codes(g, a_type, (M, K))
+    B = torch.randn((K, N), generator=g) * 0.02 if b_type == "f32" else rand_codes(g, b_type, (K, N))
+    zA = 200 if a_type == "u8" else -90
+    zB = 0 if b_type == "f32" else 3
+    got, _ = gpu_gemm(qmm, cuda, A, a_type, zA, B, b_type, zB, "s32")
+    assert_same(got, oracle_out(A, a_type, zA, B, b_type, zB, "s32"), "s32")
+
+
+@pytest.mark.parametrize("out_type", ["f32", "s8", "u8"])
+def test_umma_route_epilogues_exact(qmm, cuda, out_type):
+    g = torch.Generator().manual_seed(21)
+    M, K, N = 384, 777, 260
+    A = rand_codes(g, "u8", (M, K))
+    B = rand_codes(g, "s8", (K, N))
+    bias = torch.randint(-50000, 50000, (N,), generator=g, dtype=torch.int32)
+    s_w = (torch.rand(N, generator=g) * 9e-3 + 1e-3).float()
+    s_x = (torch.rand(M, generator=g) * 0.02 + 0.01).float()
+    got, _ = gpu_gemm(qmm, cuda, A, "u8", 140, B, "s8", -6, out_type, bias=bias, s_x=s_x, s_x_stride=1,
+                      s_w=s_w, s_y=0.61, zp_y=5 if out_type != "f32" else 0)
+    ref = oracle_out(A, "u8", 140, B, "s8", -6, out_type, bias=bias, s_x=s_x.numpy(), s_w=s_w.numpy(),
+                     s_y=0.61, zp_y=5 if out_type != "f32" else 0)
+    assert_same(got, ref, out_type)
+
+
+@pytest.mark.parametrize("pattern", ["all_extreme", "mixed_magnitudes"])
+def test_umma_fp32_accumulation_is_exact(qmm, cuda, pattern):
+    """The tensor-core route carries the integer sum in fp32 chunks of 1024 K.
+    Adversarial operands: partial sums near 2^24 inside a chunk, mixed with
+    products of 1, so a dropped low bit anywhere shows up as a mismatch."""
+    M, K, N = 256, 4608, 256
+    if pattern == "all_extreme":
+        A = torch.zeros((M, K), dtype=torch.uint8)                  # A' = -128
+        B = torch.full((K, N), -128, dtype=torch.int8)
+        B[:, 1::3] = 127
+    else:
+        g = torch.Generator().manual_seed(5)
+        kk = torch.arange(K)
+        big = (kk % 16) < 8
+        A = torch.where(big, torch.zeros(K, dtype=torch.int64), 129 + (kk % 3)).repeat(M, 1)
+        A = (A + torch.randint(0, 2, (M, K), generator=g) * (~big).long()).to(torch.uint8)
+        B = torch.where(big[:, None], torch.full((K, N), -128), torch.randint(1, 3, (K, N), generator=g))
+        B = B.to(torch.int8)
+    got, _ = gpu_gemm(qmm, cuda, A, "u8", 128, B, "s8", 0, "s32")
+    assert_same(got, oracle_out(A, "u8", 128, B, "s8", 0, "s32"), "s32")
+
+
+def test_umma_route_needs_workspace(qmm, cuda):
+    M, K, N = 256, 128, 64
+    A = torch.zeros((M, K), dtype=torch.uint8, device=cuda)
+    packed, _, col_sum = qmm.pack_b_int8(torch.zeros((K, N), dtype=torch.int8, device=cuda), "s8")
+    with pytest.raises(qmm.QmmError) as e:
+        qmm.int8_gemm(A, "u8", 0, packed, col_sum, N, "s8", 0, "s32",
+                      workspace=torch.empty(16, dtype=torch.uint8, device=cuda))
+    assert e.value.status == qmm.QMM_ERR_WORKSPACE

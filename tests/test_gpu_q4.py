@@ -41,7 +41,8 @@ def test_q4_gemm_small_shapes(qmm, cuda, N, K, M):
     y, norm = O.q4_gemm(ref_tiles, N, K, xnp(X))
     err = O.normalized_error(Y, y, norm)
     assert err <= TOL, err
-    assert err <= 2e-5, f"error {err} far above the fp32 accumulation level"
+    if M < 48:   # decode kernel: weights never rounded, only fp32 accumulation error
+        assert err <= 2e-5, f"error {err} far above the fp32 accumulation level"
 
 
 def test_q4_special_weights(qmm, cuda):
