@@ -39,18 +39,94 @@ constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+// warp 0 TMA producer, warp 1 MMA issuer, warps 2..9 epilogue.  Ten warps put
+// three on some SM sub-partitions, which caps the kernel at 168 registers.
+constexpr int kEpiWarp0 = 2;
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kTmemCols = 512;       // two 256-column fp32 accumulators
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 8 * 128 * 12 + 256;
 constexpr int kMinM = 256;           // below this the legacy-MMA route is used
 
 struct Int8UmmaParams {
   int M, N, K, Kp;
+  int tiles_n;                       // number of 256-column tiles
+  int ntiles;
   const int32_t* row_sum;            // [M] (null when zB' == 0)
   Int8Epi epi;
   int32_t* dev_status;
 };
 
+constexpr int kColConstBytes = kEpiWarps * 128 * 12;   // per-warp c1 / s_w / Mq of 128 columns
+
+// Output conversion of one element (fp32 steps with explicit IEEE rounding).
+__device__ __forceinline__ uint32_t epi_convert(const Int8Epi& e, int32_t yb, float sx, float sw, float mq,
+                                                bool per_row_mq) {
+  const int ot = e.out_type;
+  if (ot == QMM_S32) return (uint32_t)yb;
+  if (ot == QMM_F32) return __float_as_uint(__fmul_rn(__fmul_rn(__int2float_rn(yb), sx), sw));
+  const float m = per_row_mq ? __fdiv_rn(__fmul_rn(sx, sw), e.s_y) : mq;
+  float r = __fmul_rn(__int2float_rn(yb), m);
+  r = fminf(fmaxf(r, -1.0e9f), 1.0e9f);
+  int q = __float2int_rn(r) + e.zp_y;
+  q = (ot == QMM_S8) ? min(max(q, -128), 127) : min(max(q, 0), 255);
+  return (uint32_t)q & 0xFFu;
+}
+
+// 32 consecutive columns of one row: converted and stored 16 bytes at a time
+// (element-wise at ragged edges or unaligned outputs).
+__device__ __forceinline__ void epi_store32(const Int8UmmaParams& p, int row, int nb, const int32_t* acc,
+                                            const uint32_t* c1, const float* sw, const float* mq, uint32_t r1,
+                                            float sx, bool per_row_mq, bool vec_ok) {
+  const Int8Epi& e = p.epi;
+  const bool full = vec_ok && nb + 32 <= p.N;
+  if (e.out_type == QMM_S32 || e.out_type == QMM_F32) {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(e.out) + (int64_t)row * e.ldo + nb;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = 4 * v + i;
+        o[i] = epi_convert(e, (int32_t)((uint32_t)acc[c] + c1[c] + r1), sx, sw[c], mq[c], per_row_mq);
+      }
+      if (full) {
+        reinterpret_cast<uint4*>(dst)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (nb + 4 * v + i < p.N) dst[4 * v + i] = o[i];
+      }
+    }
+  } else {
+    uint8_t* dst = reinterpret_cast<uint8_t*>(e.out) + (int64_t)row * e.ldo + nb;
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+      uint32_t w[4];
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int c = 16 * v + 4 * wi + b;
+          word |= epi_convert(e, (int32_t)((uint32_t)acc[c] + c1[c] + r1), sx, sw[c], mq[c], per_row_mq)
+                  << (8 * b);
+        }
+        w[wi] = word;
+      }
+      if (full) {
+        reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (nb + 16 * v + i < p.N) dst[16 * v + i] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
+      }
+    }
+  }
+}
+
+// Persistent: each CTA walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// The stage ring and the two TMEM accumulators carry on across tiles, so the
+// epilogue of one tile overlaps the MMAs of the next.
 __global__ void __launch_bounds__(kThreads, 1)
 int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const Int8UmmaParams p) {
@@ -58,7 +134,8 @@ int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint8_t* sConst = smem + kStages * kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sConst + kColConstBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;    // [2]
   uint64_t* tempty = tfull + 2;         // [2]
@@ -67,7 +144,6 @@ int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
   const int nkb = p.Kp / kBK;
   const int nchunks = (nkb + kChunkKB - 1) / kChunkKB;
 
@@ -97,88 +173,123 @@ int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kStages;
-        if (!mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag, p.dev_status)) break;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tma_load_2d(sA + s * kABytes, &tmA, &full[s], kb * kBK, m0);
-        tma_load_2d(sB + s * kBBytes, &tmB, &full[s], kb * kBK, n0);
-        issued = kb + 1;
+      int g = 0;          // k blocks issued so far (all tiles)
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+        const int m0 = (t / p.tiles_n) * kBM, n0 = (t % p.tiles_n) * kBN;
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+          const int s = g % kStages;
+          if (!mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tma_load_2d(sA + s * kABytes, &tmA, &full[s], kb * kBK, m0);
+          tma_load_2d(sB + s * kBBytes, &tmB, &full[s], kb * kBK, n0);
+        }
       }
-      if (*abort_flag) {
+      if (!ok) {
         // let the copies already issued land before the CTA leaves
-        for (int kb = issued > kStages ? issued - kStages : 0; kb < issued; ++kb)
-          mbar_try_wait(&full[kb % kStages], (kb / kStages) & 1) ||
-              mbar_wait(&full[kb % kStages], (kb / kStages) & 1, abort_flag, nullptr, 100000000ull);
+        for (int k = g > kStages ? g - kStages : 0; k < g; ++k)
+          mbar_try_wait(&full[k % kStages], (k / kStages) & 1) ||
+              mbar_wait(&full[k % kStages], (k / kStages) & 1, abort_flag, nullptr, 100000000ull);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(kBM, kBN, false);
-      int kb = 0;
+      int g = 0, gc = 0;  // k blocks consumed, chunks issued (all tiles)
       bool ok = true;
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int d = c & 1, u = c >> 1;
-        if (!mbar_wait(&tempty[d], (u & 1) ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
-        tc_fence_after();
-        const int kend = min(nkb, (c + 1) * kChunkKB);
-        for (; kb < kend; ++kb) {
-          const int s = kb % kStages;
-          if (!mbar_wait(&full[s], (kb / kStages) & 1, abort_flag, p.dev_status)) { ok = false; break; }
+      for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+        for (int c = 0; c < nchunks && ok; ++c, ++gc) {
+          const int d = gc & 1, u = gc >> 1;
+          if (!mbar_wait(&tempty[d], (u & 1) ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + s * kABytes);
-          const uint32_t b_addr = smem_u32(sB + s * kBBytes);
+          const int kend = min(nkb, (c + 1) * kChunkKB);
+          for (int kb = c * kChunkKB; kb < kend; ++kb, ++g) {
+            const int s = g % kStages;
+            if (!mbar_wait(&full[s], (g / kStages) & 1, abort_flag, p.dev_status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sA + s * kABytes);
+            const uint32_t b_addr = smem_u32(sB + s * kBBytes);
 #pragma unroll
-          for (int j = 0; j < kBK / 16; ++j)
-            umma_f16(tmem + d * 256, desc_kmajor_sw128(a_addr + 32 * j), desc_kmajor_sw128(b_addr + 32 * j),
-                     idesc, (kb > c * kChunkKB || j > 0) ? 1u : 0u);
-          umma_commit(&empty[s]);
+            for (int j = 0; j < kBK / 16; ++j)
+              umma_f16(tmem + d * 256, desc_kmajor_sw128(a_addr + 32 * j), desc_kmajor_sw128(b_addr + 32 * j),
+                       idesc, (kb > c * kChunkKB || j > 0) ? 1u : 0u);
+            umma_commit(&empty[s]);
+          }
+          if (ok) umma_commit(&tfull[d]);
         }
-        if (ok) umma_commit(&tfull[d]);
       }
       // every MMA has completed before TMEM is released
       umma_commit(done);
       mbar_wait(done, 0, abort_flag, p.dev_status);
     }
-  } else {
+  } else if (warp >= kEpiWarp0) {
     // epilogue: warp w reads TMEM lanes 32*(w%4).. and columns h*128..h*128+127
-    const int q = warp & 3, h = (warp - 2) >> 2;
-    const int row = m0 + 32 * q + lane;
-    int32_t acc[128];
+    const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
+    const int ew = warp - kEpiWarp0;
+    uint32_t* c1 = reinterpret_cast<uint32_t*>(sConst) + ew * 384;
+    float* swc = reinterpret_cast<float*>(c1 + 128);
+    float* mqc = reinterpret_cast<float*>(c1 + 256);
+    const Int8Epi& e = p.epi;
+    const bool requant = (e.out_type == QMM_S8 || e.out_type == QMM_U8);
+    const bool per_row_sx = (e.s_x != nullptr && e.s_x_stride != 0);
+    const float sx0 = e.s_x ? e.s_x[0] : 1.0f;
+    const int esz = (e.out_type == QMM_S32 || e.out_type == QMM_F32) ? 4 : 1;
+    const bool vec_ok = ((reinterpret_cast<uintptr_t>(e.out) & 15) == 0) && (((int64_t)e.ldo * esz) % 16 == 0);
+    int gc = 0;
     bool ok = true;
-    for (int c = 0; c < nchunks; ++c) {
-      const int d = c & 1, u = c >> 1;
-      // warp-uniform: tcgen05.ld below is a whole-warp instruction
-      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[d], u & 1, abort_flag, p.dev_status))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+    for (int t = blockIdx.x; t < p.ntiles && ok; t += gridDim.x) {
+      const int m0 = (t / p.tiles_n) * kBM, n0 = (t % p.tiles_n) * kBN;
+      const int nbase = n0 + h * 128;
+      // per-column constants of this warp's 128 columns: bias - zA' colSum, s_w, Mq
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * 256 + h * 128 + 32 * j), r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int32_t v = __float2int_rn(__uint_as_float(r[i]));
-          acc[32 * j + i] = (c == 0) ? v : (int32_t)((uint32_t)acc[32 * j + i] + (uint32_t)v);
+      for (int v = 0; v < 4; ++v) {
+        const int i = lane + 32 * v, n = nbase + i;
+        uint32_t cc = 0u;
+        float w = 1.0f, m = 0.0f;
+        if (n < p.N) {
+          cc = (uint32_t)(e.bias ? e.bias[n] : 0) - e.zAp * (uint32_t)e.col_sum[n];
+          w = e.s_w ? e.s_w[n] : 1.0f;
+          if (requant && !per_row_sx) m = __fdiv_rn(__fmul_rn(sx0, w), e.s_y);
         }
+        c1[i] = cc;
+        swc[i] = w;
+        mqc[i] = m;
       }
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[d]);
-    }
-    if (ok && row < p.M) {
-      const int32_t rs = p.row_sum ? p.row_sum[row] : 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int n = n0 + h * 128 + 32 * j + i;
-          if (n < p.N) int8_store(p.epi, row, n, zp_correct(acc[32 * j + i], p.epi.col_sum[n], rs, p.epi));
+      const int row = m0 + 32 * q + lane;
+      int32_t acc[128];
+      for (int c = 0; c < nchunks; ++c, ++gc) {
+        const int d = gc & 1, u = gc >> 1;
+        // warp-uniform: tcgen05.ld below is a whole-warp instruction
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[d], u & 1, abort_flag, p.dev_status))) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * 256 + h * 128 + 32 * j), r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int32_t v = __float2int_rn(__uint_as_float(r[i]));
+            acc[32 * j + i] = (c == 0) ? v : (int32_t)((uint32_t)acc[32 * j + i] + (uint32_t)v);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[d]);
+      }
+      if (ok && row < p.M) {
+        const uint32_t r1 = p.row_sum ? (0u - e.zBp * ((uint32_t)p.row_sum[row] - e.Kz)) : 0u;
+        const float sx = per_row_sx ? e.s_x[row] : sx0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          epi_store32(p, row, nbase + 32 * j, acc + 32 * j, c1 + 32 * j, swc + 32 * j, mqc + 32 * j, r1, sx,
+                      requant && per_row_sx, vec_ok);
+      }
+      __syncwarp();
     }
   }
   tc_fence_before();
@@ -285,12 +396,17 @@ cudaError_t launch_int8_gemm_umma(const Int8GemmArgs& a, void* workspace, int32_
   p.N = a.N;
   p.K = a.K;
   p.Kp = Kp;
+  p.tiles_n = (a.N + kBN - 1) / kBN;
+  p.ntiles = ((a.M + kBM - 1) / kBM) * p.tiles_n;
   p.row_sum = rs;
   p.epi = a.epi;
   p.dev_status = dev_status;
   err = cudaFuncSetAttribute(int8_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (err != cudaSuccess) return err;
-  dim3 grid((unsigned)((a.M + kBM - 1) / kBM), (unsigned)((a.N + kBN - 1) / kBN));
+  int dev = 0, sms = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+  const int grid = p.ntiles < sms ? p.ntiles : sms;
   int8_umma_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, p);
   return cudaGetLastError();
 }
