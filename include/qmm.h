@@ -158,9 +158,10 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
  *
  * The byte map inside a tile is this library's own, because the pages do not
  * print one:
- *   bytes [0, 4096)    codes: row r owns bytes [128 r, 128 r + 128) as 32
- *                      little-endian uint32 words; word 8 t + b (t = 0..3,
- *                      b = 0..7) holds the codes of columns 32 b + 8 t + j,
+ *   bytes [0, 4096)    codes: row r owns bytes [128 r, 128 r + 128); block b
+ *                      (columns 32 b .. 32 b + 31) is the 16 bytes at
+ *                      128 r + 16 b, as 4 little-endian uint32 words; word t
+ *                      (t = 0..3) holds the codes of columns 32 b + 8 t + j,
  *                      j = 0..7, with code j = 2i in bits [4i, 4i+4) and code
  *                      j = 2i+1 in bits [16+4i, 16+4i+4).
  *   bytes [4096, 5120) (scale, min) bf16 pairs: the pair of (row r, block b)

@@ -238,8 +238,9 @@ def pack_b_int8(B, b_type: str):
 # [N/32][K/256]; tile (tr, tc) covers rows 32*tr.., columns 256*tc..)
 #
 #   bytes [0, 4096): codes.  Row r (0..31) owns bytes [128 r, 128 r + 128) as
-#     32 little-endian uint32 words.  Word number 8*t + b (t = 0..3, b = 0..7)
-#     holds the 8 codes of block b at columns k = 32 b + 8 t + j, j = 0..7.
+#     8 blocks of 16 bytes: block b (columns 32 b .. 32 b + 31) sits at bytes
+#     [128 r + 16 b, 128 r + 16 b + 16) as 4 little-endian uint32 words; word
+#     t (t = 0..3) holds the codes of columns k = 32 b + 8 t + j, j = 0..7.
 #     Inside the word, code j = 2i sits in bits [4i, 4i+4) and code j = 2i+1
 #     in bits [16+4i, 16+4i+4), i = 0..3.
 #   bytes [4096, 5120): 256 (scale, min) pairs of bf16.  The pair of (row r,
@@ -290,8 +291,8 @@ def q4_tiles_from_blocks(q, s, m):
         i, hi = divmod(j, 2)
         shift = 4 * i + (16 if hi else 0)
         words |= qv[..., j].astype(np.uint64) << np.uint64(shift)
-    # word index within the row: 8 t + b
-    words = words.transpose(0, 2, 1, 4, 3)            # tr, tc, r, t, b
+    # word index within the row: 4 b + t
+    words = words.transpose(0, 2, 1, 3, 4)            # tr, tc, r, b, t
     wbytes = words.astype(np.uint32).reshape(TR, TC, TILE_ROWS * 32).view(np.uint8)
     out[:, :, :4096] = wbytes.reshape(TR, TC, 4096)
     sb = bf16_bits(s).reshape(TR, TILE_ROWS, TC, 8)   # tr, r, tc, b
@@ -312,15 +313,15 @@ def q4_blocks_from_tiles(tiles, N, K):
     """Read tile bytes back into (q [N][K], scale [N][K/32], min [N][K/32])."""
     TR, TC = N // TILE_ROWS, K // TILE_COLS
     t = np.asarray(tiles, dtype=np.uint8).reshape(TR, TC, TILE_BYTES)
-    words = t[:, :, :4096].copy().view(np.uint32).reshape(TR, TC, TILE_ROWS, 4, 8)  # tr tc r t b
-    q = np.zeros((TR, TC, TILE_ROWS, 4, 8, 8), dtype=np.int64)  # tr tc r t b j
+    words = t[:, :, :4096].copy().view(np.uint32).reshape(TR, TC, TILE_ROWS, 8, 4)  # tr tc r b t
+    q = np.zeros((TR, TC, TILE_ROWS, 8, 4, 8), dtype=np.int64)  # tr tc r b t j
     w64 = words.astype(np.uint64)
     for j in range(8):
         i, hi = divmod(j, 2)
         shift = 4 * i + (16 if hi else 0)
         q[..., j] = ((w64 >> np.uint64(shift)) & np.uint64(0xF)).astype(np.int64)
     # k within tile = 32 b + 8 t + j
-    q = q.transpose(0, 2, 1, 4, 3, 5).reshape(N, K)   # tr r tc b t j
+    q = q.transpose(0, 2, 1, 3, 4, 5).reshape(N, K)   # tr r tc b t j
     pairs = t[:, :, 4096:].copy().view(np.uint32).reshape(TR, TC, TILE_ROWS, 8)  # tr tc r b
     s = bf16_from_bits((pairs & 0xFFFF).astype(np.uint16))
     m = bf16_from_bits((pairs >> 16).astype(np.uint16))

@@ -184,7 +184,7 @@ qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, i
     if ((M + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;
     return cuda_status(launch_q4_gemm_umma(a, dev_status, stream));
   }
-  return cuda_status(launch_q4_gemv(a, stream));
+  return cuda_status(launch_q4_gemv(a, dev_status, stream));
 }
 
 qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64_t T,

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const Int8UmmaParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align(smem_raw, 1024);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
   uint8_t* sConst = smem + kStages * kStageBytes;

@@ -137,7 +137,7 @@ __global__ void pack_q4_kernel(const float* __restrict__ W, int N, int K, int64_
       const int sh = 4 * (j >> 1) + ((j & 1) ? 16 : 0);
       word |= (uint32_t)q << sh;
     }
-    *reinterpret_cast<uint32_t*>(tile + r * 128 + (8 * t + b) * 4) = word;
+    *reinterpret_cast<uint32_t*>(tile + r * 128 + 16 * b + 4 * t) = word;
   }
   const uint32_t pair =
       (uint32_t)__bfloat16_as_ushort(sb) | ((uint32_t)__bfloat16_as_ushort(mb) << 16);

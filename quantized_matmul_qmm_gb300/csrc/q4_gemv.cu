@@ -1,0 +1,248 @@
+// Decode GEMV for one activation row (M = 1), the weight-streaming case.
+//
+// At decode sizes the q4 path is bound by the weight stream ("Zaya 8B Q4NX on
+// the AMD NPU", round 25q: the access pattern, not the fabric, set the
+// decode wall).  Weights stay packed as 32x256 q4_1 tiles ("NPU engine: full
+// ELFs, no xclbin", "Q4NX chunks") and are read once, 16 bytes per load.
+//
+// Blocks as MMA columns.  For one output row r and one 32-column block b, the
+// factored form needs
+//     P[r][b] = sum_{e<32} (128 + q[r][b][e]) * x[b][e]
+// and then y[r] += s[r][b] * P[r][b] + (min[r][b] - 128 s[r][b]) * sum_e x[b][e].
+// One mma.sync m16n8k16 (bf16, fp32 accumulate) covers 16 rows and 8
+// columns.  Here the 8 columns are the 8 blocks of a tile, not 8 activation
+// rows.  Logical k = 2t'+u belongs to block t' and k = 2t'+8+u to block
+// t'+4 (u = 0,1); MMA i takes elements 2i+u.  The B operand holds x[b][.] in
+// column b and zeros elsewhere, so after 16 MMAs
+// D[r][b] = P[r][b] for 16 rows x 8 blocks.  Every MMA column is useful, and
+// each thread then applies the scale and min of exactly its own (row, block)
+// pairs.
+//
+// Thread (g, t) of a warp works on rows g and g+8 of a 16-row slab.  It
+// reads blocks t and t+4 of those rows (two 16-byte loads per row) and the
+// (scale, min) pairs of blocks 2t and 2t+1 (its D columns).  Lanes with
+// (g & 3) == t supply x of block g.
+#include "qmm_internal.h"
+
+namespace qmm {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kPF = 3;                // tiles prefetched per warp (in registers)
+constexpr int kCtasPerSm = 2;
+
+struct Gemv1Params {
+  const uint8_t* tiles;
+  int N, K;
+  const __nv_bfloat16* X;
+  float* Y;
+  int S;                              // warps sharing one slab (K split)
+};
+
+struct G1Tile {
+  uint4 c[2][2];                      // [row g / g+8][block t / t+4]: 4 code words each
+  uint2 p[2];                         // [row]: (scale, min) of blocks 2t, 2t+1
+};
+
+QMM_DEV uint2 ldg64(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+// Fragment data of thread (g, t) straight from the tile in global memory:
+// blocks t and t+4 of rows r0 and r0+8 (16 bytes each) and the pairs of
+// blocks 2t, 2t+1.  Plain 128-bit loads kept out of L1 stream the weights at
+// a higher rate on this part than cp.async or bulk copies into shared memory.
+QMM_DEV void g1_load(G1Tile& d, const uint8_t* tile, int r0, int t) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint8_t* row = tile + (r0 + 8 * h) * 128;
+    d.c[h][0] = ldg128_stream(row + 16 * t);
+    d.c[h][1] = ldg128_stream(row + 16 * (t + 4));
+    d.p[h] = ldg64(tile + 4096 + (r0 + 8 * h) * 32 + 8 * t);
+  }
+}
+
+// One tile: 16 MMAs in four independent accumulator chains, then the scales
+// of this thread's (row, block) pairs.  xsrc points at x of block g for the
+// lanes that carry it and at a zero block otherwise (same for xsrc_hi).
+QMM_DEV void g1_tile(const G1Tile& d, const __nv_bfloat16* xlo, const __nv_bfloat16* xhi, const float* xsum_tc,
+                     int t, float& y0, float& y1) {
+  uint32_t xa[16], xb[16];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 wa = reinterpret_cast<const uint4*>(xlo)[v];
+    const uint4 wb = reinterpret_cast<const uint4*>(xhi)[v];
+    xa[4 * v + 0] = wa.x; xa[4 * v + 1] = wa.y; xa[4 * v + 2] = wa.z; xa[4 * v + 3] = wa.w;
+    xb[4 * v + 0] = wb.x; xb[4 * v + 1] = wb.y; xb[4 * v + 2] = wb.z; xb[4 * v + 3] = wb.w;
+  }
+  float acc[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[c][e] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int w = i >> 2, pi = i & 3;
+    const uint32_t a0 = q4_pair_biased(u4_get(d.c[0][0], w), pi);   // row g,   block t
+    const uint32_t a1 = q4_pair_biased(u4_get(d.c[1][0], w), pi);   // row g+8, block t
+    const uint32_t a2 = q4_pair_biased(u4_get(d.c[0][1], w), pi);   // row g,   block t+4
+    const uint32_t a3 = q4_pair_biased(u4_get(d.c[1][1], w), pi);   // row g+8, block t+4
+    mma_bf16_16816(acc[i & 3], a0, a1, a2, a3, xa[i], xb[i]);
+  }
+  float r[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) r[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
+  // r: (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
+  const float2 xsv = *reinterpret_cast<const float2*>(xsum_tc + 2 * t);
+  const float s00 = bf16lo_to_f32(d.p[0].x), s01 = bf16lo_to_f32(d.p[0].y);
+  const float s10 = bf16lo_to_f32(d.p[1].x), s11 = bf16lo_to_f32(d.p[1].y);
+  y0 = fmaf(s00, r[0], fmaf(fmaf(-128.0f, s00, bf16hi_to_f32(d.p[0].x)), xsv.x, y0));
+  y0 = fmaf(s01, r[1], fmaf(fmaf(-128.0f, s01, bf16hi_to_f32(d.p[0].y)), xsv.y, y0));
+  y1 = fmaf(s10, r[2], fmaf(fmaf(-128.0f, s10, bf16hi_to_f32(d.p[1].x)), xsv.x, y1));
+  y1 = fmaf(s11, r[3], fmaf(fmaf(-128.0f, s11, bf16hi_to_f32(d.p[1].y)), xsv.y, y1));
+}
+
+// Item cursor of one warp: (group iteration, position inside the group),
+// advanced by increments so the hot loop does no division.
+struct G1Cursor {
+  int gi;       // group iteration (group = blockIdx.x + gi * gridDim.x)
+  int pos;      // item inside the group: tile column tc = ks + pos * S
+};
+
+// Persistent: CTA b takes slab groups b, b + gridDim.x, ...  A group is
+// kWarps / S slabs; the S warps of a slab split its tiles (tc = ks, ks + S,
+// ...), and their partial sums are added in a fixed order through shared
+// memory.  Each warp walks its (group, tile) items as one flat sequence, so
+// the prefetch runs across group boundaries.
+__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) q4_gemv1_kernel(const Gemv1Params p) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  const int TC = p.K / 256;
+  __nv_bfloat16* xs_sm = reinterpret_cast<__nv_bfloat16*>(sm);                 // [K] + 32 zeros
+  float* xsum = reinterpret_cast<float*>(sm + (size_t)p.K * 2 + 64);           // [K/32]
+  float* red = xsum + p.K / 32;                                                // [kWarps][32][2]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+
+  for (int i = threadIdx.x; i < p.K / 8; i += blockDim.x)
+    reinterpret_cast<uint4*>(xs_sm)[i] = reinterpret_cast<const uint4*>(p.X)[i];
+  if (threadIdx.x < 4) reinterpret_cast<uint4*>(xs_sm + p.K)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  for (int b = threadIdx.x; b < p.K / 32; b += blockDim.x) {
+    const uint4* xp = reinterpret_cast<const uint4*>(xs_sm + 32 * b);
+    float s = 0.f;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 w = xp[v];
+      s += bf16lo_to_f32(w.x) + bf16hi_to_f32(w.x) + bf16lo_to_f32(w.y) + bf16hi_to_f32(w.y) +
+           bf16lo_to_f32(w.z) + bf16hi_to_f32(w.z) + bf16lo_to_f32(w.w) + bf16hi_to_f32(w.w);
+    }
+    xsum[b] = s;
+  }
+  __syncthreads();
+
+  const int S = p.S;
+  const int slabs_per_group = kWarps / S;
+  const int nslabs = p.N / 16;
+  const int ngroups = (nslabs + slabs_per_group - 1) / slabs_per_group;
+  const int my_groups = (int)blockIdx.x < ngroups ? (ngroups - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int ks = warp % S;
+  const int per_warp = (TC - ks + S - 1) / S;        // tiles of one slab handled by this warp
+  const int per_slot = (TC + S - 1) / S;             // items per group (uniform across warps)
+  const int nitems = my_groups * per_slot;
+  const int slab0 = (int)blockIdx.x * slabs_per_group + warp / S;
+  const int slab_step = (int)gridDim.x * slabs_per_group;
+  // x source of this lane: block g of each tile if it carries x, else the zero block
+  const bool lo = (g == t), hi = (g == t + 4);
+  const __nv_bfloat16* zero = xs_sm + p.K;
+
+  G1Cursor ld{0, 0}, cu{0, 0};
+  auto load_next = [&](G1Tile& dst) {
+    if (ld.gi < my_groups) {
+      const int slab = slab0 + ld.gi * slab_step;
+      if (ld.pos < per_warp && slab < nslabs)
+        g1_load(dst, p.tiles + ((int64_t)(slab >> 1) * TC + ks + ld.pos * S) * kTileBytes, ((slab & 1) << 4) + g,
+                t);
+    }
+    if (++ld.pos == per_slot) { ld.pos = 0; ++ld.gi; }
+  };
+
+  G1Tile ring[kPF];
+#pragma unroll
+  for (int i = 0; i < kPF; ++i) load_next(ring[i]);
+  float y0 = 0.f, y1 = 0.f;
+  for (int j0 = 0; j0 < nitems; j0 += kPF) {
+#pragma unroll
+    for (int i = 0; i < kPF; ++i) {
+      if (j0 + i < nitems) {
+        const int slab = slab0 + cu.gi * slab_step;
+        if (cu.pos < per_warp && slab < nslabs) {
+          const int tc = ks + cu.pos * S;
+          const __nv_bfloat16* xt = xs_sm + tc * 256 + 32 * g;
+          g1_tile(ring[i], lo ? xt : zero, hi ? xt : zero, xsum + tc * 8, t, y0, y1);
+        }
+        load_next(ring[i]);
+        if (++cu.pos == per_slot) {
+          // end of this group: sum over the quad, then over the S warps of the slab
+          y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+          y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+          y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+          y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+          if (S == 1) {
+            if (t == 0 && slab < nslabs) {
+              p.Y[slab * 16 + g] = y0;
+              p.Y[slab * 16 + g + 8] = y1;
+            }
+          } else {
+            red[(warp * 32 + lane) * 2 + 0] = y0;
+            red[(warp * 32 + lane) * 2 + 1] = y1;
+            __syncthreads();
+            if (ks == 0 && t == 0 && slab < nslabs) {
+              float a = 0.f, b = 0.f;
+              for (int w = 0; w < S; ++w) {
+                a += red[((warp + w) * 32 + lane) * 2 + 0];
+                b += red[((warp + w) * 32 + lane) * 2 + 1];
+              }
+              p.Y[slab * 16 + g] = a;
+              p.Y[slab * 16 + g + 8] = b;
+            }
+            __syncthreads();
+          }
+          y0 = 0.f;
+          y1 = 0.f;
+          cu.pos = 0;
+          ++cu.gi;
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, cudaStream_t stream) {
+  Gemv1Params p{};
+  p.tiles = a.tiles;
+  p.N = a.N;
+  p.K = a.K;
+  p.X = a.X;
+  p.Y = a.Y;
+  const int TC = a.K / 256;
+  const int nslabs = a.N / 16;
+  // split K across warps while there are too few slab groups to fill the GPU
+  int S = 1;
+  while (S < kWarps && S * 2 <= TC && (nslabs * S) / kWarps < 4 * sms) S *= 2;
+  p.S = S;
+  const int groups = (nslabs + kWarps / S - 1) / (kWarps / S);
+  const int grid = groups < kCtasPerSm * sms ? groups : kCtasPerSm * sms;
+  const size_t smem = (size_t)a.K * 2 + 64 + (size_t)(a.K / 32) * 4 + (size_t)kWarps * 32 * 2 * 4;
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(q4_gemv1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  q4_gemv1_kernel<<<grid, kWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace qmm

@@ -43,15 +43,15 @@ template <int NG>
 __device__ __forceinline__ void q4_tile(const uint8_t* __restrict__ tile, int64_t kbase,
                                         const __nv_bfloat16* const (&xrow)[NG], Q4Acc<NG>& acc,
                                         int g, int t) {
-  // codes: rows g, g+8, g+16, g+24; words 8t .. 8t+7 (blocks b = 0..7)
-  uint4 cw[4][2];
+  // codes: rows g, g+8, g+16, g+24; word t of every block b (byte 16b + 4t of the row)
+  uint32_t cw[4][8];
   uint4 pw[4][2];
 #pragma unroll
   for (int rs = 0; rs < 4; ++rs) {
     const int r = g + 8 * rs;
-    const uint8_t* rowp = tile + r * 128 + t * 32;
-    cw[rs][0] = ldg128_stream(rowp);
-    cw[rs][1] = ldg128_stream(rowp + 16);
+    const uint8_t* rowp = tile + r * 128 + 4 * t;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) cw[rs][b] = ldg32(rowp + 16 * b);
     const uint8_t* pp = tile + 4096 + r * 32;
     pw[rs][0] = ldg128(pp);
     pw[rs][1] = ldg128(pp + 16);
@@ -73,8 +73,8 @@ __device__ __forceinline__ void q4_tile(const uint8_t* __restrict__ tile, int64_
     }
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-      const uint32_t wA = u4_get(cw[2 * mt][b >> 2], b & 3);
-      const uint32_t wB = u4_get(cw[2 * mt + 1][b >> 2], b & 3);
+      const uint32_t wA = cw[2 * mt][b];
+      const uint32_t wB = cw[2 * mt + 1][b];
       const uint32_t pA = u4_get(pw[2 * mt][b >> 2], b & 3);
       const uint32_t pB = u4_get(pw[2 * mt + 1][b >> 2], b & 3);
       const float sA = bf16lo_to_f32(pA), sB = bf16lo_to_f32(pB);
@@ -240,6 +240,181 @@ moe_route_kernel(const int32_t* __restrict__ ids, int64_t ld_ids, int n_used, in
   }
 }
 
+// ---------------------------------------------------------------------------
+// Decode GEMV (dense, M <= 16).  Each warp owns a 16-row slab of a tile row
+// and walks its K range with the code words and (scale, min) pairs prefetched
+// kPF tiles ahead in registers.  One quad thread loads the pairs of two
+// blocks, and the quad shares them by shuffles.  The block sums of x are
+// computed once per CTA into shared memory.  When N is small, S warps split
+// the K range of a slab, and their partial sums are added in a fixed order
+// through shared memory, so the result is deterministic.
+// ---------------------------------------------------------------------------
+constexpr int kGemvWarps = 8;
+constexpr int kPF = 3;
+
+struct Q4GemvParams {
+  const uint8_t* tiles;
+  int N, K, M;
+  const __nv_bfloat16* X;
+  int64_t ldx;
+  float* Y;
+  int64_t ldy;
+  int S;            // warps per slab (K split)
+};
+
+struct SlabTile {
+  uint32_t c[2][8]; // word t of blocks 0..7 of rows R0, R1
+  uint2 p[2];       // (scale, min) of blocks 2t, 2t+1 of rows R0, R1
+};
+
+__device__ __forceinline__ void slab_load(SlabTile& d, const uint8_t* tile, int r0, int t, bool valid) {
+  if (!valid) return;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint8_t* rowp = tile + (r0 + 8 * h) * 128 + 4 * t;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) d.c[h][b] = ldg32(rowp + 16 * b);
+    d.p[h] = *reinterpret_cast<const uint2*>(tile + 4096 + (r0 + 8 * h) * 32 + 8 * t);
+  }
+}
+
+// One block of 32 columns for the two rows of this thread: MMA on the biased
+// codes, then the block's scale and min.  kOneCol: only column 0 is real.
+template <int NG, bool kOneCol>
+__device__ __forceinline__ void gemv_block(const SlabTile& cur, int b, int lane, int t, int blk_x, const float* xs,
+                                           const __nv_bfloat16* const (&xrow)[NG], float (&y)[NG][4]) {
+  const int src = (lane & ~3) | (b >> 1);
+  const uint32_t pA = __shfl_sync(0xffffffffu, (b & 1) ? cur.p[0].y : cur.p[0].x, src);
+  const uint32_t pB = __shfl_sync(0xffffffffu, (b & 1) ? cur.p[1].y : cur.p[1].x, src);
+  const float sA = bf16lo_to_f32(pA), sB = bf16lo_to_f32(pB);
+  const float mA = fmaf(-128.0f, sA, bf16hi_to_f32(pA));
+  const float mB = fmaf(-128.0f, sB, bf16hi_to_f32(pB));
+  const uint32_t wA = cur.c[0][b];
+  const uint32_t wB = cur.c[1][b];
+  const uint32_t a00 = q4_pair_biased(wA, 0), a01 = q4_pair_biased(wB, 0);
+  const uint32_t a02 = q4_pair_biased(wA, 1), a03 = q4_pair_biased(wB, 1);
+  const uint32_t a10 = q4_pair_biased(wA, 2), a11 = q4_pair_biased(wB, 2);
+  const uint32_t a12 = q4_pair_biased(wA, 3), a13 = q4_pair_biased(wB, 3);
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng) {
+    const uint4 xv = xrow[ng] ? ldg128(xrow[ng] + blk_x + 8 * t) : make_uint4(0u, 0u, 0u, 0u);
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_bf16_16816(c, a00, a01, a02, a03, xv.x, xv.y);
+    mma_bf16_16816(c, a10, a11, a12, a13, xv.z, xv.w);
+    if (kOneCol) {
+      const float x0 = xs[0];
+      y[ng][0] = fmaf(sA, c[0], fmaf(mA, x0, y[ng][0]));
+      y[ng][2] = fmaf(sB, c[2], fmaf(mB, x0, y[ng][2]));
+    } else {
+      const float2 xsv = *reinterpret_cast<const float2*>(xs + 8 * ng + 2 * t);
+      y[ng][0] = fmaf(sA, c[0], fmaf(mA, xsv.x, y[ng][0]));
+      y[ng][1] = fmaf(sA, c[1], fmaf(mA, xsv.y, y[ng][1]));
+      y[ng][2] = fmaf(sB, c[2], fmaf(mB, xsv.x, y[ng][2]));
+      y[ng][3] = fmaf(sB, c[3], fmaf(mB, xsv.y, y[ng][3]));
+    }
+  }
+}
+
+template <int NG>
+__device__ __forceinline__ void gemv_xs_prologue(const Q4GemvParams& p, float* xs, int nblk) {
+  for (int idx = threadIdx.x; idx < nblk * 8 * NG; idx += blockDim.x) {
+    const int blk = idx / (8 * NG), col = idx % (8 * NG);
+    float sum = 0.f;
+    if (col < p.M) {
+      const uint4* xp = reinterpret_cast<const uint4*>(p.X + (int64_t)col * p.ldx + blk * 32);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 w = xp[v];
+        sum += bf16lo_to_f32(w.x) + bf16hi_to_f32(w.x) + bf16lo_to_f32(w.y) + bf16hi_to_f32(w.y) +
+               bf16lo_to_f32(w.z) + bf16hi_to_f32(w.z) + bf16lo_to_f32(w.w) + bf16hi_to_f32(w.w);
+      }
+    }
+    xs[idx] = sum;
+  }
+}
+
+template <int NG, bool kOneCol>
+__device__ __forceinline__ void gemv_store(const Q4GemvParams& p, const float (&y)[NG][4], int nrow0, int g, int t) {
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int m = 8 * ng + 2 * t + (c & 1);
+      const int n = nrow0 + g + 8 * (c >> 1);
+      if (m < p.M && (!kOneCol || (c & 1) == 0)) p.Y[(int64_t)m * p.ldy + n] = y[ng][c];
+    }
+}
+
+// K split across S warps of a CTA (small N).  Partial sums are added in a
+// fixed order through shared memory.
+template <int NG>
+__global__ void __launch_bounds__(kGemvWarps * 32) q4_gemv_kernel(const Q4GemvParams p) {
+  extern __shared__ float gsm[];
+  const int nblk = p.K / 32;
+  float* xs = gsm;                                   // [nblk][8*NG]
+  float* red = gsm + nblk * 8 * NG;                  // [warps][32][4*NG]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int TC = p.K / 256;
+  gemv_xs_prologue<NG>(p, xs, nblk);
+  __syncthreads();
+
+  const int slabs_per_cta = kGemvWarps / p.S;
+  const int slab = blockIdx.x * slabs_per_cta + warp / p.S;
+  const int ks = warp % p.S;
+  const int nrow0 = slab * 16;
+  float y[NG][4];
+#pragma unroll
+  for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) y[ng][c] = 0.f;
+
+  if (nrow0 < p.N) {
+    const int tr = nrow0 / 32, r0 = (nrow0 & 31) + g;
+    const uint8_t* rowtiles = p.tiles + (int64_t)tr * TC * kTileBytes;
+    const __nv_bfloat16* xrow[NG];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng) xrow[ng] = (8 * ng + g < p.M) ? p.X + (int64_t)(8 * ng + g) * p.ldx : nullptr;
+    SlabTile ring[kPF];
+#pragma unroll
+    for (int i = 0; i < kPF; ++i) {
+      const int tc = ks + i * p.S;
+      slab_load(ring[i], rowtiles + (int64_t)tc * kTileBytes, r0, t, tc < TC);
+    }
+    for (int it0 = 0; ks + it0 * p.S < TC; it0 += kPF) {
+#pragma unroll
+      for (int i = 0; i < kPF; ++i) {
+        const int tc = ks + (it0 + i) * p.S;
+        if (tc < TC) {
+#pragma unroll
+          for (int b = 0; b < 8; ++b)
+            gemv_block<NG, false>(ring[i], b, lane, t, tc * 256 + b * 32, xs + (tc * 8 + b) * 8 * NG, xrow, y);
+          const int tn = tc + kPF * p.S;
+          slab_load(ring[i], rowtiles + (int64_t)tn * kTileBytes, r0, t, tn < TC);
+        }
+      }
+    }
+  }
+  if (p.S > 1) {
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) red[(warp * 32 + lane) * 4 * NG + ng * 4 + c] = y[ng][c];
+    __syncthreads();
+    if (ks != 0) return;
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float s = 0.f;
+        for (int w = 0; w < p.S; ++w) s += red[((warp + w) * 32 + lane) * 4 * NG + ng * 4 + c];
+        y[ng][c] = s;
+      }
+  }
+  if (nrow0 >= p.N) return;
+  gemv_store<NG, false>(p, y, nrow0, g, t);
+}
+
 template <int NG, bool kMoE>
 cudaError_t launch_small(const Q4SmallParams& p, dim3 grid, int wk, cudaStream_t stream) {
   q4_small_kernel<NG, kMoE><<<grid, wk * 32, 0, stream>>>(p);
@@ -248,22 +423,43 @@ cudaError_t launch_small(const Q4SmallParams& p, dim3 grid, int wk, cudaStream_t
 
 }  // namespace
 
-cudaError_t launch_q4_gemv(const Q4DenseArgs& a, cudaStream_t stream) {
-  Q4SmallParams p{};
+template <typename Kern>
+cudaError_t launch_gemv_kernel(Kern kern, unsigned grid, size_t smem, const Q4GemvParams& p, cudaStream_t stream) {
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<grid, kGemvWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q4_gemv(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream) {
+  (void)dev_status;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (a.M == 1) return launch_q4_gemv1(a, sms, stream);
+  Q4GemvParams p{};
   p.tiles = a.tiles;
   p.N = a.N;
   p.K = a.K;
+  p.M = a.M;
   p.X = a.X;
-  p.ldx_token = a.ldx;
+  p.ldx = a.ldx;
   p.Y = a.Y;
-  p.ldy_token = a.ldy;
-  p.n_items = a.M;
-  p.n_used = 1;
+  p.ldy = a.ldy;
   const int TC = a.K / 256;
-  const int wk = TC < kMaxWarpsK ? TC : kMaxWarpsK;
-  dim3 grid((unsigned)(a.N / 32));
-  if (a.M <= 8) return launch_small<1, false>(p, grid, wk, stream);
-  return launch_small<2, false>(p, grid, wk, stream);
+  const int slabs = a.N / 16;
+  const int NG = a.M <= 8 ? 1 : 2;
+  const size_t xs_bytes = (size_t)(a.K / 32) * 8 * NG * sizeof(float);
+  // split K across the warps of a CTA until the grid fills the GPU
+  int S = 1;
+  while (S < kGemvWarps && S < TC && (slabs * S) / kGemvWarps < 2 * sms) S *= 2;
+  p.S = S;
+  const int slabs_per_cta = kGemvWarps / S;
+  const unsigned grid = (unsigned)((slabs + slabs_per_cta - 1) / slabs_per_cta);
+  const size_t smem = xs_bytes + (size_t)kGemvWarps * 32 * 4 * NG * sizeof(float);
+  if (NG == 1) return launch_gemv_kernel(q4_gemv_kernel<1>, grid, smem, p, stream);
+  return launch_gemv_kernel(q4_gemv_kernel<2>, grid, smem, p, stream);
 }
 
 size_t q4_moe_workspace_bytes(int64_t n_expert, int64_t n_used, int64_t T) {

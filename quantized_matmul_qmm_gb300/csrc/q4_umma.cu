@@ -38,7 +38,7 @@ constexpr int kThreads = 192;
 constexpr int kTmemCols = 256;
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kWBytes + kXBytes) + 256;
 constexpr int kPrefetch = 4;        // stages of raw weights in flight per transform thread
-constexpr int kMinM = 48;           // smaller M runs the decode kernel
+constexpr int kMinM = 17;           // M <= 16 runs the decode GEMV kernel
 
 struct Q4UmmaParams {
   const uint8_t* tiles;
@@ -49,22 +49,22 @@ struct Q4UmmaParams {
 };
 
 struct RawStage {
-  uint2 w[4];   // code words (blocks 2s, 2s+1) for t = 0..3
+  uint4 w[2];   // code words 0..3 of blocks 2s and 2s+1 (32 contiguous bytes of the row)
   uint2 p;      // (scale, min) pairs of blocks 2s, 2s+1
 };
 
 __device__ __forceinline__ void load_raw(RawStage& r, const uint8_t* row_tile0, const uint8_t* pair_tile0,
                                          int kb, bool valid) {
   if (!valid) {
-#pragma unroll
-    for (int t = 0; t < 4; ++t) r.w[t] = make_uint2(0u, 0u);
+    r.w[0] = make_uint4(0u, 0u, 0u, 0u);
+    r.w[1] = make_uint4(0u, 0u, 0u, 0u);
     r.p = make_uint2(0u, 0u);
     return;
   }
   const int tc = kb >> 2, s4 = kb & 3;
-  const uint8_t* base = row_tile0 + (int64_t)tc * kTileBytes + 8 * s4;
-#pragma unroll
-  for (int t = 0; t < 4; ++t) r.w[t] = *reinterpret_cast<const uint2*>(base + 32 * t);
+  const uint8_t* base = row_tile0 + (int64_t)tc * kTileBytes + 32 * s4;
+  r.w[0] = ldg128(base);
+  r.w[1] = ldg128(base + 16);
   r.p = *reinterpret_cast<const uint2*>(pair_tile0 + (int64_t)tc * kTileBytes + 8 * s4);
 }
 
@@ -87,7 +87,7 @@ __device__ __forceinline__ void write_stage(uint8_t* tile, int row, const RawSta
     const uint32_t m2 = __byte_perm(pair, 0, 0x3232);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const uint32_t word = bl ? r.w[t].y : r.w[t].x;
+      const uint32_t word = u4_get(r.w[bl], t);
       uint4 o;
       o.x = bf16x2_sub_fma(q4_pair_biased(word, 0), s2, m2);
       o.y = bf16x2_sub_fma(q4_pair_biased(word, 1), s2, m2);
@@ -102,7 +102,7 @@ __device__ __forceinline__ void write_stage(uint8_t* tile, int row, const RawSta
 __global__ void __launch_bounds__(kThreads, 1)
 q4_umma_kernel(const __grid_constant__ CUtensorMap tmX, const Q4UmmaParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align(smem_raw, 1024);
   uint8_t* sW = smem;
   uint8_t* sX = smem + kStages * kWBytes;
   uint64_t* xfull = reinterpret_cast<uint64_t*>(smem + kStages * (kWBytes + kXBytes));

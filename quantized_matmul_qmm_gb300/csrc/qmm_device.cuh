@@ -34,6 +34,12 @@ QMM_DEV uint4 ldg128_stream(const void* p) {
   return r;
 }
 
+QMM_DEV uint32_t ldg32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
 QMM_DEV uint32_t u4_get(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }

@@ -12,6 +12,14 @@ namespace umma {
 
 QMM_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// Align a dynamic shared-memory base with pointer arithmetic on the
+// __shared__ array itself, so the compiler keeps the shared address space
+// (and emits LDS/STS rather than generic loads and stores).
+QMM_DEV uint8_t* smem_align(uint8_t* raw, uint32_t align) {
+  const uint32_t base = smem_u32(raw);
+  return raw + (((base + align - 1u) & ~(align - 1u)) - base);
+}
+
 // ---- mbarrier ----------------------------------------------------------------
 QMM_DEV void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -41,7 +41,7 @@ def test_q4_gemm_small_shapes(qmm, cuda, N, K, M):
     y, norm = O.q4_gemm(ref_tiles, N, K, xnp(X))
     err = O.normalized_error(Y, y, norm)
     assert err <= TOL, err
-    if M < 48:   # decode kernel: weights never rounded, only fp32 accumulation error
+    if M <= 16:  # decode kernel: weights never rounded, only fp32 accumulation error
         assert err <= 2e-5, f"error {err} far above the fp32 accumulation level"
 
 
@@ -94,3 +94,16 @@ def test_workload_lm_head_sampled(qmm, cuda, M):
     y, norm = O.q4_gemm_rows(tiles, N, K, xnp(c.X), rows)
     err = O.normalized_error(Y[:, rows], y, norm)
     assert err <= TOL, err
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_q4_gemv_streaming_path_full(qmm, cuda, M):
+    # N large enough for the bulk-copy streaming GEMV (many tile rows per SM)
+    N, K = 10240, 512
+    g = torch.Generator().manual_seed(77 + M)
+    W = torch.randn((N, K), generator=g) * 0.02
+    X = torch.randn((M, K), generator=g).to(torch.bfloat16)
+    tiles, Y = gpu_q4(qmm, cuda, W, X)
+    y, norm = O.q4_gemm(tiles, N, K, xnp(X))
+    err = O.normalized_error(Y, y, norm)
+    assert err <= 2e-5, err

@@ -40,7 +40,7 @@ def scalar_tile_writer(q, s, m):
             i, hi = divmod(j, 2)
             bit = 4 * i + 16 * hi
             base = (tr * TC + tc) * 5120
-            word_off = base + r * 128 + (8 * t + b) * 4
+            word_off = base + r * 128 + 16 * b + 4 * t
             byte = word_off + bit // 8
             buf[byte] |= int(q[n, k]) << (bit % 8)
         for blk in range(K // 32):
