@@ -184,7 +184,7 @@ class HotPath:
             touched = int(torch.unique(m.ids_buf[:, :m.n_used]).numel())
             per = tiles.numel() // m.n_expert
             self.moe.append((kind, m, tiles, X, ids, Y, wsb))
-            self.calls.append((f"q4_moe_{kind}", self._moe(m, tiles, X, ids, Y, wsb), 2,
+            self.calls.append((f"q4_moe_{kind}", self._moe(m, tiles, X, ids, Y, wsb), self.moe_launches(m),
                                {"flops": 2 * m.T * m.n_used * m.N * m.K, "weight_bytes": touched * per,
                                 "bytes": touched * per + X.numel() * 2 + Y.numel() * 4}))
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -194,6 +194,11 @@ class HotPath:
         # tensor-core route: widen prepass + GEMM; legacy-MMA route: one kernel
         c = self.int8
         return 2 if self.q.int8_gemm_workspace_size(c.M, c.K, c.N) > 0 else 1
+
+    def moe_launches(self, m):
+        # the grouped kernel routes its own pairs up to 8192 (token, slot) pairs;
+        # beyond that a one-CTA router runs first
+        return 1 if m.T * m.n_used <= 8192 else 2
 
     def q4_launches(self, M):
         return 1

@@ -98,12 +98,14 @@ def test_workload_lm_head_sampled(qmm, cuda, M):
 
 @pytest.mark.parametrize("M", [1, 5, 16])
 def test_q4_gemv_streaming_path_full(qmm, cuda, M):
-    # N large enough for the bulk-copy streaming GEMV (many tile rows per SM)
+    # N large enough that every SM streams several tile rows
     N, K = 10240, 512
     g = torch.Generator().manual_seed(77 + M)
     W = torch.randn((N, K), generator=g) * 0.02
     X = torch.randn((M, K), generator=g).to(torch.bfloat16)
     tiles, Y = gpu_q4(qmm, cuda, W, X)
-    y, norm = O.q4_gemm(tiles, N, K, xnp(X))
+    ref_tiles = O.pack_q4(W.numpy())
+    assert np.array_equal(tiles, ref_tiles)
+    y, norm = O.q4_gemm(ref_tiles, N, K, xnp(X))
     err = O.normalized_error(Y, y, norm)
     assert err <= 2e-5, err

@@ -8,6 +8,7 @@ row give what the workspace entry point qmm_q4_gemm_id gives, and that
 requests beyond the array's limits are refused.  pytest collects this file
 last on purpose.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -38,10 +39,13 @@ def test_noalloc_matches_workspace_entry_point_twice(qmm, cuda):
         qmm.q4_gemm_id_noalloc(tiles, E, N, K, Xd, idsd, ld, n_used, T, Y_na, dev_status=status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        _, norm = O.q4_gemm_id(tiles.cpu().numpy(), E, N, K, X.float().double().numpy(), shared,
+        ref_tiles = np.concatenate([O.pack_q4(W[e].numpy()) for e in range(E)])
+        assert np.array_equal(tiles.cpu().numpy(), ref_tiles)
+        y, norm = O.q4_gemm_id(ref_tiles, E, N, K, X.float().double().numpy(), shared,
                                ids.numpy(), ld, n_used, T)
         err = O.normalized_error(Y_na.cpu().numpy(), Y_ref.cpu().numpy(), norm)
         assert err <= TOL, err
+        assert O.normalized_error(Y_na.cpu().numpy(), y, norm) <= TOL
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(qmm, cuda):
