@@ -179,7 +179,7 @@ class HotPath:
             X = m.X.to(dev)
             ids = m.ids_buf.to(dev)
             Y = torch.empty((m.T, m.n_used, m.N), dtype=torch.float32, device=dev)
-            wsb = torch.empty(q.q4_gemm_id_workspace_size(m.n_expert, m.n_used, m.T),
+            wsb = torch.empty(q.q4_gemm_id_workspace_size(m.n_expert, m.n_used, m.T, m.K),
                               dtype=torch.uint8, device=dev)
             touched = int(torch.unique(m.ids_buf[:, :m.n_used]).numel())
             per = tiles.numel() // m.n_expert
@@ -196,9 +196,9 @@ class HotPath:
         return 2 if self.q.int8_gemm_workspace_size(c.M, c.K, c.N) > 0 else 1
 
     def moe_launches(self, m):
-        # the grouped kernel routes its own pairs up to 8192 (token, slot) pairs;
-        # beyond that a one-CTA router runs first
-        return 1 if m.T * m.n_used <= 8192 else 2
+        # up to 224 (token, slot) pairs the grouped kernel routes its own pairs;
+        # beyond that the router and the activation packing run first
+        return 1 if m.T * m.n_used <= 224 else 3
 
     def q4_launches(self, M):
         return 1

@@ -196,8 +196,10 @@ qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, i
                        cudaStream_t stream);
 
 /* Workspace of qmm_q4_gemm_id: routing tables for n_expert experts and
- * T*n_used (token, slot) pairs. */
-qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64_t T,
+ * P = T*n_used (token, slot) pairs (int32 offsets [n_expert+1] and pair ids
+ * [P], each padded to 256 bytes), followed by the pairs' activation rows
+ * packed in expert order (bf16 [P][K]). */
+qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64_t T, int64_t K,
                                          size_t* ws_bytes);
 
 /* MUL_MAT_ID over q4 experts ("Zaya 8B Q4NX on the AMD NPU": the new
@@ -213,8 +215,12 @@ qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64
  * ids       int32, a STRIDED view: the expert of (t, i) is ids[t*ld_ids + i]
  *           (ld_ids >= n_used, e.g. 17 for the top-8 of 17 sorted ids).
  * Y         fp32; row (t, i) starts at element t*ldy_token + i*ldy_slot.
- * workspace device scratch of qmm_q4_gemm_id_workspace_size bytes (256-byte
- *           aligned), rewritten on every call.
+ * workspace device scratch (256-byte aligned), rewritten on every call.
+ *           qmm_q4_gemm_id_workspace_size bytes run the fastest path, which
+ *           packs the activation rows in expert order.  A workspace that holds
+ *           only the routing tables runs a path that gathers the rows inside
+ *           the grouped kernel (same results); anything smaller returns
+ *           QMM_ERR_WORKSPACE.
  * Y[t][i][n] = sum_k x(t,i)[k] * w_{ids(t,i)}[n][k].  A pair whose id is
  * outside [0, n_expert) is skipped (its output row is left untouched) and
  * dev_status gets QMM_ERR_BAD_EXPERT_ID.

@@ -187,11 +187,12 @@ qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, i
   return cuda_status(launch_q4_gemv(a, dev_status, stream));
 }
 
-qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64_t T,
+qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64_t T, int64_t K,
                                          size_t* ws_bytes) {
-  if (ws_bytes == nullptr || n_expert < 1 || n_used < 1 || T < 1) return QMM_ERR_INVALID_ARG;
+  if (ws_bytes == nullptr || n_expert < 1 || n_used < 1 || T < 1 || K < 1) return QMM_ERR_INVALID_ARG;
+  if (K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
   if (n_expert > kMaxExperts || T * n_used > INT32_MAX) return QMM_ERR_UNSUPPORTED;
-  *ws_bytes = q4_moe_workspace_bytes(n_expert, n_used, T);
+  *ws_bytes = q4_moe_workspace_bytes(n_expert, n_used, T, K);
   return QMM_OK;
 }
 
@@ -213,8 +214,11 @@ qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_
   if (!(ldy_slot >= N && ldy_token >= ldy_slot * n_used)) return QMM_ERR_INVALID_ARG;
   if (!aligned(X, 16) || !aligned(tiles, 16) || !aligned(Y, 4) || !aligned(ids, 4))
     return QMM_ERR_INVALID_ARG;
-  const size_t need = q4_moe_workspace_bytes(n_expert, n_used, T);
-  if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256)) return QMM_ERR_WORKSPACE;
+  // The routing tables are the minimum; the full size adds the packed
+  // activations, which the fast path needs.
+  const size_t tables = q4_moe_table_bytes(n_expert, n_used, T);
+  if (workspace == nullptr || ws_bytes < tables || !aligned(workspace, 256)) return QMM_ERR_WORKSPACE;
+  const bool packed = ws_bytes >= q4_moe_workspace_bytes(n_expert, n_used, T, K);
   Q4MoEArgs a{};
   a.tiles = static_cast<const uint8_t*>(tiles);
   a.n_expert = (int)n_expert;
@@ -233,6 +237,7 @@ qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_
   char* ws = static_cast<char*>(workspace);
   a.offsets = reinterpret_cast<int32_t*>(ws);
   a.pairs = reinterpret_cast<int32_t*>(ws + (((size_t)(n_expert + 1) * 4 + 255) / 256 * 256));
+  a.xperm = packed ? reinterpret_cast<__nv_bfloat16*>(ws + tables) : nullptr;
   a.dev_status = dev_status;
   return cuda_status(launch_q4_moe(a, stream));
 }

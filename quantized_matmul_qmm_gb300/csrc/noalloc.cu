@@ -21,6 +21,7 @@ constexpr int64_t kNoAllocMaxExperts = 1024;
 constexpr int64_t kNoAllocMaxPairs = 65536;   // T * n_used
 constexpr size_t kOffsetsBytes = ((kNoAllocMaxExperts + 1) * 4 + 255) / 256 * 256;
 constexpr size_t kScratchBytes = kOffsetsBytes + (size_t)kNoAllocMaxPairs * 4;  // 266,496 bytes
+static_assert(kScratchBytes % 256 == 0, "pair table padding");
 
 // The routing scratch.  Host code must not pass this symbol to a kernel: on
 // the host it names a stand-in, not device memory.  The device address comes

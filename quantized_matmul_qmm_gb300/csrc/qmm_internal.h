@@ -22,6 +22,11 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 bool make_tmap_2d(CUtensorMap* map, bool is_bf16_or_f16, void* base, uint64_t inner, uint64_t rows,
                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
 
+// q4 tiles as a 3-D byte tensor {128 bytes, 40 rows, n_tiles}, 128-byte
+// swizzle, box {128, box_rows, 1}: rows 0..31 of a tile are its codes, rows
+// 32..39 its (scale, min) pairs.
+bool make_tmap_q4_tiles(CUtensorMap* map, const void* tiles, uint64_t n_tiles, uint32_t box_rows);
+
 // ---- packs (pack.cu) ----
 cudaError_t launch_pack_b_int8(const void* B, qmm_dtype b_type, int64_t K, int64_t N, int64_t ldb,
                                int8_t* packed, int64_t Kp, float* col_scale, int32_t* col_sum,
@@ -74,10 +79,14 @@ struct Q4MoEArgs {
   int64_t ldy_token, ldy_slot;
   int32_t* offsets;   // workspace: [n_expert + 1]
   int32_t* pairs;     // workspace: [T * n_used]
+  __nv_bfloat16* xperm;   // workspace: [T * n_used][K] packed activations, or null
   int32_t* dev_status;
 };
 constexpr int64_t kMaxExperts = 4096;
-size_t q4_moe_workspace_bytes(int64_t n_expert, int64_t n_used, int64_t T);
+// routing tables only (enough for the gather path)
+size_t q4_moe_table_bytes(int64_t n_expert, int64_t n_used, int64_t T);
+// tables + packed activations (the full workspace)
+size_t q4_moe_workspace_bytes(int64_t n_expert, int64_t n_used, int64_t T, int64_t K);
 cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream);
 
 }  // namespace qmm

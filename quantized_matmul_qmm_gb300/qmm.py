@@ -44,7 +44,7 @@ SIGNATURES = {
     "qmm_pack_q4_size": (_c.c_int, [_i64, _i64, _szp]),
     "qmm_pack_q4": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "qmm_q4_gemm": (_c.c_int, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
-    "qmm_q4_gemm_id_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
+    "qmm_q4_gemm_id_workspace_size": (_c.c_int, [_i64, _i64, _i64, _i64, _szp]),
     "qmm_q4_gemm_id": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64, _i64,
                                   _vp, _i64, _i64, _vp, _sz, _vp, _vp]),
     "qmm_q4_gemm_id_noalloc": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
@@ -171,8 +171,8 @@ def q4_gemm(tiles: torch.Tensor, N: int, K: int, X: torch.Tensor, Y=None, dev_st
     return Y
 
 
-def q4_gemm_id_workspace_size(n_expert: int, n_used: int, T: int) -> int:
-    return _size("qmm_q4_gemm_id_workspace_size", n_expert, n_used, T)
+def q4_gemm_id_workspace_size(n_expert: int, n_used: int, T: int, K: int) -> int:
+    return _size("qmm_q4_gemm_id_workspace_size", n_expert, n_used, T, K)
 
 
 def q4_gemm_id(tiles: torch.Tensor, n_expert: int, N: int, K: int, X: torch.Tensor,
@@ -187,7 +187,7 @@ def q4_gemm_id(tiles: torch.Tensor, n_expert: int, N: int, K: int, X: torch.Tens
     if Y is None:
         Y = torch.empty((T, n_used, N), dtype=torch.float32, device=X.device)
     if workspace is None:
-        workspace = torch.empty(q4_gemm_id_workspace_size(n_expert, n_used, T), dtype=torch.uint8,
+        workspace = torch.empty(q4_gemm_id_workspace_size(n_expert, n_used, T, K), dtype=torch.uint8,
                                 device=X.device)
     _check("qmm_q4_gemm_id", lib.qmm_q4_gemm_id(
         _ptr(tiles), n_expert, N, K, _ptr(X), ldx_token, ldx_slot, _ptr(ids), ld_ids, n_used, T,

@@ -37,6 +37,11 @@ def test_size_queries(qmm):
     assert qmm.pack_q4_size(32, 256) == 5120
     assert qmm.pack_q4_size(151936, 1024) == 97239040
     assert qmm.int8_gemm_workspace_size(16, 1024, 1024) >= 0
+    # MUL_MAT_ID: routing tables (256-byte padded) + packed bf16 activation rows
+    assert qmm.q4_gemm_id_workspace_size(128, 8, 512, 2048) == 768 + 16384 + 4096 * 2048 * 2
+    L = qmm.lib
+    sz = ctypes.c_size_t(0)
+    assert L.qmm_q4_gemm_id_workspace_size(128, 8, 512, 300, ctypes.byref(sz)) == qmm.QMM_ERR_UNSUPPORTED
 
 
 def test_overflow_bound_rejected(qmm):

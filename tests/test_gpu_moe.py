@@ -10,13 +10,21 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-3
 
 
-def run_moe(qmm, dev, W, X, ids_buf, ld_ids, n_used, T, status=None):
+def table_bytes(E, n_used, T):
+    """Routing tables alone: offsets [E+1] and pair ids [T*n_used], int32,
+    each padded to 256 bytes (the documented workspace layout)."""
+    pad = lambda b: (b + 255) // 256 * 256
+    return pad((E + 1) * 4) + pad(T * n_used * 4)
+
+
+def run_moe(qmm, dev, W, X, ids_buf, ld_ids, n_used, T, status=None, ws_bytes=None):
     E, N, K = W.shape
     tiles = torch.cat([qmm.pack_q4(W[e].to(dev)) for e in range(E)])
     full = torch.full((T, n_used, N + 4), float("nan"), dtype=torch.float32, device=dev)
     Y = full[:, :, :N]
+    ws = None if ws_bytes is None else torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     qmm.q4_gemm_id(tiles, E, N, K, X.to(dev), ids_buf.to(dev), ld_ids, n_used, T, Y=Y,
-                   dev_status=status)
+                   workspace=ws, dev_status=status)
     torch.cuda.synchronize()
     f = full.cpu()
     assert torch.isnan(f[:, :, N:]).all(), "canary overwritten"
@@ -56,9 +64,11 @@ def test_moe_contiguous_read_would_differ(qmm, cuda):
     assert O.normalized_error(Y, y_wrong, norm) > 0.01
 
 
-def test_moe_bad_id_sets_status(qmm, cuda):
+@pytest.mark.parametrize("T", [6, 150])
+def test_moe_bad_id_sets_status(qmm, cuda, T):
+    # T=6: the grouped kernel routes in-CTA; T=150: router + packed activations
     g = torch.Generator().manual_seed(6)
-    E, N, K, T, n_used, ld = 4, 32, 256, 6, 2, 3
+    E, N, K, n_used, ld = 4, 32, 256, 2, 3
     W = torch.randn((E, N, K), generator=g) * 0.02
     ids = torch.randint(0, E, (T, ld), generator=g, dtype=torch.int32)
     ids[2, 1] = E          # out of range
@@ -135,6 +145,20 @@ def test_workload_moe_full(qmm, cuda, kind):
     oracle."""
     c = I.moe_case(kind)
     tiles, Y = run_moe(qmm, cuda, c.W, c.X, c.ids_buf, c.ld_ids, c.n_used, c.T)
+    y, norm = O.q4_gemm_id(tiles, c.n_expert, c.N, c.K, c.X.float().double().numpy(), c.shared_src1,
+                           c.ids_buf.numpy(), c.ld_ids, c.n_used, c.T)
+    assert O.normalized_error(Y, y, norm) <= TOL
+
+
+@pytest.mark.parametrize("kind", ["gate", "down"])
+def test_workload_moe_tables_only_workspace(qmm, cuda, kind):
+    """A workspace holding only the routing tables runs the in-kernel gather
+    of the activation rows; every pair against the oracle."""
+    c = I.moe_case(kind)
+    full = qmm.q4_gemm_id_workspace_size(c.n_expert, c.n_used, c.T, c.K)
+    tb = table_bytes(c.n_expert, c.n_used, c.T)
+    assert full == tb + c.T * c.n_used * c.K * 2
+    tiles, Y = run_moe(qmm, cuda, c.W, c.X, c.ids_buf, c.ld_ids, c.n_used, c.T, ws_bytes=tb)
     y, norm = O.q4_gemm_id(tiles, c.n_expert, c.N, c.K, c.X.float().double().numpy(), c.shared_src1,
                            c.ids_buf.numpy(), c.ld_ids, c.n_used, c.T)
     assert O.normalized_error(Y, y, norm) <= TOL
