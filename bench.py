@@ -196,9 +196,8 @@ class HotPath:
         return 2 if self.q.int8_gemm_workspace_size(c.M, c.K, c.N) > 0 else 1
 
     def moe_launches(self, m):
-        # up to 224 (token, slot) pairs the grouped kernel routes its own pairs;
-        # beyond that the router and the activation packing run first
-        return 1 if m.T * m.n_used <= 224 else 3
+        # route-and-pack, then the grouped kernel
+        return 2
 
     def q4_launches(self, M):
         return 1

@@ -4,21 +4,24 @@
 // per-slot src1 row).  Weights are 32x256 q4_1 tiles, w = q * scale + min
 // ("NPU engine: full ELFs, no xclbin", "Q4NX chunks").
 //
-// One CTA owns 128 weight rows of one expert and every (token, slot) pair
-// routed to that expert, up to 64 pairs per pass.  Each weight is read from
-// HBM once per pass and used for all of the pass's pairs: the grouped
-// dispatch the pages credit for the MoE speed-up.
+// Work is cut into units of 128 weight rows of one expert; a unit's jobs are
+// its expert's (token, slot) pairs, up to 64 per job.  Each weight is read
+// from HBM once per job and used for all of the job's pairs: the grouped
+// dispatch the pages credit for the MoE speed-up.  The grid is persistent
+// (two CTAs per SM); every role walks the CTA's units in the same order, and
+// the pipelines run on across unit boundaries, so the next unit's weights
+// stream in while the current one finishes.  The fp32 accumulator is double
+// buffered in TMEM, so a job's epilogue overlaps the next job's MMAs.
 //
-// Routing.  A one-CTA router writes per-expert offsets and the grouped
-// (token, slot) list into the caller's workspace.  For decode-sized calls
-// (T * n_used no more than one pair per thread) each CTA instead scans the
-// ids itself, in pair order.
+// Routing.  A route-and-pack kernel (one block per 8 pairs) writes per-expert
+// offsets and the grouped (token, slot) list into the caller's workspace, in
+// pair order inside each expert.  The grouped kernel is launched as its
+// programmatic dependent, so it starts while routing still runs.
 //
-// Activations.  With a full workspace, a copy kernel first packs the rows of
-// src1 in expert order, so that every CTA's B operand is a dense block that
-// TMA loads whole.  With only the routing tables (the no-allocation entry
-// point) or after the in-CTA scan, a loader warp gathers the rows itself with
-// cp.async.
+// Activations.  With a full workspace, the route-and-pack kernel also packs
+// the rows of src1 in expert order, so that every job's B operand is a dense
+// block that TMA loads whole.  With only the routing tables (the
+// no-allocation entry point) a loader warp gathers the rows with cp.async.
 //
 // The contraction runs on the 5th-generation tensor cores with the weights as
 // the M = 128 side and the pairs as N (16..64).  The dequantised weights go
@@ -31,7 +34,7 @@
 //   warps 0-3  transform, one weight row per lane (TMEM lane = row): read the
 //              row's codes and pairs, w = bf16(q * s + m) with one rounding,
 //              tcgen05.st of 128 k at a time into one of two TMEM A buffers.
-//              After the last stage they drain the fp32 accumulator into Y.
+//              After each job's last stage they drain its accumulator into Y.
 //   warp 4     activation loader: TMA of the packed rows, or a cp.async
 //              gather, into the 128-byte-swizzle K-major layout (3-stage
 //              ring).
@@ -49,8 +52,8 @@ namespace {
 using namespace umma;
 
 constexpr int kThreads = 224;
-constexpr int kRows = 128;                          // weight rows per CTA (MMA M)
-constexpr int kTok = 64;                            // pairs per pass (largest MMA N)
+constexpr int kRows = 128;                          // weight rows per unit (MMA M)
+constexpr int kTok = 64;                            // pairs per job (largest MMA N)
 constexpr int kKC = 128;                            // K per MMA / activation stage
 constexpr int kRawStages = 3;                       // weight ring, one tile column (256 k) per stage
 constexpr int kBStages = 3;
@@ -61,15 +64,14 @@ constexpr int kRawBytes = 4 * (kCodeBox + kPairBox);   // 4 tile rows: codes [4]
 constexpr int kBAtomBytes = kTok * 128;             // 64 rows x 64 k bf16, 128-byte swizzle
 constexpr int kBBytes = 2 * kBAtomBytes;            // 128 k per stage
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColD = 0;                       // accumulator: columns [0, 64)
-constexpr uint32_t kColA = 64;                      // A buffer s: columns [64 + 64 s, 128 + 64 s)
-constexpr int kLoaderLag = 2;                       // activation stages in flight before signalling
+constexpr uint32_t kColD = 0;                       // accumulator j: columns [64 j, 64 j + 64)
+constexpr uint32_t kColA = 128;                     // A buffer s: columns [128 + 64 s, 192 + 64 s)
+constexpr int kLoaderLag = 2;                       // gathered activation stages in flight before signalling
 constexpr size_t kSmemBytes = 1024 + (size_t)kBStages * kBBytes + (size_t)kRawStages * kRawBytes + 256;
-constexpr int kScanMaxPairs = kThreads;             // in-CTA scan: one id per thread
 constexpr int kXBox = 16;                           // packed activations: TMA box rows
 
-// Routing and activation source of one launch.
-enum MoeMode { kScanGather = 0, kTableGather = 1, kTablePacked = 2 };
+// Activation source of one launch.
+enum MoeMode { kTableGather = 0, kTablePacked = 1 };
 
 // mbarrier block after the two rings
 constexpr int kBarWFull = 0;
@@ -79,7 +81,8 @@ constexpr int kBarAEmpty = kBarAFull + kAStages;
 constexpr int kBarBFull = kBarAEmpty + kAStages;
 constexpr int kBarBEmpty = kBarBFull + kBStages;
 constexpr int kBarDFull = kBarBEmpty + kBStages;
-constexpr int kBarDone = kBarDFull + 1;
+constexpr int kBarDEmpty = kBarDFull + 2;
+constexpr int kBarDone = kBarDEmpty + 2;
 constexpr int kNumBars = kBarDone + 1;
 static_assert(kNumBars * 8 + 8 <= 256, "barrier block");
 
@@ -88,13 +91,12 @@ struct MoeParams {
   int N, K;
   const __nv_bfloat16* X;
   int64_t ldx_token, ldx_slot;
-  const int32_t* ids;
-  int64_t ld_ids;
-  int n_used, T, n_expert;
+  int n_used, n_expert, npairs;
+  int n_units, nrb;         // units = experts x 128-row blocks, unit u = e * nrb + row block
   float* Y;
   int64_t ldy_token, ldy_slot;
-  const int32_t* offsets;   // router mode only
-  const int32_t* pairs;     // router mode only
+  const int32_t* offsets;   // [n_expert + 1]
+  const int32_t* pairs;     // grouped (token, slot) ids
   int32_t* dev_status;
 };
 
@@ -109,36 +111,36 @@ __device__ __forceinline__ uint32_t dequant2(uint32_t q2_biased, uint32_t s2, ui
   return *reinterpret_cast<const uint32_t*>(&w);
 }
 
-// Exclusive prefix of `v` over the CTA; `total` gets the sum.
-__device__ __forceinline__ int cta_exclusive_scan(int v, int* wsum, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += u;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  int before = 0;
-  total = 0;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) {
-    const int s = wsum[w];
-    before += (w < warp) ? s : 0;
-    total += s;
-  }
-  __syncthreads();
-  return before + incl - v;
-}
-
 __device__ __forceinline__ void pair_offsets(const MoeParams& p, int pr, int64_t& xo, int64_t& yo) {
   const int tok = pr / p.n_used, slot = pr % p.n_used;
   xo = (int64_t)tok * p.ldx_token + (int64_t)slot * p.ldx_slot;
   yo = (int64_t)tok * p.ldy_token + (int64_t)slot * p.ldy_slot;
 }
 
-// One weight stage: the CTA's (up to) 4 tiles of tile column tc.
+// The CTA's jobs, in the same order for every role: units blockIdx.x,
+// blockIdx.x + gridDim.x, ...; each unit's pairs in passes of up to kTok.
+// Units without pairs are skipped.
+struct Jobs {
+  int u, e, n0, first, total, pass0;
+  __device__ Jobs() : u((int)blockIdx.x - (int)gridDim.x), e(0), n0(0), first(0), total(0), pass0(0) {}
+  __device__ bool next(const MoeParams& p) {
+    pass0 += kTok;
+    while (pass0 >= total) {
+      u += gridDim.x;
+      if (u >= p.n_units) return false;
+      e = u / p.nrb;
+      n0 = (u - e * p.nrb) * kRows;
+      first = p.offsets[e];
+      total = p.offsets[e + 1] - first;
+      pass0 = 0;
+    }
+    return true;
+  }
+  __device__ int nt() const { return min(kTok, total - pass0); }
+  __device__ int ncol() const { return (nt() + 15) & ~15; }
+};
+
+// One weight stage: the unit's (up to) 4 tiles of tile column tc.
 __device__ __forceinline__ bool produce_weights(const CUtensorMap* tmC, const CUtensorMap* tmP, const MoeParams& p,
                                                 int e, int n0, int tc, int gws, uint32_t raw0, uint64_t* w_full,
                                                 uint64_t* w_empty, volatile int* abort_flag) {
@@ -162,11 +164,10 @@ template <int kMode>
 __global__ void __launch_bounds__(kThreads, 2)
 q4_moe_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
               const __grid_constant__ CUtensorMap tmX, const MoeParams p) {
-  constexpr bool kScan = kMode == kScanGather;
   constexpr bool kPacked = kMode == kTablePacked;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int64_t xoff[kTok], yoff[kTok];
-  __shared__ int wsum[kThreads / 32];
+  __shared__ int64_t xoff[kTok];      // gather mode: the loader warp's rows of the current job
+  __shared__ int64_t yoff[4][kTok];   // each epilogue warp's output rows of its current job
   uint8_t* smem = smem_align(smem_raw, 1024);
   const uint32_t sB0 = smem_u32(smem);                              // [kBStages][2 atoms]
   const uint32_t raw0 = sB0 + kBStages * kBBytes;                   // [kRawStages][codes | pairs]
@@ -177,16 +178,15 @@ q4_moe_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
   uint64_t* a_empty = bars + kBarAEmpty;   // MMA commit
   uint64_t* b_full = bars + kBarBFull;     // loader arrival (with TMA bytes when packed)
   uint64_t* b_empty = bars + kBarBEmpty;   // MMA commit
-  uint64_t* d_full = bars + kBarDFull;     // once per pass, MMA commit
+  uint64_t* d_full = bars + kBarDFull;     // [2] per job, MMA commit
+  uint64_t* d_empty = bars + kBarDEmpty;   // [2] per job, 4 epilogue-warp arrivals
   uint64_t* done = bars + kBarDone;        // teardown
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.y, n0 = blockIdx.x * kRows;
-  const int nks = p.K / kKC;     // MMA stages per pass
-  const int TC = p.K / 256;      // weight stages per pass
-  const int npairs = p.T * p.n_used;
+  const int nks = p.K / kKC;     // MMA stages per job
+  const int TC = p.K / 256;      // weight stages per job
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRawStages; ++s) {
@@ -201,47 +201,14 @@ q4_moe_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
     }
-    mbar_init(d_full, 1);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&d_full[j], 1);
+      mbar_init(&d_empty[j], 4);
+    }
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
-
-  // When most experts receive pairs, the first weight stages are fetched
-  // before the routing is known: they do not depend on it.
-  const bool early = npairs >= p.n_expert;
-  int w_issued = 0;   // weight stages of pass 0 already issued (producer lane only)
-  if (warp == 6 && lane == 0 && early) {
-    tma_prefetch_desc(&tmC);
-    tma_prefetch_desc(&tmP);
-    for (; w_issued < kRawStages && w_issued < TC; ++w_issued)
-      produce_weights(&tmC, &tmP, p, e, n0, w_issued, w_issued, raw0, w_full, w_empty, abort_flag);
-  }
-
-  // ---- this expert's pairs ----
-  uint32_t mask = 0;
-  int first = 0, total = 0, rank0 = 0;
-  if (kScan) {
-    first = threadIdx.x;   // one pair per thread (npairs <= kThreads)
-    if (first < npairs) {
-      const int id = p.ids[(int64_t)(first / p.n_used) * p.ld_ids + (first % p.n_used)];
-      if (id == e) mask = 1u;
-      if ((id < 0 || id >= p.n_expert) && blockIdx.x == 0 && blockIdx.y == 0)
-        set_status(p.dev_status, QMM_ERR_BAD_EXPERT_ID);
-    }
-    rank0 = cta_exclusive_scan(__popc(mask), wsum, total);
-  } else {
-    first = p.offsets[e];
-    total = p.offsets[e + 1] - first;
-  }
-  if (total == 0) {
-    // no TMA write may land after the CTA has left
-    if (warp == 6 && lane == 0)
-      for (int s = 0; s < w_issued; ++s) mbar_wait(&w_full[s], 0, abort_flag, p.dev_status);
-    return;
-  }
-
   if (warp == 5) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -251,32 +218,40 @@ q4_moe_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  bool ok = true;
-  int pass = 0;
-  for (int pass0 = 0; pass0 < total; pass0 += kTok, ++pass) {
-    const int nt = min(kTok, total - pass0);
-    const int ncol = (nt + 15) & ~15;
-    if (kScan) {
-      uint32_t m = mask;
-      int rk = rank0;
-      while (m) {
-        const int j = __ffs(m) - 1;
-        m &= m - 1;
-        if (rk >= pass0 && rk < pass0 + kTok) pair_offsets(p, first + j, xoff[rk - pass0], yoff[rk - pass0]);
-        ++rk;
-      }
-    } else {
-      for (int c = threadIdx.x; c < nt; c += kThreads)
-        pair_offsets(p, p.pairs[first + pass0 + c], xoff[c], yoff[c]);
-    }
-    __syncthreads();
+  // The first unit's first weight stages do not depend on the routing: when
+  // most experts receive pairs they are fetched while the route-and-pack
+  // grid may still run.
+  const int e_first = (int)blockIdx.x / p.nrb;
+  const int n0_first = ((int)blockIdx.x - e_first * p.nrb) * kRows;
+  const int pre = p.npairs >= p.n_expert ? min(kRawStages, TC) : 0;
+  if (warp == 6 && lane == 0) {
+    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmP);
+    for (int tc = 0; tc < pre; ++tc)
+      produce_weights(&tmC, &tmP, p, e_first, n0_first, tc, tc, raw0, w_full, w_empty, abort_flag);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // When the first unit has no pairs, its prefetched stages are consumed and dropped.
+  const bool first_empty = p.offsets[e_first + 1] == p.offsets[e_first];
 
-    if (warp < 4) {
-      // ---- transform: raw tiles -> bf16 weights in TMEM ----
-      const int n = n0 + 32 * warp + lane;
-      const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
-      for (int tc = 0; tc < TC && ok; ++tc) {
-        const int gws = pass * TC + tc, slot = gws % kRawStages;
+  bool ok = true;
+  int njobs = 0;
+  if (warp < 4) {
+    // ---- transform: raw tiles -> bf16 weights in TMEM; then the epilogue ----
+    const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+    int gws = 0, gs = 0;
+    if (first_empty) {
+      for (; gws < pre && ok; ++gws) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&w_full[gws], 0, abort_flag, p.dev_status));
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(&w_empty[gws]);
+      }
+    }
+    Jobs jb;
+    while (ok && jb.next(p)) {
+      const int n = jb.n0 + 32 * warp + lane;
+      for (int tc = 0; tc < TC && ok; ++tc, ++gws) {
+        const int slot = gws % kRawStages;
         if (!__all_sync(0xffffffffu, mbar_wait(&w_full[slot], (gws / kRawStages) & 1, abort_flag, p.dev_status))) {
           ok = false;
           break;
@@ -289,8 +264,8 @@ q4_moe_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
         const uint4 pr0 = lds128(pb + 16 * ((2 * (lane & 3)) ^ ((lane >> 2) & 7)));
         const uint4 pr1 = lds128(pb + 16 * ((2 * (lane & 3) + 1) ^ ((lane >> 2) & 7)));
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int gs = pass * nks + 2 * tc + h, as = gs % kAStages;
+        for (int h = 0; h < 2; ++h, ++gs) {
+          const int as = gs % kAStages;
           if (!__all_sync(0xffffffffu,
                           mbar_wait(&a_empty[as], ((gs / kAStages) & 1) ^ 1, abort_flag, p.dev_status))) {
             ok = false;
@@ -324,32 +299,48 @@ q4_moe_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
         __syncwarp();
         if (lane == 0) mbar_arrive(&w_empty[slot]);
       }
-      // ---- epilogue: fp32 accumulator -> Y (lane = weight row, column = pair) ----
-      if (ok && __all_sync(0xffffffffu, mbar_wait(d_full, pass & 1, abort_flag, p.dev_status))) {
-        tc_fence_after();
-        const bool live = n < p.N;
-        for (int c0 = 0; c0 < ncol; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(trow + kColD + c0, v);
-          tmem_wait_ld();
-          if (live) {
+      if (!ok) break;
+      // ---- epilogue of this job: lane = weight row, column = pair ----
+      const int nt = jb.nt(), ncol = jb.ncol();
+      for (int c = lane; c < nt; c += 32) {
+        int64_t xo;
+        pair_offsets(p, p.pairs[jb.first + jb.pass0 + c], xo, yoff[warp][c]);
+      }
+      __syncwarp();
+      const int db = njobs & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&d_full[db], (njobs >> 1) & 1, abort_flag, p.dev_status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool live = n < p.N;
+      for (int c0 = 0; c0 < ncol; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(trow + kColD + 64 * db + c0, v);
+        tmem_wait_ld();
+        if (live) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (c0 + i < nt) p.Y[yoff[c0 + i] + n] = __uint_as_float(v[i]);
+          for (int i = 0; i < 16; ++i) {
+            if (c0 + i < nt) p.Y[yoff[warp][c0 + i] + n] = __uint_as_float(v[i]);
           }
         }
-        tc_fence_before();
-      } else {
-        ok = false;
       }
-    } else if (warp == 4) {
-      // ---- activation loader ----
-      if (kPacked) {
-        if (lane == 0) {
-          if (pass == 0) tma_prefetch_desc(&tmX);
-          const int row0 = first + pass0;
-          for (int ks = 0; ks < nks && ok; ++ks) {
-            const int gs = pass * nks + ks, bs = gs % kBStages;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_empty[db]);
+      ++njobs;
+    }
+  } else if (warp == 4) {
+    // ---- activation loader ----
+    int gs = 0;
+    Jobs jb;
+    if (kPacked) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmX);
+        while (ok && jb.next(p)) {
+          const int row0 = jb.first + jb.pass0, ncol = jb.ncol();
+          for (int ks = 0; ks < nks; ++ks, ++gs) {
+            const int bs = gs % kBStages;
             if (!mbar_wait(&b_empty[bs], ((gs / kBStages) & 1) ^ 1, abort_flag, p.dev_status)) {
               ok = false;
               break;
@@ -363,41 +354,65 @@ q4_moe_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
                                 row0 + c0);
           }
         }
+      }
+      __syncwarp();
+    } else {
+      int signalled = 0;   // stages whose b_full has been raised
+      while (ok && jb.next(p)) {
+        const int nt = jb.nt(), ncol = jb.ncol();
+        __syncwarp();   // the previous job's copies have read xoff
+        for (int c = lane; c < nt; c += 32) {
+          int64_t yo;
+          pair_offsets(p, p.pairs[jb.first + jb.pass0 + c], xoff[c], yo);
+        }
         __syncwarp();
-      } else {
-        for (int ks = 0; ks < nks + kLoaderLag && ok; ++ks) {
-          if (ks < nks) {
-            const int gs = pass * nks + ks, bs = gs % kBStages;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait(&b_empty[bs], ((gs / kBStages) & 1) ^ 1, abort_flag, p.dev_status))) {
-              ok = false;
-              break;
-            }
-            const uint32_t sb = sB0 + bs * kBBytes;
-            for (int i = lane; i < ncol * 16; i += 32) {
-              const int c = i >> 4, ch = i & 15;
-              const bool valid = c < nt;
-              const __nv_bfloat16* src = valid ? p.X + xoff[c] + (int64_t)ks * kKC + 8 * ch : p.X;
-              const uint32_t dst = sb + (ch >> 3) * kBAtomBytes + (c >> 3) * 1024 + (c & 7) * 128 +
-                                   (uint32_t)(((ch & 7) ^ (c & 7)) << 4);
-              cp_async16_zfill(dst, src, valid ? 16u : 0u);
-            }
+        for (int ks = 0; ks < nks; ++ks, ++gs) {
+          const int bs = gs % kBStages;
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(&b_empty[bs], ((gs / kBStages) & 1) ^ 1, abort_flag, p.dev_status))) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = sB0 + bs * kBBytes;
+          for (int i = lane; i < ncol * 16; i += 32) {
+            const int c = i >> 4, ch = i & 15;
+            const bool valid = c < nt;
+            const __nv_bfloat16* src = valid ? p.X + xoff[c] + (int64_t)ks * kKC + 8 * ch : p.X;
+            const uint32_t dst = sb + (ch >> 3) * kBAtomBytes + (c >> 3) * 1024 + (c & 7) * 128 +
+                                 (uint32_t)(((ch & 7) ^ (c & 7)) << 4);
+            cp_async16_zfill(dst, src, valid ? 16u : 0u);
           }
           cp_async_commit();
-          if (ks >= kLoaderLag) {
+          if (gs + 1 - signalled > kLoaderLag) {
             cp_async_wait<kLoaderLag>();
             fence_proxy_async_smem();   // generic-proxy writes -> tcgen05 reads
             __syncwarp();
-            if (lane == 0) mbar_arrive(&b_full[(pass * nks + ks - kLoaderLag) % kBStages]);
+            if (lane == 0) mbar_arrive(&b_full[signalled % kBStages]);
+            ++signalled;
           }
         }
       }
-    } else if (warp == 5) {
-      // ---- MMA issuer ----
-      if (lane == 0) {
-        const uint32_t idesc = idesc_f16(kRows, ncol, true);
-        for (int ks = 0; ks < nks && ok; ++ks) {
-          const int gs = pass * nks + ks, as = gs % kAStages, bs = gs % kBStages;
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      for (; signalled < gs; ++signalled)
+        if (lane == 0) mbar_arrive(&b_full[signalled % kBStages]);
+    }
+  } else if (warp == 5) {
+    // ---- MMA issuer ----
+    if (lane == 0) {
+      int gs = 0;
+      Jobs jb;
+      while (ok && jb.next(p)) {
+        const int db = njobs & 1;
+        const uint32_t idesc = idesc_f16(kRows, jb.ncol(), true);
+        if (!mbar_wait(&d_empty[db], ((njobs >> 1) & 1) ^ 1, abort_flag, p.dev_status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ks = 0; ks < nks; ++ks, ++gs) {
+          const int as = gs % kAStages, bs = gs % kBStages;
           if (!mbar_wait(&a_full[as], (gs / kAStages) & 1, abort_flag, p.dev_status) ||
               !mbar_wait(&b_full[bs], (gs / kBStages) & 1, abort_flag, p.dev_status)) {
             ok = false;
@@ -407,47 +422,46 @@ q4_moe_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
           const uint32_t sb = sB0 + bs * kBBytes;
 #pragma unroll
           for (int j = 0; j < kKC / 16; ++j)
-            umma_f16_ta(tmem + kColD, tmem + kColA + 64 * as + 8 * j,
+            umma_f16_ta(tmem + kColD + 64 * db, tmem + kColA + 64 * as + 8 * j,
                         desc_kmajor_sw128(sb + (j >> 2) * kBAtomBytes + 32 * (j & 3)), idesc,
                         (ks > 0 || j > 0) ? 1u : 0u);
           umma_commit(&a_empty[as]);
           umma_commit(&b_empty[bs]);
         }
-        if (ok) umma_commit(d_full);
+        if (!ok) break;
+        umma_commit(&d_full[db]);
+        ++njobs;
       }
-      __syncwarp();
-    } else {
-      // ---- weight producer ----
-      if (lane == 0) {
-        if (pass > 0 || !early) {
-          tma_prefetch_desc(&tmC);
-          tma_prefetch_desc(&tmP);
-        }
-        for (int tc = (pass == 0 ? w_issued : 0); tc < TC && ok; ++tc)
-          ok = produce_weights(&tmC, &tmP, p, e, n0, tc, pass * TC + tc, raw0, w_full, w_empty, abort_flag);
-      }
-      __syncwarp();
     }
-    __syncthreads();   // accumulator drained; routing slots and rings free for the next pass
+    __syncwarp();
+  } else {
+    // ---- weight producer ----
+    if (lane == 0) {
+      int gws = pre;
+      Jobs jb;
+      bool first = true;
+      while (ok && jb.next(p)) {
+        // the first unit's first stages were issued before the routing wait
+        const int tc0 = (first && !first_empty) ? pre : 0;   // the first job is then the first unit's pass 0
+        first = false;
+        for (int tc = tc0; tc < TC && ok; ++tc, ++gws)
+          ok = produce_weights(&tmC, &tmP, p, jb.e, jb.n0, tc, gws, raw0, w_full, w_empty, abort_flag);
+      }
+    }
+    __syncwarp();
   }
 
   // ---- teardown ----
   cp_async_wait<0>();
   tc_fence_before();
   __syncthreads();
-  if (warp == 6 && lane == 0 && *abort_flag) {
-    // a stage the transform never consumed may still be in flight
-    const int last = pass * TC;
-    for (int g = last > kRawStages ? last - kRawStages : 0; g < last; ++g)
-      mbar_wait(&w_full[g % kRawStages], (g / kRawStages) & 1, abort_flag, nullptr, 100000000ull) ||
-          mbar_try_wait(&w_full[g % kRawStages], (g / kRawStages) & 1);
-  }
-  if (kPacked && warp == 4 && lane == 0 && *abort_flag) {
-    // activation loads of the last stages may still be in flight
-    const int last = pass * nks;
-    for (int g = last > kBStages ? last - kBStages : 0; g < last; ++g)
-      mbar_wait(&b_full[g % kBStages], (g / kBStages) & 1, abort_flag, nullptr, 100000000ull) ||
-          mbar_try_wait(&b_full[g % kBStages], (g / kBStages) & 1);
+  if (*abort_flag && lane == 0 && (warp == 4 || warp == 6)) {
+    // TMA writes of stages nobody consumed may still be in flight
+    uint64_t* full = warp == 6 ? w_full : b_full;
+    const int n = warp == 6 ? kRawStages : kBStages;
+    for (int s = 0; s < n; ++s)
+      for (int ph = 0; ph < 2; ++ph)
+        mbar_wait(&full[s], ph, abort_flag, nullptr, 50000000ull) || mbar_try_wait(&full[s], ph);
   }
   if (warp == 5) {
     if (lane == 0) {
@@ -460,73 +474,143 @@ q4_moe_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ C
   }
 }
 
-// One CTA: count pairs per expert, prefix-sum, scatter pair ids by expert.
-__global__ void __launch_bounds__(1024)
-moe_route_kernel(const int32_t* __restrict__ ids, int64_t ld_ids, int n_used, int T, int n_expert,
-                 int32_t* __restrict__ offsets, int32_t* __restrict__ pairs, int32_t* dev_status) {
-  extern __shared__ int sm[];
-  int* cnt = sm;               // [n_expert]
-  int* cursor = sm + n_expert; // [n_expert]
-  const int tid = threadIdx.x;
-  for (int e = tid; e < n_expert; e += blockDim.x) cnt[e] = 0;
-  __syncthreads();
+// Routing and activation packing in one launch.  Block b owns pairs
+// [b*PB, (b+1)*PB).  Every block reads all ids: the histogram of all pairs
+// gives the expert offsets, and the histogram of the pairs before its own
+// range gives each expert's base rank there.  Warp 0 then ranks the block's
+// pairs in pair order (lanes with the same expert found by match_any), so the
+// grouped list is deterministic.  Finally the block copies its pairs'
+// activation rows to their ranks (when the packed buffer exists).
+constexpr int kRouteThreads = 256;
+constexpr int kRouteMaxPB = 32;   // one warp ranks a block's pairs
+
+__global__ void __launch_bounds__(kRouteThreads)
+moe_route_pack_kernel(const int32_t* __restrict__ ids, int64_t ld_ids, int n_used, int T, int n_expert, int PB,
+                      const __nv_bfloat16* __restrict__ X, int64_t ldx_token, int64_t ldx_slot, int K,
+                      int32_t* __restrict__ offsets, int32_t* __restrict__ pairs, __nv_bfloat16* __restrict__ Xp,
+                      int32_t* dev_status) {
+  extern __shared__ int rsm[];
+  int* off = rsm;                    // [n_expert + 1]: histogram, then exclusive offsets
+  int* before = rsm + n_expert + 1;  // [n_expert]: pairs of each expert before this block's range
+  int* run = before + n_expert;      // [n_expert]: ranked so far inside this block
+  __shared__ int wsum[kRouteThreads / 32];
+  __shared__ int rank_s[kRouteMaxPB];
+  __shared__ int pair_s[kRouteMaxPB];
+  // the grouped kernel may start now: it prefetches weights, then waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int npairs = T * n_used;
-  bool bad = false;
-  for (int p = tid; p < npairs; p += blockDim.x) {
-    const int t = p / n_used, i = p % n_used;
-    const int e = ids[(int64_t)t * ld_ids + i];
-    if (e < 0 || e >= n_expert) { bad = true; continue; }
-    atomicAdd(&cnt[e], 1);
-  }
-  if (bad) set_status(dev_status, QMM_ERR_BAD_EXPERT_ID);
+  const int p0 = blockIdx.x * PB;
+  for (int e = tid; e <= n_expert; e += kRouteThreads) off[e] = 0;
+  for (int e = tid; e < n_expert; e += kRouteThreads) before[e] = run[e] = 0;
   __syncthreads();
-  if (tid < 32) {
-    // warp scan over contiguous segments of the expert range
-    const int per = (n_expert + 31) / 32;
+  bool bad = false;
+  // eight independent loads in flight per thread, then the shared-memory counts
+  for (int base = 0; base < npairs; base += 8 * kRouteThreads) {
+    int ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int pr = base + u * kRouteThreads + tid;
+      ev[u] = pr < npairs ? ids[(int64_t)(pr / n_used) * ld_ids + (pr % n_used)] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int pr = base + u * kRouteThreads + tid;
+      if (pr >= npairs) continue;
+      const int e = ev[u];
+      if (e < 0 || e >= n_expert) {
+        bad = true;
+        continue;
+      }
+      atomicAdd(&off[e], 1);
+      if (pr < p0) atomicAdd(&before[e], 1);
+    }
+  }
+  if (bad && blockIdx.x == 0) set_status(dev_status, QMM_ERR_BAD_EXPERT_ID);
+  __syncthreads();
+  // exclusive scan of off[0 .. n_expert) in place; off[n_expert] = total
+  {
+    const int per = (n_expert + kRouteThreads - 1) / kRouteThreads;
     const int lo = min(tid * per, n_expert), hi = min(lo + per, n_expert);
     int seg = 0;
-    for (int e = lo; e < hi; ++e) seg += cnt[e];
+    for (int e = lo; e < hi; ++e) seg += off[e];
     int incl = seg;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (tid >= d) incl += v;
+      const int u = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += u;
     }
-    int run = incl - seg;
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int wbase = 0, total = 0;
+    for (int w = 0; w < kRouteThreads / 32; ++w) {
+      wbase += (w < warp) ? wsum[w] : 0;
+      total += wsum[w];
+    }
+    int runv = wbase + incl - seg;
+    __syncthreads();   // every thread has read its segment before any is overwritten
     for (int e = lo; e < hi; ++e) {
-      offsets[e] = run;
-      cursor[e] = run;
-      run += cnt[e];
+      const int c = off[e];
+      off[e] = runv;
+      runv += c;
     }
-    if (tid == 31) offsets[n_expert] = incl;
+    if (tid == 0) off[n_expert] = total;
   }
   __syncthreads();
-  for (int p = tid; p < npairs; p += blockDim.x) {
-    const int t = p / n_used, i = p % n_used;
-    const int e = ids[(int64_t)t * ld_ids + i];
-    if (e < 0 || e >= n_expert) continue;
-    pairs[atomicAdd(&cursor[e], 1)] = p;
+  if (blockIdx.x == 0)
+    for (int e = tid; e <= n_expert; e += kRouteThreads) offsets[e] = off[e];
+  // rank this block's pairs in pair order
+  const int nb = min(PB, npairs - p0);
+  if (warp == 0) {
+    for (int j0 = 0; j0 < nb; j0 += 32) {
+      const int j = j0 + lane;
+      const int pr = p0 + j;
+      int e = -1;
+      if (j < nb) {
+        e = ids[(int64_t)(pr / n_used) * ld_ids + (pr % n_used)];
+        if (e < 0 || e >= n_expert) e = -1;
+      }
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      const int local = __popc(same & ((1u << lane) - 1u));
+      int rank = -1;
+      if (e >= 0) rank = off[e] + before[e] + run[e] + local;
+      __syncwarp();
+      if (e >= 0 && local == 0) run[e] += __popc(same);
+      __syncwarp();
+      if (j < nb) {
+        rank_s[j] = rank;
+        pair_s[j] = pr;
+        if (rank >= 0) pairs[rank] = pr;
+      }
+    }
   }
-}
-
-// Rows r of the packed activations are the pairs in expert order:
-// Xp[r][:] = src1 of pairs[r].  Eight rows per CTA, 16 bytes per thread and row.
-constexpr int kPermRows = 8;
-__global__ void __launch_bounds__(256)
-moe_permute_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx_token, int64_t ldx_slot, int n_used,
-                   const int32_t* __restrict__ offsets, int n_expert, const int32_t* __restrict__ pairs, int K,
-                   __nv_bfloat16* __restrict__ Xp) {
-  const int total = offsets[n_expert];
+  if (Xp == nullptr) return;
+  __syncthreads();
+  // copy: 16-byte units, eight loads in flight per thread
   const int chunks = K / 8;
+  const int units = nb * chunks;
+  for (int base = 0; base < units; base += 8 * kRouteThreads) {
+    uint4 v[8];
+    int dst_rank[8], c8[8];
 #pragma unroll
-  for (int i = 0; i < kPermRows; ++i) {
-    const int r = blockIdx.x * kPermRows + i;
-    if (r >= total) break;
-    const int pr = pairs[r];
-    const uint4* src = reinterpret_cast<const uint4*>(X + (int64_t)(pr / n_used) * ldx_token +
-                                                      (int64_t)(pr % n_used) * ldx_slot);
-    uint4* dst = reinterpret_cast<uint4*>(Xp + (int64_t)r * K);
-    for (int c = threadIdx.x; c < chunks; c += 256) dst[c] = ldg128(src + c);
+    for (int u = 0; u < 8; ++u) {
+      const int idx = base + u * kRouteThreads + tid;
+      dst_rank[u] = -1;
+      if (idx < units) {
+        const int j = idx / chunks;
+        c8[u] = idx - j * chunks;
+        dst_rank[u] = rank_s[j];
+        if (dst_rank[u] >= 0) {
+          const int pr = pair_s[j];
+          const uint4* src = reinterpret_cast<const uint4*>(X + (int64_t)(pr / n_used) * ldx_token +
+                                                            (int64_t)(pr % n_used) * ldx_slot);
+          v[u] = ldg128(src + c8[u]);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (dst_rank[u] >= 0) reinterpret_cast<uint4*>(Xp + (int64_t)dst_rank[u] * K)[c8[u]] = v[u];
   }
 }
 
@@ -536,9 +620,19 @@ cudaError_t launch_grouped(const CUtensorMap& tmC, const CUtensorMap& tmP, const
   cudaError_t err = cudaFuncSetAttribute(q4_moe_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
   if (err != cudaSuccess) return err;
-  dim3 grid((unsigned)((p.N + kRows - 1) / kRows), (unsigned)p.n_expert);
-  q4_moe_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(tmC, tmP, tmX, p);
-  return cudaGetLastError();
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)min(p.n_units, 2 * sms));   // persistent: two CTAs per SM
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;   // overlap the route-and-pack grid
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, q4_moe_kernel<kMode>, tmC, tmP, tmX, p);
 }
 
 }  // namespace
@@ -560,34 +654,40 @@ cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream) {
   p.X = a.X;
   p.ldx_token = a.ldx_token;
   p.ldx_slot = a.ldx_slot;
-  p.ids = a.ids;
-  p.ld_ids = a.ld_ids;
   p.n_used = a.n_used;
-  p.T = a.T;
   p.n_expert = a.n_expert;
+  p.npairs = a.T * a.n_used;
+  p.nrb = (a.N + kRows - 1) / kRows;
+  p.n_units = a.n_expert * p.nrb;
   p.Y = a.Y;
   p.ldy_token = a.ldy_token;
   p.ldy_slot = a.ldy_slot;
+  p.offsets = a.offsets;
+  p.pairs = a.pairs;
   p.dev_status = a.dev_status;
   const uint64_t n_tiles = (uint64_t)a.n_expert * (uint64_t)p.tiles_per_expert;
-  if (n_tiles > (uint64_t)INT32_MAX) return cudaErrorInvalidValue;
+  if (n_tiles > (uint64_t)INT32_MAX || (int64_t)a.n_expert * p.nrb > INT32_MAX) return cudaErrorInvalidValue;
   CUtensorMap tmC, tmP, tmX;
   if (!make_tmap_q4_tiles(&tmC, a.tiles, n_tiles, 32) || !make_tmap_q4_tiles(&tmP, a.tiles, n_tiles, 8))
     return cudaErrorInvalidValue;
   const int npairs = a.T * a.n_used;
-  if (npairs <= kScanMaxPairs) return launch_grouped<kScanGather>(tmC, tmP, tmC, p, stream);
-  const size_t smem = (size_t)a.n_expert * 2 * sizeof(int);
-  moe_route_kernel<<<1, 1024, smem, stream>>>(a.ids, a.ld_ids, a.n_used, a.T, a.n_expert, a.offsets,
-                                              a.pairs, a.dev_status);
+  // 8 pairs per block (one round of row loads per block), more when the
+  // batch is large enough that every block rereading all ids would cost more
+  int PB = 8;
+  while (PB < kRouteMaxPB && (int64_t)npairs * ((npairs + PB - 1) / PB) > (int64_t)64 << 20) PB *= 2;
+  const int nblk = (npairs + PB - 1) / PB;
+  const size_t rsmem = (size_t)(3 * a.n_expert + 1) * sizeof(int);
+  if (rsmem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(moe_route_pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)rsmem);
+    if (e != cudaSuccess) return e;
+  }
+  moe_route_pack_kernel<<<nblk, kRouteThreads, rsmem, stream>>>(
+      a.ids, a.ld_ids, a.n_used, a.T, a.n_expert, PB, a.X, a.ldx_token, a.ldx_slot, a.K, a.offsets, a.pairs,
+      a.xperm, a.dev_status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  p.offsets = a.offsets;
-  p.pairs = a.pairs;
   if (a.xperm == nullptr) return launch_grouped<kTableGather>(tmC, tmP, tmC, p, stream);
-  moe_permute_kernel<<<(unsigned)((npairs + kPermRows - 1) / kPermRows), 256, 0, stream>>>(
-      a.X, a.ldx_token, a.ldx_slot, a.n_used, a.offsets, a.n_expert, a.pairs, a.K, a.xperm);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
   if (!make_tmap_2d(&tmX, true, a.xperm, (uint64_t)a.K, (uint64_t)npairs, (uint64_t)a.K * 2, 64, kXBox))
     return cudaErrorInvalidValue;
   return launch_grouped<kTablePacked>(tmC, tmP, tmX, p, stream);
