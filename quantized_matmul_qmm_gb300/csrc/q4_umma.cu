@@ -1,23 +1,55 @@
-// 4-bit GEMM at prefill sizes on the 5th-generation tensor cores.
+// q4 GEMMs on the 5th-generation tensor cores: the prefill GEMM and
+// MUL_MAT_ID.  Weights are 32x256 q4_1 tiles, w = q * scale + min ("NPU
+// engine: full ELFs, no xclbin", "Q4NX chunks"; "Zaya 8B Q4NX on the AMD NPU",
+// round 26).
 //
-// Y[m][n] = sum_k X[m][k] * w[n][k], with w = q * scale + min from 32x256 q4_1
-// tiles ("NPU engine: full ELFs, no xclbin", "Q4NX chunks"; "Zaya 8B Q4NX on
-// the AMD NPU", round 26).  The pages' lesson for prefill (round 25o): reuse
-// each dequantised weight across many activation columns.  Here each weight
-// is dequantised once per 256 tokens, straight into shared memory, and never
-// exists in expanded form in HBM.
+// MUL_MAT_ID: for every (token t, slot i), dst[t][i] = W_e . src1 with
+// e = ids[t * ld_ids + i] ("Zaya 8B Q4NX on the AMD NPU", "The bugs that were
+// the work": the ids are a strided view, and the down projection reads a
+// per-slot src1 row).  The prefill GEMM is the same kernel with one "expert"
+// and the M rows of X in order; the pages' lesson for prefill (round 25o) is
+// to reuse each dequantised weight across many activation columns.
 //
-// One CTA computes a 128 (weight rows) x 256 (tokens) tile.  The MMA's M side
-// is the weights (the A operand, written by the transform warps in the
-// 128-byte-swizzle K-major layout).  Its N side is X (the B operand, loaded
-// by TMA).  The accumulator is fp32 in TMEM.
-//   warp 0     TMA producer for X tiles (4-stage ring)
-//   warp 1     TMEM owner and MMA issuer (tcgen05.mma kind::f16, bf16)
-//   warps 2-5  transform: each owns one 32-row tile row; lane = row.  Code
-//              words and (scale, min) pairs are prefetched four stages ahead
-//              in registers, and each weight is formed as bf16(q*s + min)
-//              with one fma.rn.bf16x2 (one rounding).  Then these warps
-//              drain TMEM and store Y.
+// Work is cut into units of 128 weight rows of one expert; a unit's jobs are
+// its expert's (token, slot) pairs, up to kTok (64, or 128 for a large dense
+// M) per job.  Each weight is read from HBM once per job and used for all of
+// the job's pairs: the grouped dispatch the pages credit for the MoE
+// speed-up.  The grid is persistent (one CTA per SM); every role walks the
+// CTA's units in the same order, and the pipelines run on across unit
+// boundaries, so the next unit's weights stream in while the current one
+// finishes.  The fp32 accumulator is double buffered in TMEM and drained by
+// warps of its own, so a job's epilogue overlaps the next job's MMAs.
+//
+// Routing.  A route-and-pack kernel (one block per 8 pairs) writes per-expert
+// offsets and the grouped (token, slot) list into the caller's workspace, in
+// pair order inside each expert.  The grouped kernel is launched as its
+// programmatic dependent, so it starts while routing still runs.
+//
+// Activations.  With a full workspace, the route-and-pack kernel also packs
+// the rows of src1 in expert order, so that every job's B operand is a dense
+// block that TMA loads whole.  With only the routing tables (the
+// no-allocation entry point) a loader warp gathers the rows with cp.async.
+//
+// The contraction runs on the 5th-generation tensor cores with the weights as
+// the M = 128 side and the pairs as N (16..kTok).  The dequantised weights go
+// from registers straight into TMEM, which tcgen05.mma reads as its A
+// operand, so they never pass through shared memory; only the raw tiles and
+// the activations do.  TMEM: two accumulators of kTok columns, then four A
+// buffers of 64 columns (128 k).  Roles (480 threads):
+//   warp 14    weight producer: TMA of whole tile columns (the 4 tiles of the
+//              unit's rows, codes and pairs as two boxes each) into a ring,
+//              128-byte swizzle.
+//   warps 0-7  transform: warp (q, h) owns TMEM lane quarter q (one weight row
+//              per lane) and 64-k half h of every 128-k stage: it reads the
+//              rows' codes and pairs, forms w = bf16(q * s + m) with one
+//              rounding, and stores the stage into an A buffer (tcgen05.st).
+//   warps 8-11 epilogue: drain a finished accumulator (tcgen05.ld) into Y.
+//   warp 12    activation loader: TMA of the packed rows (or of X for the
+//              dense GEMM), or a cp.async gather, into the 128-byte-swizzle
+//              K-major layout.
+//   warp 13    TMEM owner; lane 0 issues tcgen05.mma (kind::f16, bf16).
+// Every wait is bounded; a timeout sets the caller's status word and the CTA
+// leaves cleanly.
 #include <cuda_bf16.h>
 
 #include "qmm_internal.h"
@@ -28,109 +60,200 @@ namespace {
 
 using namespace umma;
 
-constexpr int kBW = 128;            // weight rows per tile (MMA M)
-constexpr int kBT = 256;            // tokens per tile (MMA N)
-constexpr int kBK = 64;             // K per stage
-constexpr int kStages = 4;
-constexpr int kWBytes = kBW * kBK * 2;   // 16 KB
-constexpr int kXBytes = kBT * kBK * 2;   // 32 KB
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 256;
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kWBytes + kXBytes) + 256;
-constexpr int kPrefetch = 4;        // stages of raw weights in flight per transform thread
-constexpr int kMinM = 17;           // M <= 16 runs the decode GEMV kernel
+constexpr int kRows = 128;                          // weight rows per unit (MMA M)
+constexpr int kKC = 128;                            // K per MMA / activation stage
+constexpr int kRawStagesMax = 4;                    // weight ring, one tile column (256 k) per stage
+constexpr int kBStagesMax = 4;
+constexpr int kAStages = 4;                         // TMEM A buffers of 64 columns (128 k)
+constexpr int kCodeBox = 4096;                      // 32 code rows x 128 B
+constexpr int kPairBox = 1024;                      // 8 pair rows x 128 B
+constexpr int kRawBytes = 4 * (kCodeBox + kPairBox);   // 4 tile rows: codes [4][4 KB], then pairs [4][1 KB]
+constexpr int kLoaderLag = 2;                       // gathered activation stages in flight before signalling
 
-struct Q4UmmaParams {
-  const uint8_t* tiles;
-  int N, K, M;
+// Sizes that follow from the largest job width kTok (the MMA's N): two fp32
+// accumulators of kTok columns, then two A buffers of 64 columns in TMEM;
+// activation stages of kTok rows x 128 k.
+template <int kTok>
+struct Cfg {
+  static constexpr int kRawStages = kTok == 64 ? 4 : 3;
+  static constexpr int kBStages = 4;                // activation ring depth
+  static constexpr int kBAtomBytes = kTok * 128;    // kTok rows x 64 k bf16, 128-byte swizzle
+  static constexpr int kBBytes = 2 * kBAtomBytes;   // 128 k per stage
+  static constexpr uint32_t kColA = 2 * kTok;       // after the two accumulators
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr size_t kSmemBytes = 1024 + (size_t)kBStages * kBBytes + (size_t)kRawStages * kRawBytes + 256;
+  static_assert(kColA + 64 * kAStages <= kTmemCols, "TMEM budget");
+};
+
+// Activation source of one launch: MUL_MAT_ID with the routing tables only
+// (gather), MUL_MAT_ID with packed rows, or a dense GEMM (one "expert", all
+// M rows of X in order).
+enum MoeMode { kTableGather = 0, kTablePacked = 1, kDense = 2 };
+
+// mbarrier block after the two rings
+constexpr int kBarWFull = 0;
+constexpr int kBarWEmpty = kBarWFull + kRawStagesMax;
+constexpr int kBarAFull = kBarWEmpty + kRawStagesMax;
+constexpr int kBarAEmpty = kBarAFull + kAStages;
+constexpr int kBarBFull = kBarAEmpty + kAStages;
+constexpr int kBarBEmpty = kBarBFull + kBStagesMax;
+constexpr int kBarDFull = kBarBEmpty + kBStagesMax;
+constexpr int kBarDEmpty = kBarDFull + 2;
+constexpr int kBarDone = kBarDEmpty + 2;
+constexpr int kNumBars = kBarDone + 1;
+static_assert(kNumBars * 8 + 8 <= 256, "barrier block");
+
+struct MoeParams {
+  int64_t tiles_per_expert;
+  int N, K;
+  const __nv_bfloat16* X;
+  int64_t ldx_token, ldx_slot;
+  int n_used, n_expert, npairs;
+  int n_units, nrb;         // units = experts x 128-row blocks, unit u = e * nrb + row block
   float* Y;
-  int64_t ldy;
+  int64_t ldy_token, ldy_slot;
+  const int32_t* offsets;   // [n_expert + 1]; null for the dense GEMM
+  const int32_t* pairs;     // grouped (token, slot) ids
+  int dense_rows;           // dense GEMM: M
+  int dense_chunks;         // dense GEMM: token chunks of kTok per row block; unit u = rb * chunks + chunk
   int32_t* dev_status;
 };
 
-struct RawStage {
-  uint4 w[2];   // code words 0..3 of blocks 2s and 2s+1 (32 contiguous bytes of the row)
-  uint2 p;      // (scale, min) pairs of blocks 2s, 2s+1
-};
-
-__device__ __forceinline__ void load_raw(RawStage& r, const uint8_t* row_tile0, const uint8_t* pair_tile0,
-                                         int kb, bool valid) {
-  if (!valid) {
-    r.w[0] = make_uint4(0u, 0u, 0u, 0u);
-    r.w[1] = make_uint4(0u, 0u, 0u, 0u);
-    r.p = make_uint2(0u, 0u);
-    return;
-  }
-  const int tc = kb >> 2, s4 = kb & 3;
-  const uint8_t* base = row_tile0 + (int64_t)tc * kTileBytes + 32 * s4;
-  r.w[0] = ldg128(base);
-  r.w[1] = ldg128(base + 16);
-  r.p = *reinterpret_cast<const uint2*>(pair_tile0 + (int64_t)tc * kTileBytes + 8 * s4);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_sub_fma(uint32_t q2, uint32_t s2, uint32_t m2) {
-  // (128+q) - 128 = q exactly, then q*s + m with a single rounding
-  __nv_bfloat162 q = *reinterpret_cast<__nv_bfloat162*>(&q2);
+// q * s + m in bf16 from a (128 + q) pair: the subtraction is exact, the fma
+// rounds once.
+__device__ __forceinline__ uint32_t dequant2(uint32_t q2_biased, uint32_t s2, uint32_t m2) {
+  __nv_bfloat162 q = *reinterpret_cast<__nv_bfloat162*>(&q2_biased);
   const uint32_t c128 = 0x43004300u;
   q = __hsub2(q, *reinterpret_cast<const __nv_bfloat162*>(&c128));
-  const __nv_bfloat162 w = __hfma2(q, *reinterpret_cast<__nv_bfloat162*>(&s2), *reinterpret_cast<__nv_bfloat162*>(&m2));
+  const __nv_bfloat162 w =
+      __hfma2(q, *reinterpret_cast<__nv_bfloat162*>(&s2), *reinterpret_cast<__nv_bfloat162*>(&m2));
   return *reinterpret_cast<const uint32_t*>(&w);
 }
 
-// Dequantise one stage (64 k of one row) into the swizzled A tile.
-__device__ __forceinline__ void write_stage(uint8_t* tile, int row, const RawStage& r) {
-  const uint32_t rowoff = (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
-#pragma unroll
-  for (int bl = 0; bl < 2; ++bl) {
-    const uint32_t pair = bl ? r.p.y : r.p.x;
-    const uint32_t s2 = __byte_perm(pair, 0, 0x1010);
-    const uint32_t m2 = __byte_perm(pair, 0, 0x3232);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const uint32_t word = u4_get(r.w[bl], t);
-      uint4 o;
-      o.x = bf16x2_sub_fma(q4_pair_biased(word, 0), s2, m2);
-      o.y = bf16x2_sub_fma(q4_pair_biased(word, 1), s2, m2);
-      o.z = bf16x2_sub_fma(q4_pair_biased(word, 2), s2, m2);
-      o.w = bf16x2_sub_fma(q4_pair_biased(word, 3), s2, m2);
-      const int c = 4 * bl + t;    // 16-byte chunk = k 8c .. 8c+7 of the stage
-      *reinterpret_cast<uint4*>(tile + rowoff + (uint32_t)(((c ^ (row & 7)) & 7) << 4)) = o;
-    }
+__device__ __forceinline__ void pair_offsets(const MoeParams& p, int pr, int64_t& xo, int64_t& yo) {
+  const int tok = pr / p.n_used, slot = pr % p.n_used;
+  xo = (int64_t)tok * p.ldx_token + (int64_t)slot * p.ldx_slot;
+  yo = (int64_t)tok * p.ldy_token + (int64_t)slot * p.ldy_slot;
+}
+
+// The CTA's jobs, in the same order for every role: units blockIdx.x,
+// blockIdx.x + gridDim.x, ...; each unit's pairs in passes of up to kTok.
+// Units without pairs are skipped.
+// Expert and first weight row of unit u.
+__device__ __forceinline__ void unit_rows(const MoeParams& p, int u, int& e, int& n0) {
+  if (p.offsets == nullptr) {   // dense: u = row block * chunks + token chunk
+    e = 0;
+    n0 = (u / p.dense_chunks) * kRows;
+  } else {                      // MUL_MAT_ID: u = expert * row blocks + row block
+    e = u / p.nrb;
+    n0 = (u - e * p.nrb) * kRows;
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-q4_umma_kernel(const __grid_constant__ CUtensorMap tmX, const Q4UmmaParams p) {
+template <int kTok>
+struct Jobs {
+  int u, e, n0, first, total, pass0;
+  __device__ Jobs() : u((int)blockIdx.x - (int)gridDim.x), e(0), n0(0), first(0), total(0), pass0(0) {}
+  __device__ bool next(const MoeParams& p) {
+    pass0 += kTok;
+    while (pass0 >= total) {
+      u += gridDim.x;
+      if (u >= p.n_units) return false;
+      unit_rows(p, u, e, n0);
+      if (p.offsets == nullptr) {   // one job: this unit's chunk of rows of X
+        first = 0;
+        pass0 = (u % p.dense_chunks) * kTok;
+        total = min(p.dense_rows, pass0 + kTok);
+      } else {
+        first = p.offsets[e];
+        total = p.offsets[e + 1] - first;
+        pass0 = 0;
+      }
+    }
+    return true;
+  }
+  __device__ int nt() const { return min(kTok, total - pass0); }
+  __device__ int ncol() const { return (nt() + 15) & ~15; }
+};
+
+// One weight stage: the unit's (up to) 4 tiles of tile column tc.
+template <int kRawStages>
+__device__ __forceinline__ bool produce_weights(const CUtensorMap* tmC, const CUtensorMap* tmP, const MoeParams& p,
+                                                int e, int n0, int tc, int gws, uint32_t raw0, uint64_t* w_full,
+                                                uint64_t* w_empty, volatile int* abort_flag) {
+  const int slot = gws % kRawStages;
+  if (!mbar_wait(&w_empty[slot], ((gws / kRawStages) & 1) ^ 1, abort_flag, p.dev_status)) return false;
+  // one box of the unit's 4 tile rows for the codes, one for the pairs; tile
+  // rows past the expert's last (a partial unit) load junk that no one stores
+  mbar_arrive_expect_tx(&w_full[slot], (uint32_t)(4 * (kCodeBox + kPairBox)));
+  const uint32_t sb = raw0 + slot * kRawBytes;
+  const int trow = (int)((int64_t)e * (p.N / 32) + (n0 >> 5));
+  tma_load_4d(sb, tmC, &w_full[slot], 0, 0, tc, trow);
+  tma_load_4d(sb + 4 * kCodeBox, tmP, &w_full[slot], 0, 32, tc, trow);
+  return true;
+}
+
+template <int kMode, int kTok, int kXW>
+__global__ void __launch_bounds__(32 * (kXW + 7), 1)
+q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+             const __grid_constant__ CUtensorMap tmX, const MoeParams p) {
+  constexpr bool kPacked = kMode != kTableGather;   // activations by TMA
+  constexpr int kRawStages = Cfg<kTok>::kRawStages;
+  constexpr int kBStages = Cfg<kTok>::kBStages;
+  constexpr int kBAtomBytes = Cfg<kTok>::kBAtomBytes;
+  constexpr int kBBytes = Cfg<kTok>::kBBytes;
+  constexpr uint32_t kColA = Cfg<kTok>::kColA;
+  constexpr uint32_t kTmemCols = Cfg<kTok>::kTmemCols;
+  // warps 0 .. kXW-1 transform (kXW / 4 per TMEM lane quarter), then four
+  // epilogue warps (one per quarter), the activation loader, the MMA issuer
+  // and the weight producer
+  constexpr int kHalves = kXW / 4;
+  constexpr int kWEpi = kXW, kWLoad = kXW + 4, kWMma = kXW + 5, kWProd = kXW + 6;
   extern __shared__ uint8_t smem_raw[];
+  __shared__ int64_t xoff[kTok];      // gather mode: the loader warp's rows of the current job
+  __shared__ int64_t yoff[4][kTok];   // each epilogue warp's output rows of its current job
   uint8_t* smem = smem_align(smem_raw, 1024);
-  uint8_t* sW = smem;
-  uint8_t* sX = smem + kStages * kWBytes;
-  uint64_t* xfull = reinterpret_cast<uint64_t*>(smem + kStages * (kWBytes + kXBytes));
-  uint64_t* wfull = xfull + kStages;
-  uint64_t* empty = wfull + kStages;
-  uint64_t* tfull = empty + kStages;
-  uint64_t* done = tfull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  const uint32_t sB0 = smem_u32(smem);                              // [kBStages][2 atoms]
+  const uint32_t raw0 = sB0 + kBStages * kBBytes;                   // [kRawStages][codes | pairs]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBStages * kBBytes + kRawStages * kRawBytes);
+  uint64_t* w_full = bars + kBarWFull;     // TMA bytes
+  uint64_t* w_empty = bars + kBarWEmpty;   // 4 transform-warp arrivals
+  uint64_t* a_full = bars + kBarAFull;     // 4 transform-warp arrivals
+  uint64_t* a_empty = bars + kBarAEmpty;   // MMA commit
+  uint64_t* b_full = bars + kBarBFull;     // loader arrival (with TMA bytes when packed)
+  uint64_t* b_empty = bars + kBarBEmpty;   // MMA commit
+  uint64_t* d_full = bars + kBarDFull;     // [2] per job, MMA commit
+  uint64_t* d_empty = bars + kBarDEmpty;   // [2] per job, 4 epilogue-warp arrivals
+  uint64_t* done = bars + kBarDone;        // teardown
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBW, m0 = blockIdx.y * kBT;
-  const int nkb = p.K / kBK;
-  const int TC = p.K / 256;
+  const int nks = p.K / kKC;     // MMA stages per job
+  const int TC = p.K / 256;      // weight stages per job
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&xfull[s], 1);
-      mbar_init(&wfull[s], 4);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(&w_full[s], 1);
+      mbar_init(&w_empty[s], kXW);
     }
-    mbar_init(tfull, 1);
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&a_full[s], kXW);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&d_full[j], 1);
+      mbar_init(&d_empty[j], 4);
+    }
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tmX);
   }
-  if (warp == 1) {
+  if (warp == kWMma) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -139,134 +262,535 @@ q4_umma_kernel(const __grid_constant__ CUtensorMap tmX, const Q4UmmaParams p) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kStages;
-        if (!mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag, p.dev_status)) break;
-        mbar_arrive_expect_tx(&xfull[s], kXBytes);
-        tma_load_2d(sX + s * kXBytes, &tmX, &xfull[s], kb * kBK, m0);
-        issued = kb + 1;
+  // The first unit's first weight stages do not depend on the routing: when
+  // most experts receive pairs they are fetched while the route-and-pack
+  // grid may still run.
+  int e_first, n0_first;
+  unit_rows(p, (int)blockIdx.x, e_first, n0_first);
+  const int pre = p.npairs >= p.n_expert ? min(kRawStages, TC) : 0;
+  if (warp == kWProd && lane == 0) {
+    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmP);
+    for (int tc = 0; tc < pre; ++tc)
+      produce_weights<kRawStages>(&tmC, &tmP, p, e_first, n0_first, tc, tc, raw0, w_full, w_empty, abort_flag);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // When the first unit has no pairs, its prefetched stages are consumed and dropped.
+  const bool first_empty = p.offsets != nullptr && p.offsets[e_first + 1] == p.offsets[e_first];
+
+  bool ok = true;
+  int njobs = 0;
+  if (warp < kXW) {
+    // ---- transform: raw tiles -> bf16 weights in TMEM; then the epilogue ----
+    // Warp (q, hw): TMEM lane quarter q (its 32 weight rows), and of each
+    // 128-k stage the 64-k half hw when two warps share a quarter.
+    const int q = warp & 3, hw = warp >> 2;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+    int gws = 0, gs = 0;
+    if (first_empty) {
+      for (; gws < pre && ok; ++gws) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&w_full[gws], 0, abort_flag, p.dev_status));
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(&w_empty[gws]);
       }
-      if (*abort_flag)
-        for (int kb = issued > kStages ? issued - kStages : 0; kb < issued; ++kb)
-          mbar_wait(&xfull[kb % kStages], (kb / kStages) & 1, abort_flag, nullptr, 100000000ull) ||
-              mbar_try_wait(&xfull[kb % kStages], (kb / kStages) & 1);
     }
-  } else if (warp == 1) {
+    Jobs<kTok> jb;
+    while (ok && jb.next(p)) {
+      const int n = jb.n0 + 32 * q + lane;
+      for (int tc = 0; tc < TC && ok; ++tc, ++gws) {
+        const int slot = gws % kRawStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&w_full[slot], (gws / kRawStages) & 1, abort_flag, p.dev_status))) {
+          ok = false;
+          break;
+        }
+        const uint32_t cb = raw0 + slot * kRawBytes + q * kCodeBox + lane * 128;
+        uint4 cw[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+          if (kHalves == 1 || ((b >> 1) & 1) == hw) cw[b] = lds128(cb + 16 * (b ^ (lane & 7)));
+        const uint32_t pb = raw0 + slot * kRawBytes + 4 * kCodeBox + q * kPairBox + (lane >> 2) * 128;
+        const uint4 pr0 = lds128(pb + 16 * ((2 * (lane & 3)) ^ ((lane >> 2) & 7)));
+        const uint4 pr1 = lds128(pb + 16 * ((2 * (lane & 3) + 1) ^ ((lane >> 2) & 7)));
+#pragma unroll
+        for (int h = 0; h < 2; ++h, ++gs) {
+          const int as = gs % kAStages;
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(&a_empty[as], ((gs / kAStages) & 1) ^ 1, abort_flag, p.dev_status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            if (kHalves == 2 && hh != hw) continue;
+            uint32_t v[32];
+#pragma unroll
+            for (int bb = 0; bb < 2; ++bb) {
+              const int b = 4 * h + 2 * hh + bb;
+              const uint32_t pair = u4_get(b < 4 ? pr0 : pr1, b & 3);
+              const uint32_t s2 = __byte_perm(pair, 0, 0x1010), m2 = __byte_perm(pair, 0, 0x3232);
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const uint32_t word = u4_get(cw[b], t);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[16 * bb + 4 * t + i] = dequant2(q4_pair_biased(word, i), s2, m2);
+              }
+            }
+            tmem_st32(trow + kColA + 64 * as + 32 * hh, v);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[as]);
+        }
+        // Every lane has consumed its loads of this raw slot (the values went
+        // into TMEM above), so the producer may refill it.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&w_empty[slot]);
+      }
+    }
+  } else if (warp < kWEpi + 4) {
+    // ---- epilogue: fp32 accumulator -> Y (lane = weight row, column = pair) ----
+    const int q = warp & 3;
+    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+    Jobs<kTok> jb;
+    while (ok && jb.next(p)) {
+      const int n = jb.n0 + 32 * q + lane;
+      const int nt = jb.nt(), ncol = jb.ncol();
+      for (int c = lane; c < nt; c += 32) {
+        int64_t xo;
+        if (kMode == kDense)
+          yoff[q][c] = (int64_t)(jb.pass0 + c) * p.ldy_token;
+        else
+          pair_offsets(p, p.pairs[jb.first + jb.pass0 + c], xo, yoff[q][c]);
+      }
+      __syncwarp();
+      const int db = njobs & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&d_full[db], (njobs >> 1) & 1, abort_flag, p.dev_status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool live = n < p.N;
+      for (int c0 = 0; c0 < ncol; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(trow + (uint32_t)(kTok * db) + c0, v);
+        tmem_wait_ld();
+        if (live) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c0 + i < nt) p.Y[yoff[q][c0 + i] + n] = __uint_as_float(v[i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_empty[db]);
+      ++njobs;
+    }
+  } else if (warp == kWLoad) {
+    // ---- activation loader ----
+    int gs = 0;
+    Jobs<kTok> jb;
+    if (kPacked) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmX);
+        while (ok && jb.next(p)) {
+          const int row0 = jb.first + jb.pass0;
+          for (int ks = 0; ks < nks; ++ks, ++gs) {
+            const int bs = gs % kBStages;
+            if (!mbar_wait(&b_empty[bs], ((gs / kBStages) & 1) ^ 1, abort_flag, p.dev_status)) {
+              ok = false;
+              break;
+            }
+            // whole kTok-row boxes (rows past the job's pairs are junk columns)
+            mbar_arrive_expect_tx(&b_full[bs], (uint32_t)(2 * kBAtomBytes));
+            const uint32_t sb = sB0 + bs * kBBytes;
+            tma_load_2d_u32(sb, &tmX, &b_full[bs], ks * kKC, row0);
+            tma_load_2d_u32(sb + kBAtomBytes, &tmX, &b_full[bs], ks * kKC + 64, row0);
+          }
+        }
+      }
+      __syncwarp();
+    } else {
+      int signalled = 0;   // stages whose b_full has been raised
+      while (ok && jb.next(p)) {
+        const int nt = jb.nt(), ncol = jb.ncol();
+        __syncwarp();   // the previous job's copies have read xoff
+        for (int c = lane; c < nt; c += 32) {
+          int64_t yo;
+          pair_offsets(p, p.pairs[jb.first + jb.pass0 + c], xoff[c], yo);
+        }
+        __syncwarp();
+        for (int ks = 0; ks < nks; ++ks, ++gs) {
+          const int bs = gs % kBStages;
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(&b_empty[bs], ((gs / kBStages) & 1) ^ 1, abort_flag, p.dev_status))) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = sB0 + bs * kBBytes;
+          for (int i = lane; i < ncol * 16; i += 32) {
+            const int c = i >> 4, ch = i & 15;
+            const bool valid = c < nt;
+            const __nv_bfloat16* src = valid ? p.X + xoff[c] + (int64_t)ks * kKC + 8 * ch : p.X;
+            const uint32_t dst = sb + (ch >> 3) * kBAtomBytes + (c >> 3) * 1024 + (c & 7) * 128 +
+                                 (uint32_t)(((ch & 7) ^ (c & 7)) << 4);
+            cp_async16_zfill(dst, src, valid ? 16u : 0u);
+          }
+          cp_async_commit();
+          if (gs + 1 - signalled > kLoaderLag) {
+            cp_async_wait<kLoaderLag>();
+            fence_proxy_async_smem();   // generic-proxy writes -> tcgen05 reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&b_full[signalled % kBStages]);
+            ++signalled;
+          }
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      for (; signalled < gs; ++signalled)
+        if (lane == 0) mbar_arrive(&b_full[signalled % kBStages]);
+    }
+  } else if (warp == kWMma) {
+    // ---- MMA issuer ----
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(kBW, kBT, true);
-      bool ok = true;
-      for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = (kb / kStages) & 1;
-        if (!mbar_wait(&xfull[s], ph, abort_flag, p.dev_status) ||
-            !mbar_wait(&wfull[s], ph, abort_flag, p.dev_status)) {
+      int gs = 0;
+      Jobs<kTok> jb;
+      while (ok && jb.next(p)) {
+        const int db = njobs & 1;
+        const uint32_t idesc = idesc_f16(kRows, jb.ncol(), true);
+        if (!mbar_wait(&d_empty[db], ((njobs >> 1) & 1) ^ 1, abort_flag, p.dev_status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t w_addr = smem_u32(sW + s * kWBytes);
-        const uint32_t x_addr = smem_u32(sX + s * kXBytes);
-#pragma unroll
-        for (int j = 0; j < kBK / 16; ++j)
-          umma_f16(tmem, desc_kmajor_sw128(w_addr + 32 * j), desc_kmajor_sw128(x_addr + 32 * j), idesc,
-                   (kb > 0 || j > 0) ? 1u : 0u);
-        umma_commit(&empty[s]);
-      }
-      if (ok) umma_commit(tfull);
-      umma_commit(done);
-      mbar_wait(done, 0, abort_flag, p.dev_status);
-    }
-  } else {
-    // transform warps 2..5 -> tile row tw, row = lane; then epilogue on TMEM quadrant warp%4
-    const int tw = warp - 2;
-    const int row = 32 * tw + lane;                 // row inside the 128-row tile
-    const int n = n0 + row;
-    const bool valid = n < p.N;
-    const int tr = (valid ? n : 0) / 32;
-    const uint8_t* row_tile0 = p.tiles + (int64_t)tr * TC * kTileBytes + (n & 31) * 128;
-    const uint8_t* pair_tile0 = p.tiles + (int64_t)tr * TC * kTileBytes + 4096 + (n & 31) * 32;
-    RawStage ring[kPrefetch];
-#pragma unroll
-    for (int i = 0; i < kPrefetch; ++i) load_raw(ring[i], row_tile0, pair_tile0, i, valid && i < nkb);
-    bool ok = true;
-    for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPrefetch) {
-#pragma unroll
-      for (int i = 0; i < kPrefetch; ++i) {
-        const int kb = kb0 + i;
-        if (kb < nkb && ok) {
-          const int s = kb % kStages;
-          if (!mbar_wait(&empty[s], ((kb / kStages) & 1) ^ 1, abort_flag, p.dev_status)) {
+        for (int ks = 0; ks < nks; ++ks, ++gs) {
+          const int as = gs % kAStages, bs = gs % kBStages;
+          if (!mbar_wait(&a_full[as], (gs / kAStages) & 1, abort_flag, p.dev_status) ||
+              !mbar_wait(&b_full[bs], (gs / kBStages) & 1, abort_flag, p.dev_status)) {
             ok = false;
-          } else {
-            write_stage(sW + s * kWBytes, row, ring[i]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&wfull[s]);
-            load_raw(ring[i], row_tile0, pair_tile0, kb + kPrefetch, valid && kb + kPrefetch < nkb);
+            break;
           }
-        }
-      }
-    }
-    // epilogue: this warp reads TMEM lanes 32*(warp%4)..; its rows are n0 + 32*(warp%4) + lane
-    const int q = warp & 3;
-    const int nrow = n0 + 32 * q + lane;
-    ok = __all_sync(0xffffffffu, ok);
-    // warp-uniform: tcgen05.ld below is a whole-warp instruction
-    if (ok && __all_sync(0xffffffffu, mbar_wait(tfull, 0, abort_flag, p.dev_status))) {
-      tc_fence_after();
-#pragma unroll 1
-      for (int j = 0; j < kBT / 32; ++j) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * j), r);
-        tmem_wait_ld();
-        if (nrow < p.N) {
+          tc_fence_after();
+          const uint32_t sb = sB0 + bs * kBBytes;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int m = m0 + 32 * j + i;
-            if (m < p.M) p.Y[(int64_t)m * p.ldy + nrow] = __uint_as_float(r[i]);
-          }
+          for (int j = 0; j < kKC / 16; ++j)
+            umma_f16_ta(tmem + (uint32_t)(kTok * db), tmem + kColA + 64 * as + 8 * j,
+                        desc_kmajor_sw128(sb + (j >> 2) * kBAtomBytes + 32 * (j & 3)), idesc,
+                        (ks > 0 || j > 0) ? 1u : 0u);
+          umma_commit(&a_empty[as]);
+          umma_commit(&b_empty[bs]);
         }
+        if (!ok) break;
+        umma_commit(&d_full[db]);
+        ++njobs;
       }
     }
+    __syncwarp();
+  } else {
+    // ---- weight producer ----
+    if (lane == 0) {
+      int gws = pre;
+      Jobs<kTok> jb;
+      bool first = true;
+      while (ok && jb.next(p)) {
+        // the first unit's first stages were issued before the routing wait
+        const int tc0 = (first && !first_empty) ? pre : 0;   // the first job is then the first unit's pass 0
+        first = false;
+        for (int tc = tc0; tc < TC && ok; ++tc, ++gws)
+          ok = produce_weights<kRawStages>(&tmC, &tmP, p, jb.e, jb.n0, tc, gws, raw0, w_full, w_empty, abort_flag);
+      }
+    }
+    __syncwarp();
   }
+
+  // ---- teardown ----
+  cp_async_wait<0>();
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (*abort_flag && lane == 0 && (warp == kWLoad || warp == kWProd)) {
+    // TMA writes of stages nobody consumed may still be in flight
+    uint64_t* full = warp == kWProd ? w_full : b_full;
+    const int n = warp == kWProd ? kRawStages : kBStages;
+    for (int s = 0; s < n; ++s)
+      for (int ph = 0; ph < 2; ++ph)
+        mbar_wait(&full[s], ph, abort_flag, nullptr, 50000000ull) || mbar_try_wait(&full[s], ph);
+  }
+  if (warp == kWMma) {
+    if (lane == 0) {
+      umma_commit(done);   // every MMA of this CTA has completed before TMEM is freed
+      mbar_wait(done, 0, abort_flag, nullptr, 100000000ull) || mbar_try_wait(done, 0);
+    }
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
+// Routing and activation packing in one launch.  Block b owns pairs
+// [b*PB, (b+1)*PB).  Every block reads all ids: the histogram of all pairs
+// gives the expert offsets, and the histogram of the pairs before its own
+// range gives each expert's base rank there.  Warp 0 then ranks the block's
+// pairs in pair order (lanes with the same expert found by match_any), so the
+// grouped list is deterministic.  Finally the block copies its pairs'
+// activation rows to their ranks (when the packed buffer exists).
+constexpr int kRouteThreads = 256;
+constexpr int kRouteMaxPB = 32;   // one warp ranks a block's pairs
+
+__global__ void __launch_bounds__(kRouteThreads)
+moe_route_pack_kernel(const int32_t* __restrict__ ids, int64_t ld_ids, int n_used, int T, int n_expert, int PB,
+                      const __nv_bfloat16* __restrict__ X, int64_t ldx_token, int64_t ldx_slot, int K,
+                      int32_t* __restrict__ offsets, int32_t* __restrict__ pairs, __nv_bfloat16* __restrict__ Xp,
+                      int32_t* dev_status) {
+  extern __shared__ int rsm[];
+  int* off = rsm;                    // [n_expert + 1]: histogram, then exclusive offsets
+  int* before = rsm + n_expert + 1;  // [n_expert]: pairs of each expert before this block's range
+  int* run = before + n_expert;      // [n_expert]: ranked so far inside this block
+  __shared__ int wsum[kRouteThreads / 32];
+  __shared__ int rank_s[kRouteMaxPB];
+  __shared__ int pair_s[kRouteMaxPB];
+  // the grouped kernel may start now: it prefetches weights, then waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int npairs = T * n_used;
+  const int p0 = blockIdx.x * PB;
+  for (int e = tid; e <= n_expert; e += kRouteThreads) off[e] = 0;
+  for (int e = tid; e < n_expert; e += kRouteThreads) before[e] = run[e] = 0;
+  __syncthreads();
+  bool bad = false;
+  // eight independent loads in flight per thread, then the shared-memory counts
+  for (int base = 0; base < npairs; base += 8 * kRouteThreads) {
+    int ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int pr = base + u * kRouteThreads + tid;
+      ev[u] = pr < npairs ? ids[(int64_t)(pr / n_used) * ld_ids + (pr % n_used)] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int pr = base + u * kRouteThreads + tid;
+      if (pr >= npairs) continue;
+      const int e = ev[u];
+      if (e < 0 || e >= n_expert) {
+        bad = true;
+        continue;
+      }
+      atomicAdd(&off[e], 1);
+      if (pr < p0) atomicAdd(&before[e], 1);
+    }
+  }
+  if (bad && blockIdx.x == 0) set_status(dev_status, QMM_ERR_BAD_EXPERT_ID);
+  __syncthreads();
+  // exclusive scan of off[0 .. n_expert) in place; off[n_expert] = total
+  {
+    const int per = (n_expert + kRouteThreads - 1) / kRouteThreads;
+    const int lo = min(tid * per, n_expert), hi = min(lo + per, n_expert);
+    int seg = 0;
+    for (int e = lo; e < hi; ++e) seg += off[e];
+    int incl = seg;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += u;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int wbase = 0, total = 0;
+    for (int w = 0; w < kRouteThreads / 32; ++w) {
+      wbase += (w < warp) ? wsum[w] : 0;
+      total += wsum[w];
+    }
+    int runv = wbase + incl - seg;
+    __syncthreads();   // every thread has read its segment before any is overwritten
+    for (int e = lo; e < hi; ++e) {
+      const int c = off[e];
+      off[e] = runv;
+      runv += c;
+    }
+    if (tid == 0) off[n_expert] = total;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = tid; e <= n_expert; e += kRouteThreads) offsets[e] = off[e];
+  // rank this block's pairs in pair order
+  const int nb = min(PB, npairs - p0);
+  if (warp == 0) {
+    for (int j0 = 0; j0 < nb; j0 += 32) {
+      const int j = j0 + lane;
+      const int pr = p0 + j;
+      int e = -1;
+      if (j < nb) {
+        e = ids[(int64_t)(pr / n_used) * ld_ids + (pr % n_used)];
+        if (e < 0 || e >= n_expert) e = -1;
+      }
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      const int local = __popc(same & ((1u << lane) - 1u));
+      int rank = -1;
+      if (e >= 0) rank = off[e] + before[e] + run[e] + local;
+      __syncwarp();
+      if (e >= 0 && local == 0) run[e] += __popc(same);
+      __syncwarp();
+      if (j < nb) {
+        rank_s[j] = rank;
+        pair_s[j] = pr;
+        if (rank >= 0) pairs[rank] = pr;
+      }
+    }
+  }
+  if (Xp == nullptr) return;
+  __syncthreads();
+  // copy: 16-byte units, eight loads in flight per thread
+  const int chunks = K / 8;
+  const int units = nb * chunks;
+  for (int base = 0; base < units; base += 8 * kRouteThreads) {
+    uint4 v[8];
+    int dst_rank[8], c8[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int idx = base + u * kRouteThreads + tid;
+      dst_rank[u] = -1;
+      if (idx < units) {
+        const int j = idx / chunks;
+        c8[u] = idx - j * chunks;
+        dst_rank[u] = rank_s[j];
+        if (dst_rank[u] >= 0) {
+          const int pr = pair_s[j];
+          const uint4* src = reinterpret_cast<const uint4*>(X + (int64_t)(pr / n_used) * ldx_token +
+                                                            (int64_t)(pr % n_used) * ldx_slot);
+          v[u] = ldg128(src + c8[u]);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (dst_rank[u] >= 0) reinterpret_cast<uint4*>(Xp + (int64_t)dst_rank[u] * K)[c8[u]] = v[u];
+  }
+}
+
+template <int kMode, int kTok, int kXW>
+cudaError_t launch_tc(const CUtensorMap& tmC, const CUtensorMap& tmP, const CUtensorMap& tmX, const MoeParams& p,
+                      cudaStream_t stream) {
+  auto kern = q4_tc_kernel<kMode, kTok, kXW>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<kTok>::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)min(p.n_units, sms));   // persistent, one CTA per SM
+  cfg.blockDim = dim3(32 * (kXW + 7));
+  cfg.dynamicSmemBytes = Cfg<kTok>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;   // overlap the route-and-pack grid
+  cfg.attrs = attr;
+  cfg.numAttrs = kMode == kDense ? 0 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmC, tmP, tmX, p);
+}
+
 }  // namespace
+
+size_t q4_moe_table_bytes(int64_t n_expert, int64_t n_used, int64_t T) {
+  const size_t off = ((size_t)(n_expert + 1) * 4 + 255) / 256 * 256;
+  return off + ((size_t)(T * n_used) * 4 + 255) / 256 * 256;
+}
+
+size_t q4_moe_workspace_bytes(int64_t n_expert, int64_t n_used, int64_t T, int64_t K) {
+  return q4_moe_table_bytes(n_expert, n_used, T) + (size_t)(T * n_used) * (size_t)K * 2;
+}
+
+cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream) {
+  MoeParams p{};
+  p.tiles_per_expert = (int64_t)(a.N / 32) * (a.K / 256);
+  p.N = a.N;
+  p.K = a.K;
+  p.X = a.X;
+  p.ldx_token = a.ldx_token;
+  p.ldx_slot = a.ldx_slot;
+  p.n_used = a.n_used;
+  p.n_expert = a.n_expert;
+  p.npairs = a.T * a.n_used;
+  p.nrb = (a.N + kRows - 1) / kRows;
+  p.n_units = a.n_expert * p.nrb;
+  p.Y = a.Y;
+  p.ldy_token = a.ldy_token;
+  p.ldy_slot = a.ldy_slot;
+  p.offsets = a.offsets;
+  p.pairs = a.pairs;
+  p.dev_status = a.dev_status;
+  const uint64_t n_tiles = (uint64_t)a.n_expert * (uint64_t)p.tiles_per_expert;
+  if (n_tiles > (uint64_t)INT32_MAX || (int64_t)a.n_expert * p.nrb > INT32_MAX) return cudaErrorInvalidValue;
+  CUtensorMap tmC, tmP, tmX;
+  const uint64_t tile_rows = (uint64_t)a.n_expert * (uint64_t)(a.N / 32);
+  if (!make_tmap_q4_tiles(&tmC, a.tiles, (uint64_t)(a.K / 256), tile_rows, 32) ||
+      !make_tmap_q4_tiles(&tmP, a.tiles, (uint64_t)(a.K / 256), tile_rows, 8))
+    return cudaErrorInvalidValue;
+  const int npairs = a.T * a.n_used;
+  // 8 pairs per block (one round of row loads per block), more when the
+  // batch is large enough that every block rereading all ids would cost more
+  int PB = 8;
+  while (PB < kRouteMaxPB && (int64_t)npairs * ((npairs + PB - 1) / PB) > (int64_t)64 << 20) PB *= 2;
+  const int nblk = (npairs + PB - 1) / PB;
+  const size_t rsmem = (size_t)(3 * a.n_expert + 1) * sizeof(int);
+  if (rsmem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(moe_route_pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)rsmem);
+    if (e != cudaSuccess) return e;
+  }
+  moe_route_pack_kernel<<<nblk, kRouteThreads, rsmem, stream>>>(
+      a.ids, a.ld_ids, a.n_used, a.T, a.n_expert, PB, a.X, a.ldx_token, a.ldx_slot, a.K, a.offsets, a.pairs,
+      a.xperm, a.dev_status);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if (a.xperm == nullptr) return launch_tc<kTableGather, 64, 8>(tmC, tmP, tmC, p, stream);
+  if (!make_tmap_2d(&tmX, true, a.xperm, (uint64_t)a.K, (uint64_t)npairs, (uint64_t)a.K * 2, 64, 64))
+    return cudaErrorInvalidValue;
+  return launch_tc<kTablePacked, 64, 8>(tmC, tmP, tmX, p, stream);
+}
 
 bool q4_umma_eligible(int64_t M, int64_t N, int64_t K) {
   (void)N;
   (void)K;
-  return M >= kMinM;
+  return M >= 17;   // M <= 16 runs the decode GEMV kernels
 }
 
 cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream) {
-  CUtensorMap tmX;
-  if (!make_tmap_2d(&tmX, true, const_cast<__nv_bfloat16*>(a.X), (uint64_t)a.K, (uint64_t)a.M,
-                    (uint64_t)a.ldx * 2, kBK, kBT))
-    return cudaErrorInvalidValue;
-  Q4UmmaParams p{};
-  p.tiles = a.tiles;
+  MoeParams p{};
+  p.tiles_per_expert = (int64_t)(a.N / 32) * (a.K / 256);
   p.N = a.N;
   p.K = a.K;
-  p.M = a.M;
+  p.X = a.X;
+  p.ldx_token = a.ldx;
+  p.n_used = 1;
+  p.n_expert = 1;
+  p.npairs = a.M;
+  p.nrb = (a.N + kRows - 1) / kRows;
+  p.n_units = p.nrb;
   p.Y = a.Y;
-  p.ldy = a.ldy;
+  p.ldy_token = a.ldy;
+  p.dense_rows = a.M;
   p.dev_status = dev_status;
-  cudaError_t err =
-      cudaFuncSetAttribute(q4_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (err != cudaSuccess) return err;
-  dim3 grid((unsigned)((a.N + kBW - 1) / kBW), (unsigned)((a.M + kBT - 1) / kBT));
-  q4_umma_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmX, p);
-  return cudaGetLastError();
+  if (p.tiles_per_expert > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+  CUtensorMap tmC, tmP, tmX;
+  if (!make_tmap_q4_tiles(&tmC, a.tiles, (uint64_t)(a.K / 256), (uint64_t)(a.N / 32), 32) ||
+      !make_tmap_q4_tiles(&tmP, a.tiles, (uint64_t)(a.K / 256), (uint64_t)(a.N / 32), 8))
+    return cudaErrorInvalidValue;
+  const uint32_t box_rows = a.M <= 64 ? 64 : 128;
+  if (!make_tmap_2d(&tmX, true, const_cast<__nv_bfloat16*>(a.X), (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.ldx * 2,
+                    64, box_rows))
+    return cudaErrorInvalidValue;
+  if (a.M <= 64) {
+    p.dense_chunks = 1;
+    p.n_units = p.nrb;
+    return launch_tc<kDense, 64, 8>(tmC, tmP, tmX, p, stream);
+  }
+  p.dense_chunks = (a.M + 127) / 128;
+  if ((int64_t)p.nrb * p.dense_chunks > INT32_MAX) return cudaErrorInvalidValue;
+  p.n_units = p.nrb * p.dense_chunks;
+  return launch_tc<kDense, 128, 8>(tmC, tmP, tmX, p, stream);
 }
 
 }  // namespace qmm

@@ -22,10 +22,11 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 bool make_tmap_2d(CUtensorMap* map, bool is_bf16_or_f16, void* base, uint64_t inner, uint64_t rows,
                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
 
-// q4 tiles as a 3-D byte tensor {128 bytes, 40 rows, n_tiles}, 128-byte
-// swizzle, box {128, box_rows, 1}: rows 0..31 of a tile are its codes, rows
-// 32..39 its (scale, min) pairs.
-bool make_tmap_q4_tiles(CUtensorMap* map, const void* tiles, uint64_t n_tiles, uint32_t box_rows);
+// q4 tiles as a 4-D byte tensor {128 bytes, 40 rows, tile_cols, tile_rows},
+// 128-byte swizzle, box {128, box_rows, 1, 4}: rows 0..31 of a tile are its
+// codes, rows 32..39 its (scale, min) pairs; one box covers 4 tile rows.
+bool make_tmap_q4_tiles(CUtensorMap* map, const void* tiles, uint64_t tile_cols, uint64_t tile_rows,
+                        uint32_t box_rows);
 
 // ---- packs (pack.cu) ----
 cudaError_t launch_pack_b_int8(const void* B, qmm_dtype b_type, int64_t K, int64_t N, int64_t ldb,

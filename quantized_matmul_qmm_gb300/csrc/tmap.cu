@@ -42,15 +42,18 @@ bool make_tmap_2d(CUtensorMap* map, bool is_bf16_or_f16, void* base, uint64_t in
   return r == CUDA_SUCCESS;
 }
 
-bool make_tmap_q4_tiles(CUtensorMap* map, const void* tiles, uint64_t n_tiles, uint32_t box_rows) {
+bool make_tmap_q4_tiles(CUtensorMap* map, const void* tiles, uint64_t tile_cols, uint64_t tile_rows,
+                        uint32_t box_rows) {
   std::call_once(g_once, resolve);
   if (g_encode == nullptr) return false;
-  // a tile is 40 rows of 128 bytes: 32 code rows, then 8 rows of (scale, min) pairs
-  const cuuint64_t dims[3] = {128, 40, n_tiles};
-  const cuuint64_t strides[2] = {128, (cuuint64_t)kTileBytes};
-  const cuuint32_t box[3] = {128, box_rows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(tiles), dims, strides, box,
+  // A tile is 40 rows of 128 bytes: 32 code rows, then 8 rows of (scale, min)
+  // pairs.  Tiles are [tile row][tile column]; a box spans 4 tile rows of one
+  // tile column, so that one TMA fetches a 128-row unit's stage.
+  const cuuint64_t dims[4] = {128, 40, tile_cols, tile_rows};
+  const cuuint64_t strides[3] = {128, (cuuint64_t)kTileBytes, (cuuint64_t)kTileBytes * tile_cols};
+  const cuuint32_t box[4] = {128, box_rows, 1, 4};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(tiles), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

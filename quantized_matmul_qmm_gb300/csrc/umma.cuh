@@ -43,6 +43,18 @@ QMM_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Same, but the thread may be suspended (not spinning, not issuing) for up to
+// hint_ns while the phase is incomplete; it resumes when the phase completes.
+QMM_DEV bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 QMM_DEV uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -54,19 +66,18 @@ QMM_DEV uint64_t globaltimer_ns() {
 // Every other wait of the CTA then returns false at once, every role leaves
 // its loop, and the kernel frees its TMEM and exits cleanly.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr uint32_t kSuspendHintNs = 200000;         // 0.2 ms per suspended try
 QMM_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
                        uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
-        *abort_flag = 1;
-        set_status(status, QMM_ERR_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      set_status(status, QMM_ERR_TIMEOUT);
+      return false;
     }
   }
 }
@@ -85,6 +96,14 @@ QMM_DEV void tma_load_2d_u32(uint32_t dst, const CUtensorMap* map, uint64_t* bar
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
           dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+// 4-D tiled load; c0 innermost.
+QMM_DEV void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 // 3-D tiled load; c0 innermost.
