@@ -14,11 +14,11 @@
 // its expert's (token, slot) pairs, up to kTok (64, or 128 for a large dense
 // M) per job.  Each weight is read from HBM once per job and used for all of
 // the job's pairs: the grouped dispatch the pages credit for the MoE
-// speed-up.  The grid is persistent (one CTA per SM); every role walks the
-// CTA's units in the same order, and the pipelines run on across unit
-// boundaries, so the next unit's weights stream in while the current one
-// finishes.  The fp32 accumulator is double buffered in TMEM and drained by
-// warps of its own, so a job's epilogue overlaps the next job's MMAs.
+// speed-up.  The grid is persistent (two CTAs per SM for MUL_MAT_ID, one for
+// the dense GEMM); every role walks the CTA's units in the same order, and
+// the pipelines run on across unit boundaries, so the next unit's weights
+// stream in while the current one finishes.  The fp32 accumulator is double
+// buffered in TMEM, so a job's epilogue overlaps the next job's MMAs.
 //
 // Routing.  A route-and-pack kernel (one block per 8 pairs) writes per-expert
 // offsets and the grouped (token, slot) list into the caller's workspace, in
@@ -34,20 +34,20 @@
 // the M = 128 side and the pairs as N (16..kTok).  The dequantised weights go
 // from registers straight into TMEM, which tcgen05.mma reads as its A
 // operand, so they never pass through shared memory; only the raw tiles and
-// the activations do.  TMEM: two accumulators of kTok columns, then four A
-// buffers of 64 columns (128 k).  Roles (480 threads):
-//   warp 14    weight producer: TMA of whole tile columns (the 4 tiles of the
-//              unit's rows, codes and pairs as two boxes each) into a ring,
-//              128-byte swizzle.
-//   warps 0-7  transform: warp (q, h) owns TMEM lane quarter q (one weight row
-//              per lane) and 64-k half h of every 128-k stage: it reads the
-//              rows' codes and pairs, forms w = bf16(q * s + m) with one
-//              rounding, and stores the stage into an A buffer (tcgen05.st).
-//   warps 8-11 epilogue: drain a finished accumulator (tcgen05.ld) into Y.
-//   warp 12    activation loader: TMA of the packed rows (or of X for the
-//              dense GEMM), or a cp.async gather, into the 128-byte-swizzle
-//              K-major layout.
-//   warp 13    TMEM owner; lane 0 issues tcgen05.mma (kind::f16, bf16).
+// the activations do.  TMEM: two accumulators of kTok columns, then two or
+// four A buffers of 64 columns (128 k).  Roles, in warp order:
+//   transform  four or eight warps; warp (q, h) owns TMEM lane quarter q (one
+//              weight row per lane) and, with eight, 64-k half h of every
+//              128-k stage: it reads the rows' codes and pairs, forms
+//              w = bf16(q * s + m) with one rounding, and stores the stage into
+//              an A buffer (tcgen05.st).  With four, they also drain each
+//              job's accumulator into Y.
+//   epilogue   (one CTA per SM) four warps draining accumulators into Y.
+//   loader     TMA of the packed rows (or of X for the dense GEMM), or a
+//              cp.async gather, into the 128-byte-swizzle K-major layout.
+//   MMA        TMEM owner; lane 0 issues tcgen05.mma (kind::f16, bf16).
+//   producer   TMA of whole tile columns: one box for the unit's 4 tiles'
+//              codes, one for their pairs, 128-byte swizzle.
 // Every wait is bounded; a timeout sets the caller's status word and the CTA
 // leaves cleanly.
 #include <cuda_bf16.h>
@@ -64,7 +64,7 @@ constexpr int kRows = 128;                          // weight rows per unit (MMA
 constexpr int kKC = 128;                            // K per MMA / activation stage
 constexpr int kRawStagesMax = 4;                    // weight ring, one tile column (256 k) per stage
 constexpr int kBStagesMax = 4;
-constexpr int kAStages = 4;                         // TMEM A buffers of 64 columns (128 k)
+constexpr int kAStagesMax = 4;
 constexpr int kCodeBox = 4096;                      // 32 code rows x 128 B
 constexpr int kPairBox = 1024;                      // 8 pair rows x 128 B
 constexpr int kRawBytes = 4 * (kCodeBox + kPairBox);   // 4 tile rows: codes [4][4 KB], then pairs [4][1 KB]
@@ -73,14 +73,23 @@ constexpr int kLoaderLag = 2;                       // gathered activation stage
 // Sizes that follow from the largest job width kTok (the MMA's N): two fp32
 // accumulators of kTok columns, then two A buffers of 64 columns in TMEM;
 // activation stages of kTok rows x 128 k.
-template <int kTok>
-struct Cfg {
-  static constexpr int kRawStages = kTok == 64 ? 4 : 3;
-  static constexpr int kBStages = 4;                // activation ring depth
-  static constexpr int kBAtomBytes = kTok * 128;    // kTok rows x 64 k bf16, 128-byte swizzle
-  static constexpr int kBBytes = 2 * kBAtomBytes;   // 128 k per stage
-  static constexpr uint32_t kColA = 2 * kTok;       // after the two accumulators
-  static constexpr uint32_t kTmemCols = 512;
+// Two CTA layouts.  Two CTAs per SM (MUL_MAT_ID: small jobs, so two units
+// in flight per SM hide each other's fill and drain): four transform warps
+// that also drain the accumulator, two A buffers, TMEM 256 columns.  One CTA
+// per SM (dense prefill): eight transform warps, four epilogue warps, four A
+// buffers, TMEM 512 columns, deeper rings.  kTok is the widest job (MMA N).
+template <int kTok, int kCtas>
+struct Lay {
+  static constexpr int kXW = kCtas == 2 ? 4 : 8;           // transform warps
+  static constexpr bool kSepEpi = kCtas == 1;              // epilogue warps of their own
+  static constexpr int kWarps = kXW + (kSepEpi ? 4 : 0) + 3;
+  static constexpr int kAStages = kCtas == 2 ? 2 : 4;       // TMEM A buffers of 64 columns (128 k)
+  static constexpr int kRawStages = kCtas == 2 ? 3 : (kTok == 64 ? 4 : 3);
+  static constexpr int kBStages = kCtas == 2 ? 3 : 4;       // activation ring depth
+  static constexpr int kBAtomBytes = kTok * 128;           // kTok rows x 64 k bf16, 128-byte swizzle
+  static constexpr int kBBytes = 2 * kBAtomBytes;          // 128 k per stage
+  static constexpr uint32_t kColA = 2 * kTok;              // after the two accumulators
+  static constexpr uint32_t kTmemCols = kCtas == 2 ? 256 : 512;
   static constexpr size_t kSmemBytes = 1024 + (size_t)kBStages * kBBytes + (size_t)kRawStages * kRawBytes + 256;
   static_assert(kColA + 64 * kAStages <= kTmemCols, "TMEM budget");
 };
@@ -94,8 +103,8 @@ enum MoeMode { kTableGather = 0, kTablePacked = 1, kDense = 2 };
 constexpr int kBarWFull = 0;
 constexpr int kBarWEmpty = kBarWFull + kRawStagesMax;
 constexpr int kBarAFull = kBarWEmpty + kRawStagesMax;
-constexpr int kBarAEmpty = kBarAFull + kAStages;
-constexpr int kBarBFull = kBarAEmpty + kAStages;
+constexpr int kBarAEmpty = kBarAFull + kAStagesMax;
+constexpr int kBarBFull = kBarAEmpty + kAStagesMax;
 constexpr int kBarBEmpty = kBarBFull + kBStagesMax;
 constexpr int kBarDFull = kBarBEmpty + kBStagesMax;
 constexpr int kBarDEmpty = kBarDFull + 2;
@@ -193,22 +202,62 @@ __device__ __forceinline__ bool produce_weights(const CUtensorMap* tmC, const CU
   return true;
 }
 
-template <int kMode, int kTok, int kXW>
-__global__ void __launch_bounds__(32 * (kXW + 7), 1)
+// Drain job `jb`'s accumulator (buffer njobs & 1) for TMEM lane quarter q into
+// Y: lane = weight row, column = pair.  Returns false after an abort.
+template <int kMode, int kTok>
+__device__ __forceinline__ bool epilogue_job(const MoeParams& p, const Jobs<kTok>& jb, int q, int lane, uint32_t tmem,
+                                             int njobs, uint64_t* d_full, uint64_t* d_empty, int64_t* yoff_q,
+                                             volatile int* abort_flag) {
+  const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+  const int n = jb.n0 + 32 * q + lane;
+  const int nt = jb.nt(), ncol = jb.ncol();
+  for (int c = lane; c < nt; c += 32) {
+    int64_t xo;
+    if (kMode == kDense)
+      yoff_q[c] = (int64_t)(jb.pass0 + c) * p.ldy_token;
+    else
+      pair_offsets(p, p.pairs[jb.first + jb.pass0 + c], xo, yoff_q[c]);
+  }
+  __syncwarp();
+  const int db = njobs & 1;
+  if (!__all_sync(0xffffffffu, mbar_wait(&d_full[db], (njobs >> 1) & 1, abort_flag, p.dev_status))) return false;
+  tc_fence_after();
+  const bool live = n < p.N;
+  for (int c0 = 0; c0 < ncol; c0 += 16) {
+    uint32_t v[16];
+    tmem_ld16(trow + (uint32_t)(kTok * db) + c0, v);
+    tmem_wait_ld();
+    if (live) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (c0 + i < nt) p.Y[yoff_q[c0 + i] + n] = __uint_as_float(v[i]);
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&d_empty[db]);
+  return true;
+}
+
+template <int kMode, int kTok, int kCtas>
+__global__ void __launch_bounds__(32 * Lay<kTok, kCtas>::kWarps, kCtas)
 q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
              const __grid_constant__ CUtensorMap tmX, const MoeParams p) {
   constexpr bool kPacked = kMode != kTableGather;   // activations by TMA
-  constexpr int kRawStages = Cfg<kTok>::kRawStages;
-  constexpr int kBStages = Cfg<kTok>::kBStages;
-  constexpr int kBAtomBytes = Cfg<kTok>::kBAtomBytes;
-  constexpr int kBBytes = Cfg<kTok>::kBBytes;
-  constexpr uint32_t kColA = Cfg<kTok>::kColA;
-  constexpr uint32_t kTmemCols = Cfg<kTok>::kTmemCols;
-  // warps 0 .. kXW-1 transform (kXW / 4 per TMEM lane quarter), then four
-  // epilogue warps (one per quarter), the activation loader, the MMA issuer
+  using L = Lay<kTok, kCtas>;
+  constexpr int kXW = L::kXW;
+  constexpr int kRawStages = L::kRawStages;
+  constexpr int kAStages = L::kAStages;
+  constexpr int kBStages = L::kBStages;
+  constexpr int kBAtomBytes = L::kBAtomBytes;
+  constexpr int kBBytes = L::kBBytes;
+  constexpr uint32_t kColA = L::kColA;
+  constexpr uint32_t kTmemCols = L::kTmemCols;
+  // warps 0 .. kXW-1 transform (kXW / 4 per TMEM lane quarter), then (one CTA
+  // per SM) four epilogue warps, then the activation loader, the MMA issuer
   // and the weight producer
   constexpr int kHalves = kXW / 4;
-  constexpr int kWEpi = kXW, kWLoad = kXW + 4, kWMma = kXW + 5, kWProd = kXW + 6;
+  constexpr int kWEpi = kXW, kWLoad = kXW + (L::kSepEpi ? 4 : 0), kWMma = kWLoad + 1, kWProd = kWLoad + 2;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int64_t xoff[kTok];      // gather mode: the loader warp's rows of the current job
   __shared__ int64_t yoff[4][kTok];   // each epilogue warp's output rows of its current job
@@ -348,43 +397,17 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) mbar_arrive(&w_empty[slot]);
       }
+      if (!L::kSepEpi && ok) {
+        ok = epilogue_job<kMode, kTok>(p, jb, q, lane, tmem, njobs, d_full, d_empty, yoff[q], abort_flag);
+        ++njobs;
+      }
     }
-  } else if (warp < kWEpi + 4) {
+  } else if (L::kSepEpi && warp < kWEpi + 4) {
     // ---- epilogue: fp32 accumulator -> Y (lane = weight row, column = pair) ----
     const int q = warp & 3;
-    const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
     Jobs<kTok> jb;
     while (ok && jb.next(p)) {
-      const int n = jb.n0 + 32 * q + lane;
-      const int nt = jb.nt(), ncol = jb.ncol();
-      for (int c = lane; c < nt; c += 32) {
-        int64_t xo;
-        if (kMode == kDense)
-          yoff[q][c] = (int64_t)(jb.pass0 + c) * p.ldy_token;
-        else
-          pair_offsets(p, p.pairs[jb.first + jb.pass0 + c], xo, yoff[q][c]);
-      }
-      __syncwarp();
-      const int db = njobs & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&d_full[db], (njobs >> 1) & 1, abort_flag, p.dev_status))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const bool live = n < p.N;
-      for (int c0 = 0; c0 < ncol; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(trow + (uint32_t)(kTok * db) + c0, v);
-        tmem_wait_ld();
-        if (live) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c0 + i < nt) p.Y[yoff[q][c0 + i] + n] = __uint_as_float(v[i]);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&d_empty[db]);
+      ok = epilogue_job<kMode, kTok>(p, jb, q, lane, tmem, njobs, d_full, d_empty, yoff[q], abort_flag);
       ++njobs;
     }
   } else if (warp == kWLoad) {
@@ -669,19 +692,19 @@ moe_route_pack_kernel(const int32_t* __restrict__ ids, int64_t ld_ids, int n_use
   }
 }
 
-template <int kMode, int kTok, int kXW>
+template <int kMode, int kTok, int kCtas>
 cudaError_t launch_tc(const CUtensorMap& tmC, const CUtensorMap& tmP, const CUtensorMap& tmX, const MoeParams& p,
                       cudaStream_t stream) {
-  auto kern = q4_tc_kernel<kMode, kTok, kXW>;
-  cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<kTok>::kSmemBytes);
+  using L = Lay<kTok, kCtas>;
+  auto kern = q4_tc_kernel<kMode, kTok, kCtas>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmemBytes);
   if (err != cudaSuccess) return err;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)min(p.n_units, sms));   // persistent, one CTA per SM
-  cfg.blockDim = dim3(32 * (kXW + 7));
-  cfg.dynamicSmemBytes = Cfg<kTok>::kSmemBytes;
+  cfg.gridDim = dim3((unsigned)min(p.n_units, kCtas * sms));   // persistent
+  cfg.blockDim = dim3(32 * L::kWarps);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -745,10 +768,10 @@ cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream) {
       a.xperm, a.dev_status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  if (a.xperm == nullptr) return launch_tc<kTableGather, 64, 8>(tmC, tmP, tmC, p, stream);
+  if (a.xperm == nullptr) return launch_tc<kTableGather, 64, 2>(tmC, tmP, tmC, p, stream);
   if (!make_tmap_2d(&tmX, true, a.xperm, (uint64_t)a.K, (uint64_t)npairs, (uint64_t)a.K * 2, 64, 64))
     return cudaErrorInvalidValue;
-  return launch_tc<kTablePacked, 64, 8>(tmC, tmP, tmX, p, stream);
+  return launch_tc<kTablePacked, 64, 2>(tmC, tmP, tmX, p, stream);
 }
 
 bool q4_umma_eligible(int64_t M, int64_t N, int64_t K) {
@@ -785,12 +808,12 @@ cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaS
   if (a.M <= 64) {
     p.dense_chunks = 1;
     p.n_units = p.nrb;
-    return launch_tc<kDense, 64, 8>(tmC, tmP, tmX, p, stream);
+    return launch_tc<kDense, 64, 1>(tmC, tmP, tmX, p, stream);
   }
   p.dense_chunks = (a.M + 127) / 128;
   if ((int64_t)p.nrb * p.dense_chunks > INT32_MAX) return cudaErrorInvalidValue;
   p.n_units = p.nrb * p.dense_chunks;
-  return launch_tc<kDense, 128, 8>(tmC, tmP, tmX, p, stream);
+  return launch_tc<kDense, 128, 1>(tmC, tmP, tmX, p, stream);
 }
 
 }  // namespace qmm
