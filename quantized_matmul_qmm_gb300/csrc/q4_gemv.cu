@@ -22,7 +22,15 @@
 // reads blocks t and t+4 of those rows (two 16-byte loads per row) and the
 // (scale, min) pairs of blocks 2t and 2t+1 (its D columns).  Lanes with
 // (g & 3) == t supply x of block g.
+//
+// Weight stream.  A tile row (32 outputs, all of K) is TC = K/256 contiguous
+// tiles.  One producer thread copies whole tile rows into a ring in shared
+// memory with bulk asynchronous copies (one TMA request of TC * 5120 bytes per
+// row: TMA pays a fixed cost per request, so requests are made large).  Two
+// consumer warps share each row (one 16-row slab each), four rows at a time.  Loads kept in registers
+// (q4_gemv1_regs_kernel) remain for tile rows too long for a useful ring.
 #include "qmm_internal.h"
+#include "umma.cuh"
 
 namespace qmm {
 namespace {
@@ -52,8 +60,8 @@ QMM_DEV uint2 ldg64(const void* p) {
 
 // Fragment data of thread (g, t) straight from the tile in global memory:
 // blocks t and t+4 of rows r0 and r0+8 (16 bytes each) and the pairs of
-// blocks 2t, 2t+1.  Plain 128-bit loads kept out of L1 stream the weights at
-// a higher rate on this part than cp.async or bulk copies into shared memory.
+// blocks 2t, 2t+1, with plain 128-bit loads kept out of L1 (the path for tile
+// rows too long for the streaming kernel's ring).
 QMM_DEV void g1_load(G1Tile& d, const uint8_t* tile, int r0, int t) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -116,7 +124,7 @@ struct G1Cursor {
 // ...), and their partial sums are added in a fixed order through shared
 // memory.  Each warp walks its (group, tile) items as one flat sequence, so
 // the prefetch runs across group boundaries.
-__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) q4_gemv1_kernel(const Gemv1Params p) {
+__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) q4_gemv1_regs_kernel(const Gemv1Params p) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int TC = p.K / 256;
   __nv_bfloat16* xs_sm = reinterpret_cast<__nv_bfloat16*>(sm);                 // [K] + 32 zeros
@@ -219,16 +227,187 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) q4_gemv1_kernel(const
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Streaming M = 1 GEMV: bulk copies of whole tile rows into a shared ring.
+// ---------------------------------------------------------------------------
+constexpr int kSWarps = 8;                       // consumer warps, in pairs
+constexpr int kSThreads = 32 * (kSWarps + 1);    // + the producer warp
+constexpr size_t kRingBudget = 192 * 1024;
+constexpr int kMaxSlots = 16;
+
+struct Gemv1SParams {
+  const uint8_t* tiles;
+  int N, K;
+  const __nv_bfloat16* X;
+  float* Y;
+  int slots;                                     // ring slots of one tile row each
+  int32_t* dev_status;
+};
+
+// Fragment data of thread (g, t) from a tile held in shared memory.
+QMM_DEV void g1_lds(G1Tile& d, uint32_t tile, int r0, int t) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t row = tile + (uint32_t)((r0 + 8 * h) * 128);
+    d.c[h][0] = umma::lds128(row + 16 * t);
+    d.c[h][1] = umma::lds128(row + 16 * (t + 4));
+    uint2 pv;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(pv.x), "=r"(pv.y)
+                 : "r"(tile + 4096u + (uint32_t)((r0 + 8 * h) * 32 + 8 * t)));
+    d.p[h] = pv;
+  }
+}
+
+QMM_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(umma::smem_u32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kSThreads, 1) q4_gemv1_kernel(const Gemv1SParams p) {
+  using namespace umma;
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = smem_align(sm_raw, 128);
+  const int TC = p.K / 256;
+  const uint32_t row_bytes = (uint32_t)TC * (uint32_t)kTileBytes;
+  uint8_t* ring = sm;                                                           // [slots][row_bytes]
+  __nv_bfloat16* xs_sm = reinterpret_cast<__nv_bfloat16*>(ring + (size_t)p.slots * row_bytes);  // [K] + 32 zeros
+  float* xsum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs_sm) + (size_t)p.K * 2 + 64);
+  uint64_t* full = reinterpret_cast<uint64_t*>(xsum + p.K / 32 + 2);         // [slots]
+  uint64_t* empty = full + kMaxSlots;                                         // [slots]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMaxSlots);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int nrows = p.N / 32;                                                 // tile rows
+  const int my_rows = (int)blockIdx.x < nrows ? (nrows - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.slots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 2);   // the two warps of a pair
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == kSWarps) {
+    // ---- producer: tile rows blockIdx.x, blockIdx.x + gridDim.x, ... ----
+    if (lane == 0) {
+      for (int j = 0; j < my_rows; ++j) {
+        const int s = j % p.slots;
+        if (!mbar_wait(&empty[s], ((j / p.slots) & 1) ^ 1, abort_flag, p.dev_status)) break;
+        const int tr = (int)blockIdx.x + j * (int)gridDim.x;
+        mbar_arrive_expect_tx(&full[s], row_bytes);
+        bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), p.tiles + (int64_t)tr * row_bytes, row_bytes, &full[s]);
+      }
+    }
+    // the copies in flight land before the CTA exits: consumers wait for every row
+    return;
+  }
+
+  // ---- consumers: x into shared memory, then rows j = warp, warp + 8, ... ----
+  for (int i = threadIdx.x; i < p.K / 8; i += kSWarps * 32)
+    reinterpret_cast<uint4*>(xs_sm)[i] = reinterpret_cast<const uint4*>(p.X)[i];
+  if (threadIdx.x < 4) reinterpret_cast<uint4*>(xs_sm + p.K)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+  asm volatile("bar.sync 1, %0;" ::"n"(kSWarps * 32) : "memory");
+  for (int b = threadIdx.x; b < p.K / 32; b += kSWarps * 32) {
+    const uint4* xp = reinterpret_cast<const uint4*>(xs_sm + 32 * b);
+    float s = 0.f;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 w = xp[v];
+      s += bf16lo_to_f32(w.x) + bf16hi_to_f32(w.x) + bf16lo_to_f32(w.y) + bf16hi_to_f32(w.y) +
+           bf16lo_to_f32(w.z) + bf16hi_to_f32(w.z) + bf16lo_to_f32(w.w) + bf16hi_to_f32(w.w);
+    }
+    xsum[b] = s;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kSWarps * 32) : "memory");
+
+  // A pair of warps takes each tile row, one 16-row slab each (its outputs are
+  // its own); pair q takes rows q, q + 4, ...  The slot is free once both
+  // warps of the pair have arrived on its empty barrier.
+  const bool lo = (g == t), hi = (g == t + 4);
+  const __nv_bfloat16* zero = xs_sm + p.K;
+  const int pair = warp >> 1, slab = warp & 1;
+  for (int j = pair; j < my_rows; j += kSWarps / 2) {
+    const int s = j % p.slots;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (j / p.slots) & 1, abort_flag, p.dev_status))) break;
+    const uint32_t rowbase = smem_u32(ring + (size_t)s * row_bytes);
+    // two tiles per iteration, independent until the final add (more ILP)
+    float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
+    int tc = 0;
+    for (; tc + 1 < TC; tc += 2) {
+      G1Tile d, e;
+      g1_lds(d, rowbase + (uint32_t)tc * kTileBytes, 16 * slab + g, t);
+      g1_lds(e, rowbase + (uint32_t)(tc + 1) * kTileBytes, 16 * slab + g, t);
+      const __nv_bfloat16* xt = xs_sm + tc * 256 + 32 * g;
+      const __nv_bfloat16* xu = xt + 256;
+      g1_tile(d, lo ? xt : zero, hi ? xt : zero, xsum + tc * 8, t, y0, y1);
+      g1_tile(e, lo ? xu : zero, hi ? xu : zero, xsum + tc * 8 + 8, t, z0, z1);
+    }
+    if (tc < TC) {
+      G1Tile d;
+      g1_lds(d, rowbase + (uint32_t)tc * kTileBytes, 16 * slab + g, t);
+      const __nv_bfloat16* xt = xs_sm + tc * 256 + 32 * g;
+      g1_tile(d, lo ? xt : zero, hi ? xt : zero, xsum + tc * 8, t, y0, y1);
+    }
+    y0 += z0;
+    y1 += z1;
+    // every lane's shared-memory reads of this slot went into y0, y1
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+    if (t == 0) {
+      const int tr = (int)blockIdx.x + j * (int)gridDim.x;
+      p.Y[tr * 32 + 16 * slab + g] = y0;
+      p.Y[tr * 32 + 16 * slab + g + 8] = y1;
+    }
+  }
+  if (*abort_flag && threadIdx.x == 0) {
+    // rows nobody consumed may still be landing: let them land first
+    for (int j = 0; j < my_rows; ++j)
+      mbar_wait(&full[j % p.slots], (j / p.slots) & 1, abort_flag, nullptr, 50000000ull) ||
+          mbar_try_wait(&full[j % p.slots], (j / p.slots) & 1);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, cudaStream_t stream) {
+  const int TC = a.K / 256;
+  const size_t row_bytes = (size_t)TC * kTileBytes;
+  int slots = (int)(kRingBudget / row_bytes);
+  if (slots > kMaxSlots) slots = kMaxSlots;
+  if (slots >= 3) {
+    Gemv1SParams p{};
+    p.tiles = a.tiles;
+    p.N = a.N;
+    p.K = a.K;
+    p.X = a.X;
+    p.Y = a.Y;
+    p.slots = slots;
+    p.dev_status = nullptr;
+    const int nrows = a.N / 32;
+    const int grid = nrows < sms ? nrows : sms;
+    const size_t smem = 128 + (size_t)slots * row_bytes + (size_t)a.K * 2 + 64 + (size_t)(a.K / 32) * 4 +
+                        (size_t)(kSWarps * 32 + 2) * 4 + 2 * kMaxSlots * 8 + 16;
+    const cudaError_t e = cudaFuncSetAttribute(q4_gemv1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    q4_gemv1_kernel<<<grid, kSThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
   Gemv1Params p{};
   p.tiles = a.tiles;
   p.N = a.N;
   p.K = a.K;
   p.X = a.X;
   p.Y = a.Y;
-  const int TC = a.K / 256;
   const int nslabs = a.N / 16;
   // split K across warps while there are too few slab groups to fill the GPU
   int S = 1;
@@ -238,10 +417,11 @@ cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, cudaStream_t stream) 
   const int grid = groups < kCtasPerSm * sms ? groups : kCtasPerSm * sms;
   const size_t smem = (size_t)a.K * 2 + 64 + (size_t)(a.K / 32) * 4 + (size_t)kWarps * 32 * 2 * 4;
   if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(q4_gemv1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e =
+        cudaFuncSetAttribute(q4_gemv1_regs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  q4_gemv1_kernel<<<grid, kWarps * 32, smem, stream>>>(p);
+  q4_gemv1_regs_kernel<<<grid, kWarps * 32, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
