@@ -260,12 +260,6 @@ QMM_DEV void g1_lds(G1Tile& d, uint32_t tile, int r0, int t) {
   }
 }
 
-QMM_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(umma::smem_u32(bar))
-      : "memory");
-}
 
 __global__ void __launch_bounds__(kSThreads, 1) q4_gemv1_kernel(const Gemv1SParams p) {
   using namespace umma;
@@ -301,7 +295,7 @@ __global__ void __launch_bounds__(kSThreads, 1) q4_gemv1_kernel(const Gemv1SPara
         if (!mbar_wait(&empty[s], ((j / p.slots) & 1) ^ 1, abort_flag, p.dev_status)) break;
         const int tr = (int)blockIdx.x + j * (int)gridDim.x;
         mbar_arrive_expect_tx(&full[s], row_bytes);
-        bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), p.tiles + (int64_t)tr * row_bytes, row_bytes, &full[s]);
+        umma::bulk_g2s(smem_u32(ring + (size_t)s * row_bytes), p.tiles + (int64_t)tr * row_bytes, row_bytes, &full[s]);
       }
     }
     // the copies in flight land before the CTA exits: consumers wait for every row
