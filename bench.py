@@ -8,10 +8,13 @@ inputs that are already resident in HBM:
   * q4 prefill     the 7 projections and lm_head at M=512
   * q4 MUL_MAT_ID  128 experts, top-8 of 17 strided ids, 512 tokens: gate, up, down
 Weight packing (packB, pack_q4) is done once, before timing, as the pages do it
-("once per (tensor, K, N)").  L2 is flushed before every step: a 256 MiB write,
-then a 256 MiB read, so that the lines left in L2 are clean and hold none of
-the step's inputs (a write-only flush leaves ~L2-sized dirty data whose
-write-back would land inside the first timed call).
+("once per (tensor, K, N)").  L2 is flushed before every call of the step, outside
+its timed bracket: a 256 MiB write, then a 256 MiB read, so that the lines left
+in L2 are clean and hold none of the call's inputs.  (A write-only flush leaves
+~L2-sized dirty data whose write-back lands inside the timed call; without a
+flush between calls, a call pays for the write-back of its predecessor's
+outputs and workspace, e.g. the int8 GEMM's 80 MB of f16 operands evicted by
+the next weight stream.)  A step's time is the sum of its calls' times.
 
 The printed `value` is int8 GEMM TOPS on the M=4096 K=N=4608 GEMM (the first
 half of the metric).  The q4 GEMV weight bandwidth (its second half) is
@@ -241,13 +244,13 @@ def run_ours(args, rank, world, dev):
         flush_rd.max()   # reads 256 MiB: replaces the dirty lines with clean ones
 
     def step(evs=None):
-        flush_l2()
-        if evs is not None:
-            evs[0].record(stream)
         for i, (_, fn, _, _) in enumerate(hp.calls):
+            flush_l2()
+            if evs is not None:
+                evs[2 * i].record(stream)
             fn()
             if evs is not None:
-                evs[i + 1].record(stream)
+                evs[2 * i + 1].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -262,7 +265,7 @@ def run_ours(args, rank, world, dev):
     time.sleep(0.3)
     all_evs = []
     for _ in range(args.steps):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(ncalls + 1)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * ncalls)]
         step(evs)
         all_evs.append(evs)
     torch.cuda.synchronize()
@@ -273,8 +276,9 @@ def run_ours(args, rank, world, dev):
     total = 0.0
     for evs in all_evs:
         for i in range(ncalls):
-            per_call[i] += evs[i].elapsed_time(evs[i + 1])
-        total += evs[0].elapsed_time(evs[-1])
+            ms = evs[2 * i].elapsed_time(evs[2 * i + 1])
+            per_call[i] += ms
+            total += ms
     t = torch.tensor(per_call + [total], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -410,7 +414,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": {"workload": WORKLOAD, "int8": f"u8xs8 M={c.M} K={c.K} N={c.N} int8 out",
-                   "l2": "flushed before every step (256 MiB write, then 256 MiB read)",
+                   "l2": "flushed before every timed call (256 MiB write, then 256 MiB read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "rooflines": rooflines,
