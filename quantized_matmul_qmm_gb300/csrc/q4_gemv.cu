@@ -321,12 +321,17 @@ __global__ void __launch_bounds__(kSThreads, 1) q4_gemv1_kernel(const Gemv1SPara
   asm volatile("bar.sync 1, %0;" ::"n"(kSWarps * 32) : "memory");
 
   // A pair of warps takes each tile row, one 16-row slab each (its outputs are
-  // its own); pair q takes rows q, q + 4, ...  The slot is free once both
+  // its own); pair q takes rows q, q + P, ... with P = min(4, slots) active
+  // pairs.  The launcher makes the slot count a multiple of P, so the rows
+  // that share a slot (j, j + slots, ...) all belong to one pair and are
+  // consumed in order: a pair never waits on a slot's phase before the
+  // previous phase of that slot has completed, and the slot is free once both
   // warps of the pair have arrived on its empty barrier.
   const bool lo = (g == t), hi = (g == t + 4);
   const __nv_bfloat16* zero = xs_sm + p.K;
   const int pair = warp >> 1, slab = warp & 1;
-  for (int j = pair; j < my_rows; j += kSWarps / 2) {
+  const int npairs = min(kSWarps / 2, p.slots);
+  for (int j = pair < npairs ? pair : my_rows; j < my_rows; j += npairs) {
     const int s = j % p.slots;
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (j / p.slots) & 1, abort_flag, p.dev_status))) break;
     const uint32_t rowbase = smem_u32(ring + (size_t)s * row_bytes);
@@ -378,6 +383,8 @@ cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, cudaStream_t stream) 
   const size_t row_bytes = (size_t)TC * kTileBytes;
   int slots = (int)(kRingBudget / row_bytes);
   if (slots > kMaxSlots) slots = kMaxSlots;
+  // a multiple of the active consumer pairs (see the kernel's row loop)
+  if (slots >= kSWarps / 2) slots -= slots % (kSWarps / 2);
   if (slots >= 3) {
     Gemv1SParams p{};
     p.tiles = a.tiles;

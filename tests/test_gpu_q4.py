@@ -109,3 +109,29 @@ def test_q4_gemv_streaming_path_full(qmm, cuda, M):
     y, norm = O.q4_gemm(ref_tiles, N, K, xnp(X))
     err = O.normalized_error(Y, y, norm)
     assert err <= 2e-5, err
+
+
+@pytest.mark.parametrize("K,rows_per_sm", [(1024, 12), (2048, 7), (2560, 5)])
+def test_q4_gemv_ring_slot_reuse(qmm, cuda, K, rows_per_sm):
+    """M=1 streaming GEMV with more tile rows per CTA than ring slots, so every
+    slot is refilled: K=1024 (8 slots, 4 consumer pairs), K=2048 (4 slots),
+    K=2560 (3 slots, 3 pairs).  Sampled tile rows include every row of the
+    first CTA's sequence and the last rows of the launch."""
+    sms = torch.cuda.get_device_properties(cuda).multi_processor_count
+    N = 32 * sms * rows_per_sm
+    g = torch.Generator().manual_seed(K + rows_per_sm)
+    W = torch.randn((N, K), generator=g) * 0.02
+    X = torch.randn((1, K), generator=g).to(torch.bfloat16)
+    tiles, Y = gpu_q4(qmm, cuda, W, X, pad=0)
+    rng = np.random.default_rng(K)
+    ntr = N // 32
+    trs = np.unique(np.concatenate([np.arange(0, ntr, sms), np.arange(ntr - 8, ntr),
+                                    rng.choice(ntr, 24, replace=False)]))
+    per = (K // 256) * 5120
+    rows = np.concatenate([np.arange(32 * tr, 32 * tr + 32) for tr in trs])
+    Wn = W.numpy()
+    for tr in trs:   # packing of the sampled tile rows, byte for byte
+        assert np.array_equal(tiles[tr * per:(tr + 1) * per], O.pack_q4(Wn[32 * tr:32 * tr + 32]))
+    y, norm = O.q4_gemm_rows(tiles, N, K, xnp(X), rows)
+    err = O.normalized_error(Y[:, rows], y, norm)
+    assert err <= 2e-5, err
