@@ -133,6 +133,8 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) q4_gemv1_regs_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
 
+  umma::pdl_launch_dependents();
+  umma::pdl_wait();
   for (int i = threadIdx.x; i < p.K / 8; i += blockDim.x)
     reinterpret_cast<uint4*>(xs_sm)[i] = reinterpret_cast<const uint4*>(p.X)[i];
   if (threadIdx.x < 4) reinterpret_cast<uint4*>(xs_sm + p.K)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
@@ -235,6 +237,7 @@ constexpr int kSWarps = 8;                       // consumer warps, in pairs
 constexpr int kSThreads = 32 * (kSWarps + 1);    // + the producer warp
 constexpr size_t kRingBudget = 192 * 1024;
 constexpr int kMaxSlots = 16;
+constexpr int kPrefetchRows = 2;                 // rows warmed in L2 before the dependency wait
 
 struct Gemv1SParams {
   const uint8_t* tiles;
@@ -273,11 +276,13 @@ __global__ void __launch_bounds__(kSThreads, 1) q4_gemv1_kernel(const Gemv1SPara
   uint64_t* full = reinterpret_cast<uint64_t*>(xsum + p.K / 32 + 2);         // [slots]
   uint64_t* empty = full + kMaxSlots;                                         // [slots]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kMaxSlots);
+  float* red = reinterpret_cast<float*>(empty + kMaxSlots + 2);               // [pair][slab][g][2]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int nrows = p.N / 32;                                                 // tile rows
   const int my_rows = (int)blockIdx.x < nrows ? (nrows - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.slots; ++s) {
       mbar_init(&full[s], 1);
@@ -290,6 +295,15 @@ __global__ void __launch_bounds__(kSThreads, 1) q4_gemv1_kernel(const Gemv1SPara
   if (warp == kSWarps) {
     // ---- producer: tile rows blockIdx.x, blockIdx.x + gridDim.x, ... ----
     if (lane == 0) {
+      // While the previous grid finishes, pull the first two rows into L2.
+      // L2 is where global memory is coherent, so a line warmed here and
+      // written later by that grid is still read correctly: the copies into
+      // shared memory are only issued after the wait below.  (More rows delay
+      // the first copy: this SM's TMA unit works through the prefetch
+      // requests first.)
+      for (int j = 0; j < my_rows && j < kPrefetchRows; ++j)
+        bulk_prefetch_l2(p.tiles + (int64_t)((int)blockIdx.x + j * (int)gridDim.x) * row_bytes, row_bytes);
+      pdl_wait();
       for (int j = 0; j < my_rows; ++j) {
         const int s = j % p.slots;
         if (!mbar_wait(&empty[s], ((j / p.slots) & 1) ^ 1, abort_flag, p.dev_status)) break;
@@ -303,6 +317,7 @@ __global__ void __launch_bounds__(kSThreads, 1) q4_gemv1_kernel(const Gemv1SPara
   }
 
   // ---- consumers: x into shared memory, then rows j = warp, warp + 8, ... ----
+  pdl_wait();   // x and y may belong to the previous grid
   for (int i = threadIdx.x; i < p.K / 8; i += kSWarps * 32)
     reinterpret_cast<uint4*>(xs_sm)[i] = reinterpret_cast<const uint4*>(p.X)[i];
   if (threadIdx.x < 4) reinterpret_cast<uint4*>(xs_sm + p.K)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
@@ -331,7 +346,43 @@ __global__ void __launch_bounds__(kSThreads, 1) q4_gemv1_kernel(const Gemv1SPara
   const __nv_bfloat16* zero = xs_sm + p.K;
   const int pair = warp >> 1, slab = warp & 1;
   const int npairs = min(kSWarps / 2, p.slots);
-  for (int j = pair < npairs ? pair : my_rows; j < my_rows; j += npairs) {
+  if (nrows <= (int)gridDim.x) {
+    // One tile row per CTA (small N): all four pairs split the row's tiles
+    // (tc = pair, pair + 4, ...; one row uses no slot twice) so that no pair
+    // walks all of K alone, and their partial sums are added in pair order
+    // through shared memory.
+    constexpr int kSplit = kSWarps / 2;
+    float y0 = 0.f, y1 = 0.f;
+    if (my_rows == 1 &&
+        __all_sync(0xffffffffu, mbar_wait(&full[0], 0, abort_flag, p.dev_status))) {
+      const uint32_t rowbase = smem_u32(ring);
+      for (int tc = pair; tc < TC; tc += kSplit) {
+        G1Tile d;
+        g1_lds(d, rowbase + (uint32_t)tc * kTileBytes, 16 * slab + g, t);
+        const __nv_bfloat16* xt = xs_sm + tc * 256 + 32 * g;
+        g1_tile(d, lo ? xt : zero, hi ? xt : zero, xsum + tc * 8, t, y0, y1);
+      }
+    }
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+    if (t == 0) {
+      red[((pair * 2 + slab) * 8 + g) * 2] = y0;
+      red[((pair * 2 + slab) * 8 + g) * 2 + 1] = y1;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kSWarps * 32) : "memory");
+    if (pair == 0 && t == 0 && my_rows == 1 && !*abort_flag) {
+      float s0 = 0.f, s1 = 0.f;
+      for (int q = 0; q < kSplit; ++q) {
+        s0 += red[((q * 2 + slab) * 8 + g) * 2];
+        s1 += red[((q * 2 + slab) * 8 + g) * 2 + 1];
+      }
+      p.Y[(int)blockIdx.x * 32 + 16 * slab + g] = s0;
+      p.Y[(int)blockIdx.x * 32 + 16 * slab + g + 8] = s1;
+    }
+  }
+  for (int j = (pair < npairs && nrows > (int)gridDim.x) ? pair : my_rows; j < my_rows; j += npairs) {
     const int s = j % p.slots;
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (j / p.slots) & 1, abort_flag, p.dev_status))) break;
     const uint32_t rowbase = smem_u32(ring + (size_t)s * row_bytes);
@@ -397,11 +448,10 @@ cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, cudaStream_t stream) 
     const int nrows = a.N / 32;
     const int grid = nrows < sms ? nrows : sms;
     const size_t smem = 128 + (size_t)slots * row_bytes + (size_t)a.K * 2 + 64 + (size_t)(a.K / 32) * 4 +
-                        (size_t)(kSWarps * 32 + 2) * 4 + 2 * kMaxSlots * 8 + 16;
+                        (size_t)(kSWarps * 32 + 2) * 4 + 2 * kMaxSlots * 8 + 16 + (size_t)(kSWarps / 2) * 2 * 8 * 2 * 4;
     const cudaError_t e = cudaFuncSetAttribute(q4_gemv1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    q4_gemv1_kernel<<<grid, kSThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(q4_gemv1_kernel, dim3(grid), dim3(kSThreads), smem, stream, p);
   }
   Gemv1Params p{};
   p.tiles = a.tiles;
@@ -422,8 +472,7 @@ cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, cudaStream_t stream) 
         cudaFuncSetAttribute(q4_gemv1_regs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  q4_gemv1_regs_kernel<<<grid, kWarps * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(q4_gemv1_regs_kernel, dim3(grid), dim3(kWarps * 32), smem, stream, p);
 }
 
 }  // namespace qmm

@@ -138,6 +138,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32) q4_gemv_kernel(const Q4GemvPa
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int TC = p.K / 256;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // x and y may belong to the previous grid
   gemv_xs_prologue<NG>(p, xs, nblk);
   __syncthreads();
 
@@ -205,8 +207,7 @@ cudaError_t launch_gemv_kernel(Kern kern, unsigned grid, size_t smem, const Q4Ge
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<grid, kGemvWarps * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kGemvWarps * 32), smem, stream, p);
 }
 
 cudaError_t launch_q4_gemv(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream) {

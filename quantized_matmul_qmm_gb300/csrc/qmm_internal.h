@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "qmm.h"
 #include "qmm_device.cuh"
 
@@ -16,6 +18,26 @@ constexpr int64_t kTileBytes = 5120;
 
 inline int64_t padded_k(int64_t K) { return (K + 63) / 64 * 64; }
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Launch with programmatic stream serialization: the grid may start while the
+// previous grid in the stream finishes.  The kernel must execute
+// griddepcontrol.wait before touching anything that grid could have written,
+// and it releases its own dependents with griddepcontrol.launch_dependents.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---- TMA descriptors (tmap.cu): 2-byte elements, 128-byte swizzle, box
 // box_inner x box_rows (box_inner * 2 == 128 bytes) ----

@@ -122,6 +122,16 @@ QMM_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* b
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Warm L2 with `bytes` (a multiple of 16) of global memory from a 16-byte
+// aligned address; nothing lands in shared memory.
+QMM_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// Programmatic dependent launch: let the next grid in the stream start its
+// prologue now / wait until the previous grid has completed and its memory
+// is visible (a no-op when the launch carries no programmatic dependency).
+QMM_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+QMM_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 QMM_DEV void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
