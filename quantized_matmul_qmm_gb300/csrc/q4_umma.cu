@@ -52,6 +52,8 @@
 // leaves cleanly.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "qmm_internal.h"
 #include "umma.cuh"
 
@@ -552,35 +554,31 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
   }
 }
 
-// Routing and activation packing in one launch.  Block b owns pairs
-// [b*PB, (b+1)*PB).  Every block reads all ids: the histogram of all pairs
-// gives the expert offsets, and the histogram of the pairs before its own
-// range gives each expert's base rank there.  Warp 0 then ranks the block's
-// pairs in pair order (lanes with the same expert found by match_any), so the
-// grouped list is deterministic.  Finally the block copies its pairs'
-// activation rows to their ranks (when the packed buffer exists).
+// Routing: expert offsets and the grouped pair list.  Block b owns pairs
+// [b*PB, (b+1)*PB), PB a multiple of 256.  Every block counts all ids (the
+// expert offsets) and the ids before its range (each expert's base rank
+// there).  It then ranks its pairs in rounds of 256, in pair order: inside a
+// warp, lanes with the same expert are ordered by match_any; across the eight
+// warps of a round, by per-warp expert counts in shared memory.  So the
+// grouped list is deterministic.
 constexpr int kRouteThreads = 256;
-constexpr int kRouteMaxPB = 32;   // one warp ranks a block's pairs
+constexpr int kRouteWarps = kRouteThreads / 32;
 
 __global__ void __launch_bounds__(kRouteThreads)
-moe_route_pack_kernel(const int32_t* __restrict__ ids, int64_t ld_ids, int n_used, int T, int n_expert, int PB,
-                      const __nv_bfloat16* __restrict__ X, int64_t ldx_token, int64_t ldx_slot, int K,
-                      int32_t* __restrict__ offsets, int32_t* __restrict__ pairs, __nv_bfloat16* __restrict__ Xp,
-                      int32_t* dev_status) {
+moe_route_kernel(const int32_t* __restrict__ ids, int64_t ld_ids, int n_used, int T, int n_expert, int PB,
+                 int32_t* __restrict__ offsets, int32_t* __restrict__ pairs, int32_t* dev_status) {
   extern __shared__ int rsm[];
   int* off = rsm;                    // [n_expert + 1]: histogram, then exclusive offsets
-  int* before = rsm + n_expert + 1;  // [n_expert]: pairs of each expert before this block's range
-  int* run = before + n_expert;      // [n_expert]: ranked so far inside this block
-  __shared__ int wsum[kRouteThreads / 32];
-  __shared__ int rank_s[kRouteMaxPB];
-  __shared__ int pair_s[kRouteMaxPB];
-  // the grouped kernel may start now: it prefetches weights, then waits for this grid
+  int* before = rsm + n_expert + 1;  // [n_expert]: pairs of each expert before the current round
+  int* cnt = before + n_expert;      // [kRouteWarps][n_expert]: this round's counts per warp
+  __shared__ int wsum[kRouteWarps];
+  // the packing grid (or the grouped kernel) may start; it waits for this grid
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int npairs = T * n_used;
   const int p0 = blockIdx.x * PB;
   for (int e = tid; e <= n_expert; e += kRouteThreads) off[e] = 0;
-  for (int e = tid; e < n_expert; e += kRouteThreads) before[e] = run[e] = 0;
+  for (int e = tid; e < n_expert; e += kRouteThreads) before[e] = 0;
   __syncthreads();
   bool bad = false;
   // eight independent loads in flight per thread, then the shared-memory counts
@@ -621,7 +619,7 @@ moe_route_pack_kernel(const int32_t* __restrict__ ids, int64_t ld_ids, int n_use
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     int wbase = 0, total = 0;
-    for (int w = 0; w < kRouteThreads / 32; ++w) {
+    for (int w = 0; w < kRouteWarps; ++w) {
       wbase += (w < warp) ? wsum[w] : 0;
       total += wsum[w];
     }
@@ -637,58 +635,68 @@ moe_route_pack_kernel(const int32_t* __restrict__ ids, int64_t ld_ids, int n_use
   __syncthreads();
   if (blockIdx.x == 0)
     for (int e = tid; e <= n_expert; e += kRouteThreads) offsets[e] = off[e];
-  // rank this block's pairs in pair order
-  const int nb = min(PB, npairs - p0);
-  if (warp == 0) {
-    for (int j0 = 0; j0 < nb; j0 += 32) {
-      const int j = j0 + lane;
-      const int pr = p0 + j;
-      int e = -1;
-      if (j < nb) {
-        e = ids[(int64_t)(pr / n_used) * ld_ids + (pr % n_used)];
-        if (e < 0 || e >= n_expert) e = -1;
-      }
-      const unsigned same = __match_any_sync(0xffffffffu, e);
-      const int local = __popc(same & ((1u << lane) - 1u));
-      int rank = -1;
-      if (e >= 0) rank = off[e] + before[e] + run[e] + local;
-      __syncwarp();
-      if (e >= 0 && local == 0) run[e] += __popc(same);
-      __syncwarp();
-      if (j < nb) {
-        rank_s[j] = rank;
-        pair_s[j] = pr;
-        if (rank >= 0) pairs[rank] = pr;
-      }
+  // rank this block's pairs, 256 per round, in pair order
+  const int p_end = min(p0 + PB, npairs);
+  for (int r0 = p0; r0 < p_end; r0 += kRouteThreads) {
+    for (int i = tid; i < kRouteWarps * n_expert; i += kRouteThreads) cnt[i] = 0;
+    __syncthreads();
+    const int pr = r0 + tid;
+    int e = -1;
+    if (pr < p_end) {
+      e = ids[(int64_t)(pr / n_used) * ld_ids + (pr % n_used)];
+      if (e < 0 || e >= n_expert) e = -1;
     }
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int local = __popc(same & ((1u << lane) - 1u));
+    if (e >= 0 && local == 0) cnt[warp * n_expert + e] = __popc(same);
+    __syncthreads();
+    if (e >= 0) {
+      int rank = off[e] + before[e] + local;
+      for (int w = 0; w < warp; ++w) rank += cnt[w * n_expert + e];
+      pairs[rank] = pr;
+    }
+    __syncthreads();
+    // this round's pairs come before the next round's
+    for (int x = tid; x < n_expert; x += kRouteThreads) {
+      int sum = 0;
+      for (int w = 0; w < kRouteWarps; ++w) sum += cnt[w * n_expert + x];
+      before[x] += sum;
+    }
+    __syncthreads();
   }
-  if (Xp == nullptr) return;
-  __syncthreads();
-  // copy: 16-byte units, eight loads in flight per thread
+}
+
+// Activation packing: the src1 row of every grouped pair, copied to its rank
+// so that each job's B operand is one dense block.  One warp per row, the
+// whole row's 16-byte loads in flight at once.
+__global__ void __launch_bounds__(kRouteThreads)
+moe_pack_kernel(const int32_t* __restrict__ pairs, const int32_t* __restrict__ offsets, int n_expert, int n_used,
+                const __nv_bfloat16* __restrict__ X, int64_t ldx_token, int64_t ldx_slot, int K,
+                __nv_bfloat16* __restrict__ Xp) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the pair list comes from the routing grid
+  const int lane = threadIdx.x & 31;
+  const int total = offsets[n_expert];
   const int chunks = K / 8;
-  const int units = nb * chunks;
-  for (int base = 0; base < units; base += 8 * kRouteThreads) {
-    uint4 v[8];
-    int dst_rank[8], c8[8];
+  const int nw = (int)gridDim.x * kRouteWarps;
+  for (int r = (int)blockIdx.x * kRouteWarps + ((int)threadIdx.x >> 5); r < total; r += nw) {
+    const int pr = pairs[r];
+    const int t = pr / n_used, i = pr - t * n_used;
+    const uint4* src = reinterpret_cast<const uint4*>(X + (int64_t)t * ldx_token + (int64_t)i * ldx_slot);
+    uint4* dst = reinterpret_cast<uint4*>(Xp + (int64_t)r * K);
+    for (int c0 = 0; c0 < chunks; c0 += 8 * 32) {
+      uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int idx = base + u * kRouteThreads + tid;
-      dst_rank[u] = -1;
-      if (idx < units) {
-        const int j = idx / chunks;
-        c8[u] = idx - j * chunks;
-        dst_rank[u] = rank_s[j];
-        if (dst_rank[u] >= 0) {
-          const int pr = pair_s[j];
-          const uint4* src = reinterpret_cast<const uint4*>(X + (int64_t)(pr / n_used) * ldx_token +
-                                                            (int64_t)(pr % n_used) * ldx_slot);
-          v[u] = ldg128(src + c8[u]);
-        }
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < chunks) v[u] = ldg128(src + c);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < chunks) dst[c] = v[u];
       }
     }
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (dst_rank[u] >= 0) reinterpret_cast<uint4*>(Xp + (int64_t)dst_rank[u] * K)[c8[u]] = v[u];
   }
 }
 
@@ -752,22 +760,29 @@ cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream) {
       !make_tmap_q4_tiles(&tmP, a.tiles, (uint64_t)(a.K / 256), tile_rows, 8))
     return cudaErrorInvalidValue;
   const int npairs = a.T * a.n_used;
-  // 8 pairs per block (one round of row loads per block), more when the
-  // batch is large enough that every block rereading all ids would cost more
-  int PB = 8;
-  while (PB < kRouteMaxPB && (int64_t)npairs * ((npairs + PB - 1) / PB) > (int64_t)64 << 20) PB *= 2;
+  // 256 pairs per routing block, more when the batch is large enough that
+  // every block recounting all ids would cost more
+  int PB = kRouteThreads;
+  while ((int64_t)npairs * ((npairs + PB - 1) / PB) > (int64_t)16 << 20) PB *= 2;
   const int nblk = (npairs + PB - 1) / PB;
-  const size_t rsmem = (size_t)(3 * a.n_expert + 1) * sizeof(int);
+  const size_t rsmem = (size_t)((2 + kRouteWarps) * a.n_expert + 1) * sizeof(int);
   if (rsmem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(moe_route_pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)rsmem);
     if (e != cudaSuccess) return e;
   }
-  moe_route_pack_kernel<<<nblk, kRouteThreads, rsmem, stream>>>(
-      a.ids, a.ld_ids, a.n_used, a.T, a.n_expert, PB, a.X, a.ldx_token, a.ldx_slot, a.K, a.offsets, a.pairs,
-      a.xperm, a.dev_status);
+  moe_route_kernel<<<nblk, kRouteThreads, rsmem, stream>>>(a.ids, a.ld_ids, a.n_used, a.T, a.n_expert, PB,
+                                                           a.offsets, a.pairs, a.dev_status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  if (a.xperm != nullptr) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int pgrid = std::max(1, std::min((npairs + kRouteWarps - 1) / kRouteWarps, 8 * sms));
+    err = launch_pdl(moe_pack_kernel, dim3(pgrid), dim3(kRouteThreads), 0, stream, (const int32_t*)a.pairs,
+                     (const int32_t*)a.offsets, a.n_expert, a.n_used, a.X, a.ldx_token, a.ldx_slot, a.K, a.xperm);
+    if (err != cudaSuccess) return err;
+  }
   if (a.xperm == nullptr) return launch_tc<kTableGather, 64, 2>(tmC, tmP, tmC, p, stream);
   if (!make_tmap_2d(&tmX, true, a.xperm, (uint64_t)a.K, (uint64_t)npairs, (uint64_t)a.K * 2, 64, 64))
     return cudaErrorInvalidValue;
