@@ -44,6 +44,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+HOST_LEAD_CYCLES = 4_000_000   # ~2 ms of GPU sleep at ~2 GHz before each timed step or pass
 METRIC = "int8 GEMM TOPS (% tensor peak); 4-bit GEMV weight GB/s (% HBM) at 1 GB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 INT8_M, INT8_K, INT8_N = 4096, 4608, 4608
@@ -247,6 +248,9 @@ def run_ours(args, rank, world, dev):
         flush_rd.max()   # reads 256 MiB: replaces the dirty lines with clean ones
 
     def step(evs=None):
+        # the GPU idles ~2 ms (outside every timed bracket) while the host
+        # enqueues the whole step, so no call's bracket waits on the host
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
         for i, (_, fn, _, _) in enumerate(hp.calls):
             flush_l2()
             if evs is not None:
@@ -359,6 +363,7 @@ def run_gemv_streams(hp, q, args, dev, stream):
         out = []
         for i in range(args.warmup + n):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(HOST_LEAD_CYCLES)   # the host enqueues the pass ahead of the GPU
             e0.record(stream)
             fn()
             e1.record(stream)

@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(kSThreads, 1) q4_gemv1_kernel(const Gemv1SPara
 
 }  // namespace
 
-cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, cudaStream_t stream) {
+cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, int32_t* dev_status, cudaStream_t stream) {
   const int TC = a.K / 256;
   const size_t row_bytes = (size_t)TC * kTileBytes;
   int slots = (int)(kRingBudget / row_bytes);
@@ -444,7 +444,7 @@ cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, cudaStream_t stream) 
     p.X = a.X;
     p.Y = a.Y;
     p.slots = slots;
-    p.dev_status = nullptr;
+    p.dev_status = dev_status;
     const int nrows = a.N / 32;
     const int grid = nrows < sms ? nrows : sms;
     const size_t smem = 128 + (size_t)slots * row_bytes + (size_t)a.K * 2 + 64 + (size_t)(a.K / 32) * 4 +

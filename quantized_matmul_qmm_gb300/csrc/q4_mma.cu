@@ -211,10 +211,9 @@ cudaError_t launch_gemv_kernel(Kern kern, unsigned grid, size_t smem, const Q4Ge
 }
 
 cudaError_t launch_q4_gemv(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream) {
-  (void)dev_status;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (a.M == 1) return launch_q4_gemv1(a, sms, stream);
+  if (a.M == 1) return launch_q4_gemv1(a, sms, dev_status, stream);
   Q4GemvParams p{};
   p.tiles = a.tiles;
   p.N = a.N;

@@ -20,15 +20,16 @@
 // stream in while the current one finishes.  The fp32 accumulator is double
 // buffered in TMEM, so a job's epilogue overlaps the next job's MMAs.
 //
-// Routing.  A route-and-pack kernel (one block per 8 pairs) writes per-expert
-// offsets and the grouped (token, slot) list into the caller's workspace, in
-// pair order inside each expert.  The grouped kernel is launched as its
-// programmatic dependent, so it starts while routing still runs.
+// Routing.  A routing grid writes per-expert offsets and the grouped
+// (token, slot) list into the caller's workspace, in pair order inside each
+// expert.
 //
-// Activations.  With a full workspace, the route-and-pack kernel also packs
-// the rows of src1 in expert order, so that every job's B operand is a dense
-// block that TMA loads whole.  With only the routing tables (the
-// no-allocation entry point) a loader warp gathers the rows with cp.async.
+// Activations.  With a full workspace, a packing grid (the routing grid's
+// programmatic dependent) copies the rows of src1 in expert order, so that
+// every job's B operand is a dense block that TMA loads whole.  With only the
+// routing tables (the no-allocation entry point) a loader warp gathers the
+// rows with cp.async.  The grouped kernel is launched as the last grid's
+// programmatic dependent, so it starts while that grid still runs.
 //
 // The contraction runs on the 5th-generation tensor cores with the weights as
 // the M = 128 side and the pairs as N (16..kTok).  The dequantised weights go
@@ -85,9 +86,11 @@ struct Lay {
   static constexpr int kXW = kCtas == 2 ? 4 : 8;           // transform warps
   static constexpr bool kSepEpi = kCtas == 1;              // epilogue warps of their own
   static constexpr int kWarps = kXW + (kSepEpi ? 4 : 0) + 3;
-  static constexpr int kAStages = kCtas == 2 ? 2 : 4;       // TMEM A buffers of 64 columns (128 k)
+  // TMEM A buffers of 64 columns (128 k); a 192-token job's two accumulators
+  // leave room for two
+  static constexpr int kAStages = (kCtas == 2 || kTok > 128) ? 2 : 4;
   static constexpr int kRawStages = kCtas == 2 ? 3 : (kTok == 64 ? 4 : 3);
-  static constexpr int kBStages = kCtas == 2 ? 3 : 4;       // activation ring depth
+  static constexpr int kBStages = (kCtas == 2 || kTok > 128) ? 3 : 4;   // activation ring depth
   static constexpr int kBAtomBytes = kTok * 128;           // kTok rows x 64 k bf16, 128-byte swizzle
   static constexpr int kBBytes = 2 * kBAtomBytes;          // 128 k per stage
   static constexpr uint32_t kColA = 2 * kTok;              // after the two accumulators
@@ -314,8 +317,9 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
   const uint32_t tmem = *tmem_slot;
 
   // The first unit's first weight stages do not depend on the routing: when
-  // most experts receive pairs they are fetched while the route-and-pack
-  // grid may still run.
+  // most experts receive pairs they are fetched while the routing or packing
+  // grid may still run.  (The routing grid is an ordinary stream-ordered
+  // launch, so whatever wrote the tiles before it has completed.)
   int e_first, n0_first;
   unit_rows(p, (int)blockIdx.x, e_first, n0_first);
   const int pre = p.npairs >= p.n_expert ? min(kRawStages, TC) : 0;
@@ -480,33 +484,50 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
     }
   } else if (warp == kWMma) {
     // ---- MMA issuer ----
+    // The tensor pipe queues few MMAs and this thread shares its SM
+    // sub-partition with busy transform and epilogue warps, so the issue loop
+    // is kept short: stages and phases are counted, and every descriptor is a
+    // precomputed base plus a constant.
     if (lane == 0) {
-      int gs = 0;
+      const uint64_t bdesc0 = desc_kmajor_sw128(sB0);
+      const uint32_t acol0 = tmem + kColA;
+      int as = 0, bs = 0;
+      uint32_t aph = 0, bph = 0;
       Jobs<kTok> jb;
       while (ok && jb.next(p)) {
         const int db = njobs & 1;
         const uint32_t idesc = idesc_f16(kRows, jb.ncol(), true);
+        const uint32_t dt = tmem + (uint32_t)(kTok * db);
         if (!mbar_wait(&d_empty[db], ((njobs >> 1) & 1) ^ 1, abort_flag, p.dev_status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int ks = 0; ks < nks; ++ks, ++gs) {
-          const int as = gs % kAStages, bs = gs % kBStages;
-          if (!mbar_wait(&a_full[as], (gs / kAStages) & 1, abort_flag, p.dev_status) ||
-              !mbar_wait(&b_full[bs], (gs / kBStages) & 1, abort_flag, p.dev_status)) {
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!(mbar_try_wait(&a_full[as], aph) || mbar_wait(&a_full[as], aph, abort_flag, p.dev_status)) ||
+              !(mbar_try_wait(&b_full[bs], bph) || mbar_wait(&b_full[bs], bph, abort_flag, p.dev_status))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sb = sB0 + bs * kBBytes;
+          const uint32_t at = acol0 + 64u * (uint32_t)as;
+          // +32 bytes per 16 k inside a 128-byte swizzle row (+2 in the address
+          // field); the second 64 k of the stage is the next atom
+          const uint64_t bd = bdesc0 + (uint64_t)((bs * kBBytes) >> 4);
 #pragma unroll
           for (int j = 0; j < kKC / 16; ++j)
-            umma_f16_ta(tmem + (uint32_t)(kTok * db), tmem + kColA + 64 * as + 8 * j,
-                        desc_kmajor_sw128(sb + (j >> 2) * kBAtomBytes + 32 * (j & 3)), idesc,
-                        (ks > 0 || j > 0) ? 1u : 0u);
+            umma_f16_ta(dt, at + 8u * (uint32_t)j, bd + (uint64_t)((j >> 2) * (kBAtomBytes >> 4) + 2 * (j & 3)),
+                        idesc, (ks > 0 || j > 0) ? 1u : 0u);
           umma_commit(&a_empty[as]);
           umma_commit(&b_empty[bs]);
+          if (++as == kAStages) {
+            as = 0;
+            aph ^= 1u;
+          }
+          if (++bs == kBStages) {
+            bs = 0;
+            bph ^= 1u;
+          }
         }
         if (!ok) break;
         umma_commit(&d_full[db]);
@@ -816,18 +837,22 @@ cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaS
   if (!make_tmap_q4_tiles(&tmC, a.tiles, (uint64_t)(a.K / 256), (uint64_t)(a.N / 32), 32) ||
       !make_tmap_q4_tiles(&tmP, a.tiles, (uint64_t)(a.K / 256), (uint64_t)(a.N / 32), 8))
     return cudaErrorInvalidValue;
-  const uint32_t box_rows = a.M <= 64 ? 64 : 128;
+  // Token chunk per job (the MMA's N): 64 for small M.  Otherwise 192 when
+  // that takes fewer chunks than 128 and the units still cover every SM
+  // (wider MMAs amortise their issue, and each weight is dequantised fewer
+  // times); small N keeps 128 for more units.
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int c192 = (a.M + 191) / 192, c128 = (a.M + 127) / 128;
+  const int tok = a.M <= 64 ? 64 : (a.M > 128 && c192 < c128 && (int64_t)p.nrb * c192 >= sms ? 192 : 128);
   if (!make_tmap_2d(&tmX, true, const_cast<__nv_bfloat16*>(a.X), (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.ldx * 2,
-                    64, box_rows))
+                    64, (uint32_t)tok))
     return cudaErrorInvalidValue;
-  if (a.M <= 64) {
-    p.dense_chunks = 1;
-    p.n_units = p.nrb;
-    return launch_tc<kDense, 64, 1>(tmC, tmP, tmX, p, stream);
-  }
-  p.dense_chunks = (a.M + 127) / 128;
+  p.dense_chunks = (a.M + tok - 1) / tok;
   if ((int64_t)p.nrb * p.dense_chunks > INT32_MAX) return cudaErrorInvalidValue;
   p.n_units = p.nrb * p.dense_chunks;
+  if (tok == 64) return launch_tc<kDense, 64, 1>(tmC, tmP, tmX, p, stream);
+  if (tok == 192) return launch_tc<kDense, 192, 1>(tmC, tmP, tmX, p, stream);
   return launch_tc<kDense, 128, 1>(tmC, tmP, tmX, p, stream);
 }
 

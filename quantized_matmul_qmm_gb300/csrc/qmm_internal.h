@@ -86,7 +86,7 @@ struct Q4DenseArgs {
   int64_t ldy;
 };
 cudaError_t launch_q4_gemv(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream);
-cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, cudaStream_t stream);
+cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, int32_t* dev_status, cudaStream_t stream);
 bool q4_umma_eligible(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream);
 

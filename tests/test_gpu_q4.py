@@ -30,7 +30,7 @@ def xnp(X):
 
 
 @pytest.mark.parametrize("N,K", [(32, 256), (64, 512), (96, 768), (1024, 1024), (1024, 3072)])
-@pytest.mark.parametrize("M", [1, 2, 7, 8, 9, 16, 17, 33, 100])
+@pytest.mark.parametrize("M", [1, 2, 7, 8, 9, 16, 17, 33, 100, 300, 577])
 def test_q4_gemm_small_shapes(qmm, cuda, N, K, M):
     g = torch.Generator().manual_seed(N + K + M)
     W = torch.randn((N, K), generator=g) * 0.02
@@ -135,3 +135,18 @@ def test_q4_gemv_ring_slot_reuse(qmm, cuda, K, rows_per_sm):
     y, norm = O.q4_gemm_rows(tiles, N, K, xnp(X), rows)
     err = O.normalized_error(Y[:, rows], y, norm)
     assert err <= 2e-5, err
+
+
+@pytest.mark.parametrize("M,N,K", [(577, 8192, 256), (300, 12288, 256)])
+def test_q4_prefill_192_token_chunks(qmm, cuda, M, N, K):
+    """Prefill GEMMs large enough in N to take 192-token jobs (the MMA's N),
+    with a ragged last chunk: 577 = 3 x 192 + 1, 300 = 192 + 108."""
+    g = torch.Generator().manual_seed(M + N)
+    W = torch.randn((N, K), generator=g) * 0.02
+    X = torch.randn((M, K), generator=g).to(torch.bfloat16)
+    tiles, Y = gpu_q4(qmm, cuda, W, X)
+    ref_tiles = O.pack_q4(W.numpy())
+    assert np.array_equal(tiles, ref_tiles)
+    y, norm = O.q4_gemm(ref_tiles, N, K, xnp(X))
+    err = O.normalized_error(Y, y, norm)
+    assert err <= TOL, err
