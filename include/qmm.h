@@ -146,6 +146,36 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
                          int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
                          cudaStream_t stream);
 
+/* Workspace of qmm_quantize_act_int8: 256 bytes for per-tensor scaling, 0 per row. */
+qmm_status qmm_quantize_act_int8_workspace_size(int64_t M, int64_t K, int per_row, size_t* ws_bytes);
+
+/* Symmetric int8 quantisation of activations for qmm_int8_gemm ("int8
+ * inference", "Product kernel (Int8Gemm)": per-tensor symmetric activations
+ * with scale amax/127; the ONNX pack page, "What works today": the per-row
+ * scale vector s_x[m] of the float epilogue).  The rule is packB's, applied to
+ * each row (per_row = 1) or to the whole tensor (per_row = 0):
+ *   s    = fl(amax / 127), amax = max |X| over the row or the tensor;
+ *   A[m][k] = clamp(rint_even(fl(X[m][k] / s)), -127, 127), and 0 where s == 0.
+ * Every step is IEEE fp32, so the codes and scales are bit-exact.
+ *
+ * X        [M][K] fp32 (x_type QMM_F32) or bf16 (QMM_BF16), row stride ldx
+ *          elements (ldx >= K), base aligned to its element size.
+ * A        int8 [M][K] out, row stride lda bytes: lda >= K, lda % 16 == 0, base
+ *          16-byte aligned (what qmm_int8_gemm takes, with a_type QMM_S8 and
+ *          zA = 0).  Bytes past K in a row are not written.
+ * s_x      fp32 out: [M] per row, [1] per tensor.  Pass it as the epilogue's s_x
+ *          with s_x_stride = per_row.
+ * workspace / ws_bytes  at least qmm_quantize_act_int8_workspace_size bytes,
+ *          16-byte aligned (NULL when that size is 0).
+ * X must be finite: for an inf or NaN input the codes and scales are
+ * unspecified.
+ * Errors: QMM_ERR_INVALID_ARG for null or misaligned pointers, M < 1, K < 1,
+ * ldx < K, a bad lda or x_type, per_row not 0 or 1; QMM_ERR_WORKSPACE.
+ */
+qmm_status qmm_quantize_act_int8(const void* X, qmm_dtype x_type, int64_t M, int64_t K, int64_t ldx,
+                                 int per_row, void* A, int64_t lda, float* s_x, void* workspace,
+                                 size_t ws_bytes, cudaStream_t stream);
+
 /* ========================================================================
  * (II) 4-bit block weights
  *

@@ -207,6 +207,29 @@ def quantize_columns_f32(W):
     return q, scale
 
 
+def quantize_activations_f32(X, per_row: bool):
+    """Symmetric int8 activations: scale = amax/127 over each row (per_row) or
+    over the whole tensor, then packB's rounding, q = clamp(rint_even(R(x/s)),
+    -127, 127), and q = 0 where s == 0.
+
+    (int8 inference, "Product kernel (Int8Gemm)": per-tensor symmetric
+    activations with scale amax/127; ONNX pack page, "What works today": the
+    per-row activation scale s_x[m] of the float epilogue.)
+    X: fp32 values [M][K].  Returns (codes int64 [M][K], scales fp64 holding
+    fp32 values: [M] per row, [1] per tensor).
+    """
+    X = _f32(np.asarray(X, np.float64))
+    M = X.shape[0]
+    amax = np.abs(X).max(axis=1) if per_row else np.array([np.abs(X).max()])
+    scale = _f32(amax / 127.0)
+    q = np.zeros(X.shape, dtype=np.int64)
+    for m in range(M):
+        s = scale[m] if per_row else scale[0]
+        if s > 0:
+            q[m] = np.clip(np.rint(_f32(X[m] / s)), -127, 127).astype(np.int64)
+    return q, scale
+
+
 def pack_b_int8(B, b_type: str):
     """Packed weights for the int8 GEMM.
 

@@ -141,6 +141,26 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
   return cuda_status(launch_int8_gemm_mma(a, stream));
 }
 
+qmm_status qmm_quantize_act_int8_workspace_size(int64_t M, int64_t K, int per_row, size_t* ws_bytes) {
+  if (ws_bytes == nullptr || M < 1 || K < 1 || (per_row != 0 && per_row != 1)) return QMM_ERR_INVALID_ARG;
+  *ws_bytes = per_row ? 0 : 256;
+  return QMM_OK;
+}
+
+qmm_status qmm_quantize_act_int8(const void* X, qmm_dtype x_type, int64_t M, int64_t K, int64_t ldx,
+                                 int per_row, void* A, int64_t lda, float* s_x, void* workspace,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  if (X == nullptr || A == nullptr || s_x == nullptr) return QMM_ERR_INVALID_ARG;
+  if (x_type != QMM_F32 && x_type != QMM_BF16) return QMM_ERR_INVALID_ARG;
+  if (M < 1 || K < 1 || ldx < K || lda < K || lda % 16 != 0 || (per_row != 0 && per_row != 1))
+    return QMM_ERR_INVALID_ARG;
+  if (!aligned(X, x_type == QMM_F32 ? 4 : 2) || !aligned(A, 16) || !aligned(s_x, 4)) return QMM_ERR_INVALID_ARG;
+  if (M > INT32_MAX || K > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  if (!per_row && (workspace == nullptr || ws_bytes < 256 || !aligned(workspace, 16))) return QMM_ERR_WORKSPACE;
+  return cuda_status(launch_quantize_act(X, x_type == QMM_BF16, (int)M, (int)K, ldx, per_row == 1,
+                                         static_cast<int8_t*>(A), lda, s_x, workspace, stream));
+}
+
 // ---------------------------------------------------------------------------
 // 4-bit
 // ---------------------------------------------------------------------------

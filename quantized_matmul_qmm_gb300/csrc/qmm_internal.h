@@ -75,6 +75,9 @@ bool int8_umma_eligible(int64_t M, int64_t K, int64_t N);
 size_t int8_umma_workspace_bytes(int64_t M, int64_t K, int64_t N);
 cudaError_t launch_int8_gemm_umma(const Int8GemmArgs& a, void* workspace, int32_t* dev_status,
                                   cudaStream_t stream);
+// activation quantisation (quant_act.cu); the per-tensor path uses 4 bytes of workspace
+cudaError_t launch_quantize_act(const void* X, bool x_bf16, int M, int K, int64_t ldx, bool per_row, int8_t* A,
+                                int64_t lda, float* s_x, void* workspace, cudaStream_t stream);
 
 // ---- q4 kernels (q4_mma.cu, q4_umma.cu) ----
 struct Q4DenseArgs {

@@ -41,6 +41,9 @@ SIGNATURES = {
     "qmm_int8_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
     "qmm_int8_gemm": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _c.c_int,
                                  _i32, _c.POINTER(QmmEpilogue), _vp, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_quantize_act_int8_workspace_size": (_c.c_int, [_i64, _i64, _c.c_int, _szp]),
+    "qmm_quantize_act_int8": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _c.c_int, _vp, _i64, _vp, _vp, _sz,
+                                         _vp]),
     "qmm_pack_q4_size": (_c.c_int, [_i64, _i64, _szp]),
     "qmm_pack_q4": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "qmm_q4_gemm": (_c.c_int, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
@@ -141,6 +144,29 @@ def int8_gemm(A: torch.Tensor, a_type: str, zA: int, packed: torch.Tensor, col_s
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream()))
     return out
+
+
+def quantize_act_int8_workspace_size(M: int, K: int, per_row: bool) -> int:
+    return _size("qmm_quantize_act_int8_workspace_size", M, K, int(per_row))
+
+
+def quantize_act_int8(X: torch.Tensor, per_row: bool = True, A=None, s_x=None, workspace=None):
+    """Symmetric int8 codes of X (fp32 or bf16 [M][K] on the device) through
+    qmm_quantize_act_int8.  Returns (A int8 [M][K], s_x fp32 [M] or [1])."""
+    M, K = X.shape
+    x_type = {torch.float32: "f32", torch.bfloat16: "bf16"}[X.dtype]
+    if A is None:
+        lda = (K + 15) // 16 * 16
+        A = torch.empty((M, lda), dtype=torch.int8, device=X.device)[:, :K]
+    if s_x is None:
+        s_x = torch.empty(M if per_row else 1, dtype=torch.float32, device=X.device)
+    ws_need = quantize_act_int8_workspace_size(M, K, per_row)
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=X.device)
+    _check("qmm_quantize_act_int8", lib.qmm_quantize_act_int8(
+        _ptr(X), DTYPES[x_type], M, K, X.stride(0), int(per_row), _ptr(A), A.stride(0), _ptr(s_x),
+        _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(), _stream()))
+    return A, s_x
 
 
 # ---------------------------------------------------------------------------

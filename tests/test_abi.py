@@ -104,3 +104,22 @@ def test_binding_has_no_oracle_imports():
     for f in ("qmm.py", "build.py", "__init__.py", "inputs.py"):
         src = open(os.path.join(ROOT, "quantized_matmul_qmm_gb300", f)).read()
         assert not re.search(r"^\s*(import|from)\s+oracle", src, flags=re.M), f
+
+
+def test_quantize_act_host_validation(qmm):
+    L = qmm.lib
+    P = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: every call below fails on the host
+    sz = ctypes.c_size_t(0)
+    assert L.qmm_quantize_act_int8_workspace_size(4, 16, 0, ctypes.byref(sz)) == qmm.QMM_OK and sz.value == 256
+    assert L.qmm_quantize_act_int8_workspace_size(4, 16, 1, ctypes.byref(sz)) == qmm.QMM_OK and sz.value == 0
+    assert L.qmm_quantize_act_int8_workspace_size(4, 16, 2, ctypes.byref(sz)) == qmm.QMM_ERR_INVALID_ARG
+    q = L.qmm_quantize_act_int8
+    # x_type, per_row, lda % 16, lda < K, ldx < K, misaligned A, missing per-tensor workspace
+    assert q(P, qmm.QMM_S8, 4, 16, 16, 1, P, 16, P, None, 0, None) == qmm.QMM_ERR_INVALID_ARG
+    assert q(P, qmm.QMM_F32, 4, 16, 16, 2, P, 16, P, None, 0, None) == qmm.QMM_ERR_INVALID_ARG
+    assert q(P, qmm.QMM_F32, 4, 16, 16, 1, P, 24, P, None, 0, None) == qmm.QMM_ERR_INVALID_ARG
+    assert q(P, qmm.QMM_F32, 4, 40, 40, 1, P, 32, P, None, 0, None) == qmm.QMM_ERR_INVALID_ARG
+    assert q(P, qmm.QMM_F32, 4, 40, 39, 1, P, 48, P, None, 0, None) == qmm.QMM_ERR_INVALID_ARG
+    assert q(P, qmm.QMM_F32, 4, 16, 16, 1, ctypes.c_void_p((1 << 20) + 8), 16, P, None, 0, None) == qmm.QMM_ERR_INVALID_ARG
+    assert q(P, qmm.QMM_F32, 4, 16, 16, 0, P, 16, P, None, 0, None) == qmm.QMM_ERR_WORKSPACE
+    assert q(P, qmm.QMM_F32, 4, 16, 16, 0, P, 16, P, P, 64, None) == qmm.QMM_ERR_WORKSPACE

@@ -220,3 +220,51 @@ def test_packb_from_u8_shifts():
     p = O.pack_b_int8(B, "u8")
     assert np.array_equal(p["packed"][:, :33].T.astype(np.int64), B - 128)
     assert p["col_sum"].tolist() == [sum(int(B[k, n]) - 128 for k in range(33)) for n in range(5)]
+
+
+# ---------------------------------------------------------------------------
+# activation quantisation (s = amax/127 per row or per tensor, packB rounding)
+# ---------------------------------------------------------------------------
+
+def test_activation_quant_amax_maps_to_127_and_ties_to_even():
+    # amax = 127 gives s = 1 exactly, so the codes are the rounded values
+    X = np.array([[127.0, 2.5, 3.5, -2.5, 0.5, 1.5, -126.4, -0.49],
+                  [-127.0, 0.0, 63.5, -63.5, 64.5, 1e-8, 5.5, -5.5]], dtype=np.float32)
+    q, s = O.quantize_activations_f32(X, per_row=True)
+    assert list(s) == [1.0, 1.0]
+    assert q[0].tolist() == [127, 2, 4, -2, 0, 2, -126, 0]
+    assert q[1].tolist() == [-127, 0, 64, -64, 64, 0, 6, -6]
+
+
+def test_activation_quant_zero_row_and_bound():
+    g = np.random.default_rng(3)
+    X = (g.standard_normal((6, 257)) * np.array([[1e-3], [0.0], [1.0], [40.0], [1e4], [0.02]])).astype(np.float32)
+    q, s = O.quantize_activations_f32(X, per_row=True)
+    assert s[1] == 0.0 and not q[1].any()
+    for m in range(6):
+        assert np.abs(q[m]).max() <= 127
+        if s[m] > 0:
+            i = np.argmax(np.abs(X[m]))
+            assert abs(q[m, i]) == 127 and np.sign(q[m, i]) == np.sign(X[m, i])
+            # packB's rounding bound: |x - q s| <= s/2 (one fp32 rounding of x/s on top)
+            assert np.all(np.abs(X[m].astype(np.float64) - q[m] * s[m]) <= s[m] * 0.5 * (1 + 2.0 ** -22))
+
+
+def test_activation_quant_rows_are_packb_columns():
+    # the row rule is packB's column rule on the transpose (checked separately above)
+    g = np.random.default_rng(4)
+    X = (g.standard_normal((9, 130)) * 3).astype(np.float32)
+    q, s = O.quantize_activations_f32(X, per_row=True)
+    qc, sc = O.quantize_columns_f32(X.T)
+    assert np.array_equal(q, qc.T) and np.array_equal(s, sc)
+
+
+def test_activation_quant_per_tensor():
+    g = np.random.default_rng(5)
+    X = (g.standard_normal((7, 100)) * np.arange(1, 8)[:, None]).astype(np.float32)
+    q, s = O.quantize_activations_f32(X, per_row=False)
+    qr, sr = O.quantize_activations_f32(X, per_row=True)
+    assert s.shape == (1,) and s[0] == sr.max()                # one scale: the largest row's
+    assert np.array_equal(q[np.argmax(sr)], qr[np.argmax(sr)])  # that row is coded as per row
+    q1, s1 = O.quantize_activations_f32(X[2:3], per_row=False)
+    assert np.array_equal(q1, qr[2:3]) and s1[0] == sr[2]       # one row: the two modes agree
