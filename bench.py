@@ -319,6 +319,9 @@ def run_ours(args, rank, world, dev):
     streams = run_gemv_streams(hp, q, args, dev, stream)
     if int(hp.status.item()) != 0:
         raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
+    streams["w8"] = run_w8(q, I, args, dev, stream, hp.status, flush_l2)
+    if int(hp.status.item()) != 0:
+        raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
     return hp, per_call, total, clk, e2e_ms, streams
 
 
@@ -389,6 +392,79 @@ def run_gemv_streams(hp, q, args, dev, stream):
                            "launches_per_pass": 7 * C},
         "l2_bytes": l2,
     }
+
+
+def run_w8(q, I, args, dev, stream, status, flush_l2):
+    """W8A16 (int8 weights, one fp32 scale per row and 1,024 weights, bf16
+    activations), timed apart from the step:
+      * lm_head M=1 decode GEMV, back-to-back launches over rotating copies of
+        the codes totalling >= 4x the L2 size (as for the q4 GEMV);
+      * the tensor-core route (codes widened to bf16, then the pair GEMM) on
+        M=4096 K=N=4608 and on lm_head M=512, one call after an L2 flush.
+    Medians over `args.steps` timed repetitions after `args.warmup`."""
+    import math
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def timed(fn, flush):
+        out = []
+        for i in range(args.warmup + args.steps):
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
+            if flush:
+                flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= args.warmup:
+                out.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) * 1e3 for a, b in out)
+
+    res = {}
+    name, K, N = I.QWEN3_06B_LM_HEAD
+    W = I.q4_weights(9 * 1000 + N % 997 + K, N, K).to(dev)
+    codes, scales = q.pack_w8(W)
+    del W
+    wbytes = codes.numel() + scales.numel() * 4
+    x1 = I.q4_activations(9 * 7919 + 1, 1, K).to(dev)
+    y1 = torch.empty((1, N), dtype=torch.float32, device=dev)
+    R = max(2, math.ceil(4 * l2 / wbytes))
+    copies = [(codes, scales)] + [(codes.clone(), scales.clone()) for _ in range(R - 1)]
+
+    def lm_pass():
+        for c, sc in copies:
+            q.w8_gemm(c, sc, N, K, x1, Y=y1, dev_status=status)
+
+    us = timed(lm_pass, False) / R
+    res["w8_gemv_lm_head_m1_stream"] = {"us": us, "copies": R, "launches": 1, "weight_bytes": wbytes,
+                                       "weight_GBs": wbytes / (us * 1e-6) / 1e9,
+                                       "GBs": (wbytes + 2 * K + 4 * N) / (us * 1e-6) / 1e9}
+    del copies
+    us = timed(lambda: q.w8_gemm(codes, scales, N, K, x1, Y=y1, dev_status=status), True)
+    res["w8_gemv_lm_head_m1"] = {"us": us, "launches": 1, "weight_bytes": wbytes,
+                                "weight_GBs": wbytes / (us * 1e-6) / 1e9,
+                                "GBs": (wbytes + 2 * K + 4 * N) / (us * 1e-6) / 1e9}
+    x512 = I.q4_activations(9 * 7919 + 512, 512, K).to(dev)
+    y512 = torch.empty((512, N), dtype=torch.float32, device=dev)
+    ws = torch.empty(q.w8_gemm_workspace_size(512, K, N), dtype=torch.uint8, device=dev)
+    us = timed(lambda: q.w8_gemm(codes, scales, N, K, x512, Y=y512, workspace=ws, dev_status=status), True)
+    res["w8_gemm_lm_head_m512"] = {"us": us, "launches": 2, "TFLOPS": 2 * 512 * N * K / (us * 1e-6) / 1e12,
+                                   "weight_bytes": wbytes}
+    del codes, scales, ws, y512, x512
+    M, Kb, Nb = 4096, 4608, 4608
+    W = I.q4_weights(4608, Nb, Kb).to(dev)
+    codes, scales = q.pack_w8(W)
+    del W
+    X = I.q4_activations(4096, M, Kb).to(dev)
+    Y = torch.empty((M, Nb), dtype=torch.float32, device=dev)
+    ws = torch.empty(q.w8_gemm_workspace_size(M, Kb, Nb), dtype=torch.uint8, device=dev)
+    us = timed(lambda: q.w8_gemm(codes, scales, Nb, Kb, X, Y=Y, workspace=ws, dev_status=status), True)
+    res["w8_gemm_m4096"] = {"us": us, "launches": 2, "TFLOPS": 2 * M * Nb * Kb / (us * 1e-6) / 1e12,
+                            "shape": f"M={M} K={Kb} N={Nb}"}
+    del codes, scales, ws, X, Y
+    torch.cuda.synchronize()
+    return res
 
 
 def cpu_int8_sample(rows: int):
@@ -493,6 +569,15 @@ def main():
     rooflines["q4_gemv_projection_set_m1_graph"] = {"bound": "hbm", "achieved": st_ps["GBs"], "peak": hbm_peak,
                                                     "unit": "GB/s", "frac": st_ps["GBs"] / hbm_peak,
                                                     "traffic": None}
+    w8 = streams["w8"]
+    for name in ("w8_gemv_lm_head_m1_stream", "w8_gemv_lm_head_m1"):
+        d = w8[name]
+        rooflines[name] = {"bound": "hbm", "achieved": d["GBs"], "peak": hbm_peak, "unit": "GB/s",
+                           "frac": d["GBs"] / hbm_peak, "traffic": traffic.get("w8_gemv_lm_head_m1")}
+    for name in ("w8_gemm_lm_head_m512", "w8_gemm_m4096"):
+        d = w8[name]
+        rooflines[name] = {"bound": "tensor", "achieved": d["TFLOPS"], "peak": tensor_peak, "unit": "TFLOP/s",
+                           "frac": d["TFLOPS"] / tensor_peak, "traffic": traffic.get(name)}
     c = hp.int8
     launches = sum(l for (_, _, l, _) in hp.calls) * args.steps
     line = {
@@ -514,6 +599,9 @@ def main():
                  "single_call": {"weight_GBs": world * lm["weight_GBs"], "frac_hbm": lm["GBs"] / hbm_peak,
                                  "us": lm["us"], "note": "one launch timed alone after an L2 flush"}},
         "kernels": kern,
+        "w8a16": {"note": "int8 weights with one fp32 scale per row and 1,024 weights, bf16 activations; "
+                          "timed apart from the step (median, L2 flushed before each single call)",
+                  **w8},
         "e2e": {"value": world * 2.0 * c.M * c.N * c.K / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
                 "h2d_bytes_per_step": c.M * c.K, "d2h_bytes_per_step": c.M * c.N},
         "gpu_launches": launches,

@@ -288,6 +288,64 @@ qmm_status qmm_q4_gemm_id_noalloc(const void* tiles, int64_t n_expert, int64_t N
                                   float* Y, int64_t ldy_token, int64_t ldy_slot,
                                   int32_t* dev_status, cudaStream_t stream);
 
+/* ========================================================================
+ * (III) W8A16: int8 weights with block scales, bf16 activations
+ *
+ * "llama.cpp-xdna -- CPU, iGPU and XDNA1 NPU on AMD Ryzen APUs", sections
+ * "The NPU worker" and "Running": the GGML_XDNA_NPU_W8 mode keeps the weights
+ * as int8 with one scale per row and 1,024 weights, forms the partial sums
+ * per block of inputs, and applies the block scales to them.
+ *
+ * Layout (this library's own; the page gives the block size, not the bytes):
+ *   codes   int8 [N][Kp], Kp = K rounded up to 64, row n = output n, zeros in
+ *           the padding columns.
+ *   scales  fp32 [N][nb], nb = ceil(K / 1024): scale of (row n, block b)
+ *           covers columns 1024 b .. min(K, 1024 b + 1024) - 1.
+ * ======================================================================== */
+
+/* Bytes of the codes (N * Kp) and of the scales (N * nb * 4).  K <= 65536,
+ * N <= 2^31 - 1, else QMM_ERR_UNSUPPORTED. */
+qmm_status qmm_pack_w8_size(int64_t N, int64_t K, size_t* code_bytes, size_t* scale_bytes);
+
+/* Quantise fp32 W [N][K] (row stride ldw elements, ldw >= K).  Per (row n,
+ * block b), with IEEE fp32 steps (the same rule as qmm_pack_b_int8):
+ *   s = fl(amax / 127), amax = max |W[n][k]| over the block;
+ *   q = clamp(rint_even(fl(W[n][k] / s)), -127, 127), 0 where s == 0.
+ * codes 16-byte aligned with code_bytes >= the size above; scales 4-byte
+ * aligned.  W must be finite.  Errors: QMM_ERR_INVALID_ARG for null or
+ * misaligned pointers, short buffers, N < 1, K < 1 or ldw < K.
+ */
+qmm_status qmm_pack_w8(const float* W, int64_t N, int64_t K, int64_t ldw, void* codes, size_t code_bytes,
+                       float* scales, size_t scale_bytes, cudaStream_t stream);
+
+/* Workspace of qmm_w8_gemm: 0 for M <= 16 (the decode GEMV), else N * Kp * 2
+ * bytes (the codes widened to bf16 for the tensor cores). */
+qmm_status qmm_w8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes);
+
+/* Y[m][n] = sum_b scales[n][b] * sum_{k in block b} codes[n][k] * X[m][k],
+ * with fp32 accumulation.
+ *
+ * X      bf16 [M][K], row stride ldx elements (ldx >= K, ldx % 8 == 0, base
+ *        16-byte aligned).
+ * Y      fp32 [M][N], row stride ldy elements (ldy >= N), 4-byte aligned.
+ * workspace / ws_bytes  qmm_w8_gemm_workspace_size bytes, 256-byte aligned
+ *        (NULL when that size is 0), rewritten by the call.
+ * M <= 16 runs the decode GEMV (codes streamed once, one warp per row);
+ * larger M the tensor-core GEMM (the codes widened to bf16, which is exact;
+ * each 1,024-k block summed in the tensor cores' fp32 accumulator, then
+ * scaled).  Both compute the same function, within
+ * max |y - y_exact| <= 2e-4 * sum_k |x| |w|: the products code * x are exact
+ * in fp32, so the only error is fp32 summation over at most 1,024 terms per
+ * block (1,024 * 2^-23 < 1.3e-4 even if every addition truncates) and over
+ * the at most 64 blocks.
+ * Errors: QMM_ERR_INVALID_ARG for null or misaligned pointers and bad sizes or
+ * strides; QMM_ERR_WORKSPACE for a missing or short workspace;
+ * QMM_ERR_UNSUPPORTED for K > 65536.
+ */
+qmm_status qmm_w8_gemm(const void* codes, const float* scales, int64_t N, int64_t K, const void* X, int64_t M,
+                       int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                       cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -437,3 +437,51 @@ def normalized_error(y_test, y_ref, norm):
         return float("inf")
     d = np.abs(y_test - y_ref)
     return float((d[~zero] / norm[~zero]).max(initial=0.0))
+
+
+# ----------------------------------------------------------------------------
+# W8A16: int8 weights with one scale per row and 1,024 weights, bf16 activations
+# ----------------------------------------------------------------------------
+# "llama.cpp-xdna -- CPU, iGPU and XDNA1 NPU on AMD Ryzen APUs", sections "The
+# NPU worker" and "Running" (GGML_XDNA_NPU_W8): weights as int8 with one scale
+# per row and 1,024 weights, activations bf16;
+# partial sums are formed per block of inputs and the int8 scales applied to
+# them.  The per-block quantisation rule is packB's (amax/127, round half to
+# even, clamp to +-127, zero block -> scale 0): the pages give the granularity,
+# not the rounding.
+
+W8_BLOCK = 1024
+
+
+def pack_w8(W):
+    """W: fp32 values [N][K] (weight rows).  Returns (codes int64 [N][K],
+    scales fp64 holding fp32 values [N][ceil(K/1024)])."""
+    W = _f32(np.asarray(W, np.float64))
+    N, K = W.shape
+    nb = (K + W8_BLOCK - 1) // W8_BLOCK
+    q = np.zeros((N, K), dtype=np.int64)
+    s = np.zeros((N, nb))
+    for b in range(nb):
+        blk = W[:, b * W8_BLOCK:(b + 1) * W8_BLOCK]
+        sc = _f32(np.abs(blk).max(axis=1) / 127.0)
+        s[:, b] = sc
+        for n in range(N):
+            if sc[n] > 0:
+                q[n, b * W8_BLOCK:(b + 1) * W8_BLOCK] = np.clip(np.rint(_f32(blk[n] / sc[n])), -127, 127)
+    return q, s
+
+
+def w8_gemm(codes, scales, X):
+    """Y[m][n] = sum_b scales[n][b] * sum_{k in block b} codes[n][k] * X[m][k], in fp64.
+    Also returns the normaliser sum_k |x| |w| per output (w = code * scale)."""
+    codes = np.asarray(codes, np.float64)
+    X = np.asarray(X, np.float64)
+    N, K = codes.shape
+    M = X.shape[0]
+    Y = np.zeros((M, N))
+    norm = np.zeros((M, N))
+    for b in range(scales.shape[1]):
+        sl = slice(b * W8_BLOCK, min(K, (b + 1) * W8_BLOCK))
+        Y += (X[:, sl] @ codes[:, sl].T) * scales[:, b][None, :]
+        norm += (np.abs(X[:, sl]) @ np.abs(codes[:, sl]).T) * scales[:, b][None, :]
+    return Y, norm

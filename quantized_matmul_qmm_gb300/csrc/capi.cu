@@ -162,6 +162,54 @@ qmm_status qmm_quantize_act_int8(const void* X, qmm_dtype x_type, int64_t M, int
 }
 
 // ---------------------------------------------------------------------------
+// W8A16: int8 weights, one fp32 scale per row and 1,024 weights
+// ---------------------------------------------------------------------------
+
+qmm_status qmm_pack_w8_size(int64_t N, int64_t K, size_t* code_bytes, size_t* scale_bytes) {
+  if (code_bytes == nullptr || scale_bytes == nullptr || N < 1 || K < 1) return QMM_ERR_INVALID_ARG;
+  if (N > INT32_MAX || K > kW8MaxK) return QMM_ERR_UNSUPPORTED;
+  *code_bytes = (size_t)N * w8_padded_k(K);
+  *scale_bytes = (size_t)N * w8_blocks(K) * sizeof(float);
+  return QMM_OK;
+}
+
+qmm_status qmm_pack_w8(const float* W, int64_t N, int64_t K, int64_t ldw, void* codes, size_t code_bytes,
+                       float* scales, size_t scale_bytes, cudaStream_t stream) {
+  if (W == nullptr || codes == nullptr || scales == nullptr || N < 1 || K < 1 || ldw < K)
+    return QMM_ERR_INVALID_ARG;
+  if (N > INT32_MAX || K > kW8MaxK) return QMM_ERR_UNSUPPORTED;
+  if (!aligned(W, 4) || !aligned(codes, 16) || !aligned(scales, 4)) return QMM_ERR_INVALID_ARG;
+  if (code_bytes < (size_t)N * w8_padded_k(K) || scale_bytes < (size_t)N * w8_blocks(K) * sizeof(float))
+    return QMM_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_w8(W, (int)N, (int)K, ldw, static_cast<int8_t*>(codes), scales, stream));
+}
+
+qmm_status qmm_w8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes) {
+  if (ws_bytes == nullptr || M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (K > kW8MaxK) return QMM_ERR_UNSUPPORTED;
+  *ws_bytes = M > kW8GemvMaxM ? w8_umma_workspace_bytes(K, N) : 0;
+  return QMM_OK;
+}
+
+qmm_status qmm_w8_gemm(const void* codes, const float* scales, int64_t N, int64_t K, const void* X, int64_t M,
+                       int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                       cudaStream_t stream) {
+  if (codes == nullptr || scales == nullptr || X == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
+  if (N < 1 || K < 1 || M < 1 || ldx < K || ldy < N) return QMM_ERR_INVALID_ARG;
+  if (ldx % 8 != 0 || !aligned(X, 16) || !aligned(codes, 16) || !aligned(scales, 4) || !aligned(Y, 4))
+    return QMM_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > kW8MaxK) return QMM_ERR_UNSUPPORTED;
+  const int8_t* c = static_cast<const int8_t*>(codes);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
+  if (M <= kW8GemvMaxM) return cuda_status(launch_w8_gemv(c, scales, (int)N, (int)K, x, ldx, (int)M, Y, ldy, stream));
+  const size_t need = w8_umma_workspace_bytes(K, N);
+  if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256)) return QMM_ERR_WORKSPACE;
+  if ((N + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;
+  return cuda_status(launch_w8_gemm_umma(c, scales, (int)N, (int)K, x, ldx, (int)M, Y, ldy, workspace, dev_status,
+                                         stream));
+}
+
+// ---------------------------------------------------------------------------
 // 4-bit
 // ---------------------------------------------------------------------------
 

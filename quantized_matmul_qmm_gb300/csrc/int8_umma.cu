@@ -24,6 +24,7 @@
 //      in the even CTA, issues the MMAs; warps 2..9 drain the CTA's own
 //      128 x 256 accumulator and run the exact epilogue: zero points, bias,
 //      output conversion.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -68,7 +69,14 @@ struct Int8UmmaParams {
   const int32_t* row_sum;            // [M] (null when zB' == 0)
   Int8Epi epi;
   int32_t* dev_status;
+  const float* w8_scales;            // W8A16: [N][w8_nb], one per row and 1,024 k
+  int w8_nb;
 };
+
+// W8A16 instance of the kernel: bf16 activations x int8 weights widened to
+// bf16 (exact), each 1,024-k accumulator chunk scaled per column by its
+// block's weight scale, fp32 output.
+constexpr int kW8Out = 100;
 
 // Output conversion of one element (fp32 steps with explicit IEEE rounding),
 // specialised on the output type; kPerRowMq: requantisation with a per-row
@@ -227,7 +235,7 @@ int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       // The issue loop is kept short (stage and phase counted, descriptors
       // offset from precomputed bases): the tensor pipe queues few MMAs, so
       // this thread's latency per 64-k block is on the critical path.
-      constexpr uint32_t idesc = idesc_f16(2 * kBM, kBN, false);
+      constexpr uint32_t idesc = idesc_f16(2 * kBM, kBN, kOut == kW8Out);   // bf16 operands for W8A16
       const uint64_t adesc0 = desc_kmajor_sw128(smem_u32(sA)), bdesc0 = desc_kmajor_sw128(smem_u32(sB));
       int s = 0, gc = 0;  // stage; chunks issued (all tiles)
       uint32_t ph = 0;    // phase parity of the full barriers at stage s
@@ -262,7 +270,83 @@ int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       umma_commit_pair(done, 0x1);
       mbar_wait(done, 0, abort_flag, p.dev_status);
     }
-  } else if (warp >= kEpiWarp0) {
+  } else if (kOut == kW8Out && warp >= kEpiWarp0) {
+    // W8A16 epilogue: each 1,024-k chunk of the accumulator, times the weight
+    // scale of that chunk's block for each column, is added in fp32.  A warp's
+    // 128 column scales are fetched one chunk ahead into shared memory.
+    const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
+    const int ew = warp - kEpiWarp0;
+    float* scs = reinterpret_cast<float*>(sConst) + ew * 768;   // [2][128]
+    const uint32_t tempty_even[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
+    auto load_scales = [&](int t, int c, int b) {
+      const int nbase = (t % p.tiles_n) * kBN + h * 128;
+      float sv[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int n = nbase + lane + 32 * v;
+        sv[v] = n < p.N ? p.w8_scales[(int64_t)n * p.w8_nb + c] : 0.f;
+      }
+#pragma unroll
+      for (int v = 0; v < 4; ++v) scs[b * 128 + lane + 32 * v] = sv[v];
+    };
+    if (pair < p.ntiles) load_scales(pair, 0, 0);
+    __syncwarp();
+    float* Yf = reinterpret_cast<float*>(p.epi.out);
+    const bool vec_ok = ((reinterpret_cast<uintptr_t>(Yf) & 15) == 0) && (p.epi.ldo % 4 == 0);
+    int gc = 0;
+    bool ok = true;
+    for (int t = pair; t < p.ntiles && ok; t += npairs) {
+      const int m0 = (t / p.tiles_n) * (2 * kBM) + (int)rank * kBM, n0 = (t % p.tiles_n) * kBN;
+      const int nbase = n0 + h * 128;
+      const int row = m0 + 32 * q + lane;
+      float acc[128];
+      for (int c = 0; c < nchunks; ++c, ++gc) {
+        const int d = gc & 1, u = gc >> 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[d], u & 1, abort_flag, p.dev_status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float* sc = scs + (gc & 1) * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * kBN + h * 128 + 32 * j), r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float v = __uint_as_float(r[i]), w = sc[32 * j + i];
+            acc[32 * j + i] = (c == 0) ? __fmul_rn(v, w) : fmaf(v, w, acc[32 * j + i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tempty_even[d]);
+        // the next chunk's scales: this tile's next block, or the next tile's first
+        if (c + 1 < nchunks) load_scales(t, c + 1, (gc + 1) & 1);
+        else if (t + npairs < p.ntiles) load_scales(t + npairs, 0, (gc + 1) & 1);
+        __syncwarp();
+      }
+      if (ok && row < p.M) {
+        float* yrow = Yf + (int64_t)row * p.epi.ldo;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int nb = nbase + 32 * j;
+          if (vec_ok && nb + 32 <= p.N) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              reinterpret_cast<float4*>(yrow + nb)[v] = make_float4(acc[32 * j + 4 * v], acc[32 * j + 4 * v + 1],
+                                                                     acc[32 * j + 4 * v + 2], acc[32 * j + 4 * v + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (nb + i < p.N) yrow[nb + i] = acc[32 * j + i];
+          }
+        }
+      }
+      __syncwarp();
+    }
+  } else if (kOut != kW8Out && warp >= kEpiWarp0) {
     // epilogue: warp w reads TMEM lanes 32*(w%4).. and columns h*128..h*128+127
     const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
     const int ew = warp - kEpiWarp0;
@@ -381,6 +465,7 @@ struct WidenParams {
   int32_t* dev_status;
   int M, K, N, Kp, R;
   bool a_u8;
+  bool b_bf16;   // B' as bf16 instead of f16 (the W8A16 instance; M == 0 then)
 };
 
 __global__ void __launch_bounds__(kWidenThreads) int8_widen_kernel(const WidenParams p) {
@@ -452,6 +537,16 @@ __global__ void __launch_bounds__(kWidenThreads) int8_widen_kernel(const WidenPa
             }
           }
         }
+        if (p.b_bf16) {
+          // every int8 code is exact in bf16 (8 significant bits)
+          __nv_bfloat16 h[8];
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) h[4 * q + b] = __int2bfloat16_rn((int)(int8_t)(w[q] >> (8 * b)));
+          *reinterpret_cast<uint4*>(dst + k) = *reinterpret_cast<const uint4*>(h);
+          continue;
+        }
         __half h[8];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -502,10 +597,12 @@ WsLayout ws_layout(int64_t M, int64_t K, int64_t N) {
 
 using UmmaKernel = void (*)(CUtensorMap, CUtensorMap, Int8UmmaParams);
 // One instantiation per output conversion: S32, F32, S8, U8, then S8 and U8
-// with a per-row activation scale.
-constexpr UmmaKernel kUmmaKernels[6] = {
+// with a per-row activation scale; last the W8A16 instance.
+constexpr UmmaKernel kUmmaKernels[7] = {
     int8_umma_kernel<QMM_S32, false>, int8_umma_kernel<QMM_F32, false>, int8_umma_kernel<QMM_S8, false>,
-    int8_umma_kernel<QMM_U8, false>,  int8_umma_kernel<QMM_S8, true>,   int8_umma_kernel<QMM_U8, true>};
+    int8_umma_kernel<QMM_U8, false>,  int8_umma_kernel<QMM_S8, true>,   int8_umma_kernel<QMM_U8, true>,
+    int8_umma_kernel<kW8Out, false>};
+constexpr int kW8Kernel = 6;
 
 // Clusters of two that fit on the device at once (a GPC with an odd SM count
 // leaves one SM over), with the kernel's shared-memory opt-in done: once per
@@ -616,6 +713,68 @@ cudaError_t launch_int8_gemm_umma(const Int8GemmArgs& a, void* workspace, int32_
   const bool per_row_mq = (ot == QMM_S8 || ot == QMM_U8) && a.epi.s_x != nullptr && a.epi.s_x_stride != 0;
   const int which = ot == QMM_S32 ? 0 : ot == QMM_F32 ? 1 : (ot == QMM_S8 ? 2 : 3) + (per_row_mq ? 2 : 0);
   return cudaLaunchKernelEx(&cfg, kUmmaKernels[which], tmA, tmB, p);
+}
+
+size_t w8_umma_workspace_bytes(int64_t K, int64_t N) { return (size_t)N * padded_k(K) * 2; }
+
+// W8A16 GEMM on the pair kernel: the weight codes are widened to bf16 (exact)
+// into the workspace, the bf16 activations are read by TMA in place (rows
+// past M and columns past K arrive as zeros), and each 1,024-k accumulator
+// chunk is scaled by its block's per-row weight scale in the epilogue.
+cudaError_t launch_w8_gemm_umma(const int8_t* codes, const float* scales, int N, int K,
+                                const __nv_bfloat16* X, int64_t ldx, int M, float* Y, int64_t ldy,
+                                void* workspace, int32_t* dev_status, cudaStream_t stream) {
+  const int Kp = (int)padded_k(K);
+  __nv_bfloat16* B16 = static_cast<__nv_bfloat16*>(workspace);
+  WidenParams wp{};
+  wp.B = codes;
+  wp.B16 = reinterpret_cast<__half*>(B16);
+  wp.dev_status = dev_status;
+  wp.M = 0;
+  wp.K = K;
+  wp.N = N;
+  wp.Kp = Kp;
+  wp.b_bf16 = true;
+  wp.R = std::max(1, std::min(kWidenMaxRows, kWidenGroupBytes / Kp));
+  const size_t wsmem = 128 + (size_t)2 * wp.R * Kp;
+  const int ngroups = (N + wp.R - 1) / wp.R;
+  int pairs = 0;
+  cudaError_t err = resident_pairs(&pairs);
+  if (err != cudaSuccess) return err;
+  const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(8, (200u << 10) / wsmem));
+  const int wgrid = std::min(ngroups, 2 * pairs * per_sm);
+  int8_widen_kernel<<<wgrid, kWidenThreads, wsmem, stream>>>(wp);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+
+  CUtensorMap tmA, tmB;
+  if (!make_tmap_2d(&tmA, true, const_cast<__nv_bfloat16*>(X), (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2, kBK,
+                    kBM) ||
+      !make_tmap_2d(&tmB, true, B16, (uint64_t)Kp, (uint64_t)N, (uint64_t)Kp * 2, kBK, kBNh))
+    return cudaErrorInvalidValue;
+  Int8UmmaParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.Kp = Kp;
+  p.tiles_n = (N + kBN - 1) / kBN;
+  p.ntiles = ((M + 2 * kBM - 1) / (2 * kBM)) * p.tiles_n;
+  p.epi.out = Y;
+  p.epi.ldo = ldy;
+  p.dev_status = dev_status;
+  p.w8_scales = scales;
+  p.w8_nb = (K + kChunkK - 1) / kChunkK;
+  if (pairs > p.ntiles) pairs = p.ntiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;   // overlap the widen grid
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kUmmaKernels[kW8Kernel], tmA, tmB, p);
 }
 
 }  // namespace qmm

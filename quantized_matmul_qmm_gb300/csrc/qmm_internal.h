@@ -79,6 +79,20 @@ cudaError_t launch_int8_gemm_umma(const Int8GemmArgs& a, void* workspace, int32_
 cudaError_t launch_quantize_act(const void* X, bool x_bf16, int M, int K, int64_t ldx, bool per_row, int8_t* A,
                                 int64_t lda, float* s_x, void* workspace, cudaStream_t stream);
 
+// ---- W8A16 (w8.cu, and the pair kernel in int8_umma.cu for M > kW8GemvMaxM) ----
+constexpr int64_t kW8MaxK = 65536;
+constexpr int64_t kW8GemvMaxM = 16;
+int64_t w8_padded_k(int64_t K);   // codes per row: K rounded up to 64
+int64_t w8_blocks(int64_t K);     // scales per row: ceil(K / 1024)
+cudaError_t launch_pack_w8(const float* W, int N, int K, int64_t ldw, int8_t* codes, float* scales,
+                           cudaStream_t stream);
+cudaError_t launch_w8_gemv(const int8_t* codes, const float* scales, int N, int K, const __nv_bfloat16* X,
+                           int64_t ldx, int M, float* Y, int64_t ldy, cudaStream_t stream);
+size_t w8_umma_workspace_bytes(int64_t K, int64_t N);
+cudaError_t launch_w8_gemm_umma(const int8_t* codes, const float* scales, int N, int K,
+                                const __nv_bfloat16* X, int64_t ldx, int M, float* Y, int64_t ldy,
+                                void* workspace, int32_t* dev_status, cudaStream_t stream);
+
 // ---- q4 kernels (q4_mma.cu, q4_umma.cu) ----
 struct Q4DenseArgs {
   const uint8_t* tiles;

@@ -52,6 +52,10 @@ SIGNATURES = {
                                   _vp, _i64, _i64, _vp, _sz, _vp, _vp]),
     "qmm_q4_gemm_id_noalloc": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
                                           _i64, _vp, _i64, _i64, _vp, _vp]),
+    "qmm_pack_w8_size": (_c.c_int, [_i64, _i64, _szp, _szp]),
+    "qmm_pack_w8": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _sz, _vp, _sz, _vp]),
+    "qmm_w8_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
+    "qmm_w8_gemm": (_c.c_int, [_vp, _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _vp]),
 }
 
 
@@ -237,4 +241,46 @@ def q4_gemm_id_noalloc(tiles: torch.Tensor, n_expert: int, N: int, K: int, X: to
     _check("qmm_q4_gemm_id_noalloc", lib.qmm_q4_gemm_id_noalloc(
         _ptr(tiles), n_expert, N, K, _ptr(X), ldx_token, ldx_slot, _ptr(ids), ld_ids, n_used, T,
         _ptr(Y), Y.stride(0), Y.stride(1), _ptr(dev_status), _stream()))
+    return Y
+
+
+# ---------------------------------------------------------------------------
+# W8A16
+# ---------------------------------------------------------------------------
+
+def pack_w8_size(N: int, K: int):
+    """(code bytes, scale bytes) of an N x K weight."""
+    cb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("qmm_pack_w8_size", lib.qmm_pack_w8_size(N, K, ctypes.byref(cb), ctypes.byref(sb)))
+    return int(cb.value), int(sb.value)
+
+
+def pack_w8(W: torch.Tensor):
+    """W: device fp32 [N][K].  Returns (codes int8 [N][Kp], scales fp32 [N][ceil(K/1024)])."""
+    N, K = W.shape
+    cb, sb = pack_w8_size(N, K)
+    codes = torch.empty((N, cb // N), dtype=torch.int8, device=W.device)
+    scales = torch.empty((N, sb // (4 * N)), dtype=torch.float32, device=W.device)
+    _check("qmm_pack_w8", lib.qmm_pack_w8(_ptr(W), N, K, W.stride(0), _ptr(codes), cb, _ptr(scales), sb,
+                                          _stream()))
+    return codes, scales
+
+
+def w8_gemm_workspace_size(M: int, K: int, N: int) -> int:
+    return _size("qmm_w8_gemm_workspace_size", M, K, N)
+
+
+def w8_gemm(codes: torch.Tensor, scales: torch.Tensor, N: int, K: int, X: torch.Tensor, Y=None, workspace=None,
+            dev_status=None):
+    """Y[m][n] = sum_b scales[n][b] sum_{k in b} codes[n][k] X[m][k]; X bf16 [M][K] on the device."""
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        need = w8_gemm_workspace_size(M, K, N)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    _check("qmm_w8_gemm", lib.qmm_w8_gemm(
+        _ptr(codes), _ptr(scales), N, K, _ptr(X), M, X.stride(0), _ptr(Y), Y.stride(0), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
     return Y

@@ -123,3 +123,33 @@ def test_quantize_act_host_validation(qmm):
     assert q(P, qmm.QMM_F32, 4, 16, 16, 1, ctypes.c_void_p((1 << 20) + 8), 16, P, None, 0, None) == qmm.QMM_ERR_INVALID_ARG
     assert q(P, qmm.QMM_F32, 4, 16, 16, 0, P, 16, P, None, 0, None) == qmm.QMM_ERR_WORKSPACE
     assert q(P, qmm.QMM_F32, 4, 16, 16, 0, P, 16, P, P, 64, None) == qmm.QMM_ERR_WORKSPACE
+
+
+def test_w8_sizes_and_host_validation(qmm):
+    # codes N x Kp (K rounded up to 64), scales N x ceil(K / 1024) fp32
+    assert qmm.pack_w8_size(3, 1) == (3 * 64, 3 * 4)
+    assert qmm.pack_w8_size(1024, 1024) == (1024 * 1024, 1024 * 4)
+    assert qmm.pack_w8_size(7, 1025) == (7 * 1088, 7 * 2 * 4)
+    assert qmm.pack_w8_size(2, 65536) == (2 * 65536, 2 * 64 * 4)
+    assert qmm.w8_gemm_workspace_size(16, 1000, 300) == 0
+    assert qmm.w8_gemm_workspace_size(17, 1000, 300) == 300 * 1024 * 2
+    L = qmm.lib
+    P = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: every call below fails on the host
+    cb, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert L.qmm_pack_w8_size(2, 65537, ctypes.byref(cb), ctypes.byref(sb)) == qmm.QMM_ERR_UNSUPPORTED
+    assert L.qmm_pack_w8_size(0, 16, ctypes.byref(cb), ctypes.byref(sb)) == qmm.QMM_ERR_INVALID_ARG
+    pk = L.qmm_pack_w8
+    # ldw < K, short code buffer, short scale buffer, misaligned codes
+    assert pk(P, 4, 100, 99, P, 4 * 128, P, 16, None) == qmm.QMM_ERR_INVALID_ARG
+    assert pk(P, 4, 100, 100, P, 4 * 128 - 1, P, 16, None) == qmm.QMM_ERR_INVALID_ARG
+    assert pk(P, 4, 100, 100, P, 4 * 128, P, 15, None) == qmm.QMM_ERR_INVALID_ARG
+    assert pk(P, 4, 100, 100, ctypes.c_void_p((1 << 20) + 8), 4 * 128, P, 16, None) == qmm.QMM_ERR_INVALID_ARG
+    g = L.qmm_w8_gemm
+    # ldx % 8, ldx < K, ldy < N, misaligned X, K too large, missing or short workspace (M > 16)
+    assert g(P, P, 64, 100, P, 4, 100, P, 64, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, P, 64, 100, P, 4, 96, P, 64, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, P, 64, 96, P, 4, 96, P, 63, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, P, 64, 96, ctypes.c_void_p((1 << 20) + 2), 4, 96, P, 64, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, P, 64, 65544, P, 4, 65544, P, 64, None, 0, None, None) == qmm.QMM_ERR_UNSUPPORTED
+    assert g(P, P, 64, 96, P, 17, 96, P, 64, None, 0, None, None) == qmm.QMM_ERR_WORKSPACE
+    assert g(P, P, 64, 96, P, 17, 96, P, 64, P, 64 * 128 * 2 - 1, None, None) == qmm.QMM_ERR_WORKSPACE

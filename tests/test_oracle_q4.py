@@ -200,3 +200,51 @@ def test_normalized_error():
     assert O.normalized_error([1.0, 0.0], [1.0, 0.0], [2.0, 0.0]) == 0.0
     assert O.normalized_error([1.1, 0.0], [1.0, 0.0], [2.0, 0.0]) == pytest.approx(0.05)
     assert O.normalized_error([1.0, 1e-9], [1.0, 0.0], [2.0, 0.0]) == float("inf")
+
+
+# ---------------------------------------------------------------------------
+# W8A16 (int8 weights, one scale per row and 1,024 weights)
+# ---------------------------------------------------------------------------
+
+def test_w8_blocks_are_packb_columns():
+    # each (row, 1024-block) follows packB's column rule: compare block by block
+    g = np.random.default_rng(11)
+    W = (g.standard_normal((5, 2500)) * np.array([[0.02], [1.0], [0.0], [3e-4], [50.0]])).astype(np.float32)
+    q, s = O.pack_w8(W)
+    assert s.shape == (5, 3)
+    for b in range(3):
+        blk = W[:, b * 1024:(b + 1) * 1024]
+        qc, sc = O.quantize_columns_f32(blk.T)
+        assert np.array_equal(q[:, b * 1024:(b + 1) * 1024], qc.T) and np.array_equal(s[:, b], sc)
+    assert not q[2].any() and not s[2].any()            # zero row: scale 0, codes 0
+    assert np.abs(q).max() == 127
+
+
+def test_w8_gemm_brute_force_and_block_scales():
+    g = np.random.default_rng(12)
+    N, K, M = 3, 2100, 2
+    q = g.integers(-127, 128, (N, K))
+    s = g.uniform(1e-3, 1e-1, (N, 3))
+    X = g.standard_normal((M, K))
+    Y, norm = O.w8_gemm(q, s, X)
+    for m in range(M):
+        for n in range(N):
+            want = sum(s[n, k // 1024] * q[n, k] * X[m, k] for k in range(K))
+            assert abs(Y[m, n] - want) <= 1e-9 * norm[m, n]
+            assert abs(norm[m, n] - sum(abs(s[n, k // 1024] * q[n, k] * X[m, k]) for k in range(K))) <= 1e-9 * norm[m, n]
+    # a block's scale multiplies only that block's partial sum
+    s2 = s.copy()
+    s2[1, 2] *= 2
+    Y2, _ = O.w8_gemm(q, s2, X)
+    part = X[:, 2048:] @ q[1, 2048:].astype(np.float64)
+    assert np.allclose(Y2[:, 1] - Y[:, 1], part * s[1, 2])
+    assert np.array_equal(Y2[:, [0, 2]], Y[:, [0, 2]])
+
+
+def test_w8_decode_bound():
+    g = np.random.default_rng(13)
+    W = (g.standard_normal((4, 3000)) * 0.05).astype(np.float32)
+    q, s = O.pack_w8(W)
+    dec = q * np.repeat(s, 1024, axis=1)[:, :3000]
+    lim = np.repeat(s, 1024, axis=1)[:, :3000] * 0.5 * (1 + 2.0 ** -22)
+    assert np.all(np.abs(W.astype(np.float64) - dec) <= lim)
