@@ -35,6 +35,10 @@ Sources (page title, section)
   every tile to full precision and runs a plain matmul.  "The bugs that were
   the work": the ids of MUL_MAT_ID are a strided view, and down-projection
   experts read a per-slot src1 column i + t*n_expert_used.
+* NPU engine: full ELFs, no xclbin -- "Q4NX chunks": Q4_K weights are
+  repacked into q4_1 exactly apart from rounding S*scale and M*min to bf16;
+  Q8 tiles store code (r, k) at byte k*32 + r or at
+  (r/16)*4096 + (k/32)*512 + (k%32)*16 + r%16.
 
 Readings where the pages are silent
 -----------------------------------
@@ -48,6 +52,9 @@ These are the repository's own choices, and the design notes list them.
   q = clamp(rint_even(R(R(x-m)/s)), 0, 15), and q = 0 when s == 0.
 * The intra-tile byte map is defined below in ``Q4 TILE FORMAT``.  The pages
   do not print the byte layout of a tile.
+* Q4_K bytes follow GGML's published super-block layout (the pages name the
+  type only).  Q8 tiles add one bf16 scale per (row, 32 columns) after the
+  8192 code bytes, and quantise with s = bf16(amax/127) and packB's rounding.
 """
 from __future__ import annotations
 
@@ -485,3 +492,165 @@ def w8_gemm(codes, scales, X):
         Y += (X[:, sl] @ codes[:, sl].T) * scales[:, b][None, :]
         norm += (np.abs(X[:, sl]) @ np.abs(codes[:, sl]).T) * scales[:, b][None, :]
     return Y, norm
+
+
+# ----------------------------------------------------------------------------
+# More weight formats ("NPU engine: full ELFs, no xclbin", section "Q4NX
+# chunks"): Q4_K repacked into q4_1 tiles, and 8-bit (Q8) tiles in the two
+# code layouts that the section describes.
+# ----------------------------------------------------------------------------
+#
+# Q4_K -> q4_1.  The section says the repack keeps the 4-bit codes and is exact
+# apart from rounding S*scale and M*min to bf16.  The pages name Q4_K but do
+# not print its bytes; the layout read here is GGML's published k-quant
+# super-block (it must match the files the weights come from).  Per 256
+# consecutive weights of one row, 144 bytes:
+#   [0, 2)    d, fp16 (the super-block scale S of the 6-bit scale codes)
+#   [2, 4)    dmin, fp16 (the super-block scale M of the 6-bit min codes)
+#   [4, 16)   twelve bytes b[0..11] holding eight 6-bit scale codes sc_j and
+#             eight 6-bit min codes mn_j, one pair per sub-block j of 32:
+#               j < 4:  sc_j = b[j] & 63,   mn_j = b[j+4] & 63
+#               j >= 4: sc_j = (b[j+4] & 15) | ((b[j-4] >> 6) << 4)
+#                       mn_j = (b[j+4] >> 4) | ((b[j] >> 6) << 4)
+#   [16, 144) 128 code bytes: weight 64c + l (c = 0..3, l = 0..31) is the low
+#             nibble of byte 32c + l, weight 64c + 32 + l its high nibble.
+#   Weight of sub-block j: w = d*sc_j*q - dmin*mn_j.
+# The q4_1 block of sub-block j then has scale bf16(d*sc_j), min
+# bf16(-(dmin*mn_j)) and the same codes.  Both products are exact in fp32 (an
+# 11-bit significand times a 6-bit integer), so each is rounded once.
+
+Q4K_SB, Q4K_BYTES = 256, 144
+
+
+def q4k_fields(buf, N: int, K: int, row_bytes: int | None = None):
+    """Parse Q4_K super-blocks of an N x K weight (rows of K/256 blocks,
+    ``row_bytes`` apart; default contiguous).  Returns
+    (d [N][K/256], dmin, sc [N][K/256][8], mn [N][K/256][8], q [N][K]),
+    d and dmin as fp64, the codes as int64."""
+    assert K % Q4K_SB == 0
+    nsb = K // Q4K_SB
+    if row_bytes is None:
+        row_bytes = nsb * Q4K_BYTES
+    raw = np.asarray(buf, dtype=np.uint8).reshape(-1)
+    blk = np.stack([raw[n * row_bytes:n * row_bytes + nsb * Q4K_BYTES] for n in range(N)])
+    blk = blk.reshape(N, nsb, Q4K_BYTES)
+    d = blk[:, :, 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    dmin = blk[:, :, 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+    b = blk[:, :, 4:16].astype(np.int64)
+    sc = np.zeros((N, nsb, 8), dtype=np.int64)
+    mn = np.zeros((N, nsb, 8), dtype=np.int64)
+    for j in range(8):
+        if j < 4:
+            sc[..., j] = b[..., j] & 63
+            mn[..., j] = b[..., j + 4] & 63
+        else:
+            sc[..., j] = (b[..., j + 4] & 15) | ((b[..., j - 4] >> 6) << 4)
+            mn[..., j] = (b[..., j + 4] >> 4) | ((b[..., j] >> 6) << 4)
+    qs = blk[:, :, 16:].astype(np.int64).reshape(N, nsb, 4, 32)   # n, sb, c, l
+    q = np.stack([qs & 15, qs >> 4], axis=3)                      # n, sb, c, half, l
+    return d, dmin, sc, mn, q.reshape(N, K)
+
+
+def q4k_decode(buf, N: int, K: int, row_bytes: int | None = None):
+    """Dense fp64 weights of a Q4_K tensor: w = d*sc_j*q - dmin*mn_j."""
+    d, dmin, sc, mn, q = q4k_fields(buf, N, K, row_bytes)
+    scale = (d[:, :, None] * sc).reshape(N, K // BLOCK)
+    mins = (dmin[:, :, None] * mn).reshape(N, K // BLOCK)
+    return q * np.repeat(scale, BLOCK, axis=1) - np.repeat(mins, BLOCK, axis=1)
+
+
+def repack_q4k(buf, N: int, K: int, row_bytes: int | None = None):
+    """Q4_K -> q4_1 tile bytes: scale bf16(d*sc), min bf16(-(dmin*mn)), same codes."""
+    d, dmin, sc, mn, q = q4k_fields(buf, N, K, row_bytes)
+    s = bf16_rne(_f32((d[:, :, None] * sc).reshape(N, K // BLOCK)))
+    m = bf16_rne(_f32(-(dmin[:, :, None] * mn).reshape(N, K // BLOCK)))
+    return q4_tiles_from_blocks(q, s, m)
+
+
+# Q8 tiles.  The section gives the two code layouts of a 32 x 256 tile:
+#   layout 0: code (r, k) at byte k*32 + r;
+#   layout 1: code (r, k) at byte (r/16)*4096 + (k/32)*512 + (k%32)*16 + r%16.
+# It gives no scale bytes ("npu/q4nx.h has the byte layouts"), so these are
+# the library's own: each tile is 8704 bytes, the 8192 code bytes followed by
+# one bf16 scale per (row r, block g of 32 columns) at byte
+# 8192 + 2*(32 g + r); codes are int8 and w = code * scale (Q8 does not fit
+# q4_1's code + min form).  Tiles are row-major over the [N/32][K/256] grid,
+# as for q4.  Quantiser (the pages give none; packB's rule per block with the
+# scale kept in bf16):
+#   s = bf16(fl(amax / 127)); q = clamp(rint_even(fl(x / s)), -127, 127);
+#   q = 0 where s == 0.
+
+Q8_TILE_BYTES, Q8_CODE_BYTES = 8704, 8192
+
+
+def q8_code_offsets(layout: int):
+    """Byte offset of code (r, k) in a tile, as an int64 array [32][256]."""
+    r = np.arange(TILE_ROWS, dtype=np.int64)[:, None]
+    k = np.arange(TILE_COLS, dtype=np.int64)[None, :]
+    if layout == 0:
+        return k * 32 + r
+    if layout == 1:
+        return (r // 16) * 4096 + (k // 32) * 512 + (k % 32) * 16 + r % 16
+    raise ValueError("Q8 layout is 0 or 1")
+
+
+def q8_quantize_blocks(W):
+    """fp32 W [N][K] -> (q int64 [N][K], scale fp64 bf16 values [N][K/32])."""
+    W = _f32(np.asarray(W, np.float64))
+    N, K = W.shape
+    assert K % BLOCK == 0
+    Wb = W.reshape(N, K // BLOCK, BLOCK)
+    s = bf16_rne(_f32(np.abs(Wb).max(axis=2) / 127.0))
+    nz = s > 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = _f32(Wb / np.where(nz, s, 1.0)[:, :, None])
+    q = np.where(nz[:, :, None], np.clip(np.rint(u), -127, 127), 0).astype(np.int64)
+    return q.reshape(N, K), s
+
+
+def q8_tiles_from_blocks(q, s, layout: int):
+    q = np.asarray(q, np.int64)
+    N, K = q.shape
+    assert N % TILE_ROWS == 0 and K % TILE_COLS == 0
+    assert q.min(initial=0) >= -128 and q.max(initial=0) <= 127
+    TR, TC = N // TILE_ROWS, K // TILE_COLS
+    off = q8_code_offsets(layout)
+    out = np.zeros((TR, TC, Q8_TILE_BYTES), dtype=np.uint8)
+    qt = q.reshape(TR, TILE_ROWS, TC, TILE_COLS).transpose(0, 2, 1, 3)   # tr tc r k
+    codes = np.zeros((TR, TC, Q8_CODE_BYTES), dtype=np.uint8)
+    codes[:, :, off] = (qt & 0xFF).astype(np.uint8)
+    out[:, :, :Q8_CODE_BYTES] = codes
+    sb = bf16_bits(s).reshape(TR, TILE_ROWS, TC, 8).transpose(0, 2, 3, 1)   # tr tc g r
+    out[:, :, Q8_CODE_BYTES:] = sb.reshape(TR, TC, 256).astype(np.uint16).view(np.uint8).reshape(TR, TC, 512)
+    return out.reshape(-1)
+
+
+def pack_q8(W, layout: int):
+    """fp32 W [N][K] -> Q8 tile bytes in the given code layout."""
+    q, s = q8_quantize_blocks(W)
+    return q8_tiles_from_blocks(q, s, layout)
+
+
+def q8_blocks_from_tiles(tiles, N: int, K: int, layout: int):
+    """Tile bytes -> (q int64 [N][K], scale fp64 [N][K/32])."""
+    TR, TC = N // TILE_ROWS, K // TILE_COLS
+    t = np.asarray(tiles, dtype=np.uint8).reshape(TR, TC, Q8_TILE_BYTES)
+    off = q8_code_offsets(layout)
+    q = t[:, :, :Q8_CODE_BYTES][:, :, off].view(np.int8).astype(np.int64)   # tr tc r k
+    q = q.transpose(0, 2, 1, 3).reshape(N, K)
+    sb = t[:, :, Q8_CODE_BYTES:].copy().view(np.uint16).reshape(TR, TC, 8, TILE_ROWS)   # tr tc g r
+    s = bf16_from_bits(sb).transpose(0, 3, 1, 2).reshape(N, K // BLOCK)
+    return q, s
+
+
+def q8_decode(tiles, N: int, K: int, layout: int):
+    """Dense fp64 weights w = code * scale."""
+    q, s = q8_blocks_from_tiles(tiles, N, K, layout)
+    return q.astype(np.float64) * np.repeat(s, BLOCK, axis=1)
+
+
+def q8_gemm(tiles, N: int, K: int, X, layout: int):
+    """y[m][n] = sum_k x[m][k] w[n][k] in fp64, plus the normaliser sum_k |x||w|."""
+    W = q8_decode(tiles, N, K, layout)
+    X = np.asarray(X, np.float64)
+    return X @ W.T, np.abs(X) @ np.abs(W).T

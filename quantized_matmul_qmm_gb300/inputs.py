@@ -176,3 +176,22 @@ def moe_case(kind: str, seed: int = 10, n_expert: int = 128, n_used: int = 8, T:
     W = torch.randn((n_expert, N, K), generator=gw, dtype=torch.float32) * 0.02
     return MoECase(f"moe_{kind}_e{n_expert}_top{n_used}_t{T}", n_expert, n_used, T, K, N, shared,
                    W, X, ids_buf, ld_ids)
+
+
+def q4k_superblocks(seed: int, N: int, K: int, d_range=(1e-4, 2e-3), dmin_range=(1e-4, 2e-3)) -> torch.Tensor:
+    """Random Q4_K super-blocks for an N x K weight: uint8 [N][K/256 * 144].
+
+    Each 144-byte block holds two fp16 values drawn uniformly from the given
+    ranges at bytes 0..3, then 140 uniformly random bytes (the twelve bytes of
+    6-bit scale and min codes and the 128 bytes of 4-bit codes), so every
+    scale, min and code value occurs.  Weights of N(0, 0.02) quantised to Q4_K
+    have super-block scales in about this range."""
+    assert K % 256 == 0
+    g = _gen(seed)
+    nsb = K // 256
+    blk = _randint(g, 0, 255, (N, nsb, 144), torch.uint8)
+    d = _uniform(g, d_range[0], d_range[1], (N, nsb)).to(torch.float16)
+    dmin = _uniform(g, dmin_range[0], dmin_range[1], (N, nsb)).to(torch.float16)
+    blk[:, :, 0:2] = d.view(torch.uint8).reshape(N, nsb, 2)
+    blk[:, :, 2:4] = dmin.view(torch.uint8).reshape(N, nsb, 2)
+    return blk.reshape(N, nsb * 144).contiguous()
