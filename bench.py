@@ -209,8 +209,8 @@ class HotPath:
         return 2 if self.q.int8_gemm_workspace_size(c.M, c.K, c.N) > 0 else 1
 
     def moe_launches(self, m):
-        # route-and-pack, then the grouped kernel
-        return 2
+        # routing grid, packing grid, then the grouped kernel
+        return 3
 
     def q4_launches(self, M):
         return 1
@@ -320,6 +320,9 @@ def run_ours(args, rank, world, dev):
     if int(hp.status.item()) != 0:
         raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
     streams["w8"] = run_w8(q, I, args, dev, stream, hp.status, flush_l2)
+    if int(hp.status.item()) != 0:
+        raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
+    streams["q8"] = run_q8(q, I, args, dev, stream, hp.status, flush_l2)
     if int(hp.status.item()) != 0:
         raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
     return hp, per_call, total, clk, e2e_ms, streams
@@ -467,6 +470,67 @@ def run_w8(q, I, args, dev, stream, status, flush_l2):
     return res
 
 
+def run_q8(q, I, args, dev, stream, status, flush_l2):
+    """Q8 tiles (the two 8-bit code layouts of the Q4NX chunk format), timed
+    apart from the step like the W8A16 path:
+      * lm_head M=1 decode GEMV in each layout, back-to-back launches over
+        rotating copies of the tiles totalling >= 4x the L2 size;
+      * lm_head M=512 through the tensor-core route (tiles decoded to bf16,
+        then the pair GEMM), one call after an L2 flush.
+    Medians over `args.steps` timed repetitions after `args.warmup`."""
+    import math
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def timed(fn, flush):
+        out = []
+        for i in range(args.warmup + args.steps):
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
+            if flush:
+                flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= args.warmup:
+                out.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) * 1e3 for a, b in out)
+
+    res = {}
+    name, K, N = I.QWEN3_06B_LM_HEAD
+    W = I.q4_weights(9 * 1000 + N % 997 + K, N, K).to(dev)
+    x1 = I.q4_activations(9 * 7919 + 1, 1, K).to(dev)
+    y1 = torch.empty((1, N), dtype=torch.float32, device=dev)
+    for layout in (q.QMM_Q8_LAYOUT_KR, q.QMM_Q8_LAYOUT_SLAB16):
+        tiles = q.pack_q8(W, layout)
+        wbytes = tiles.numel()
+        R = max(2, math.ceil(4 * l2 / wbytes))
+        copies = [tiles] + [tiles.clone() for _ in range(R - 1)]
+
+        def lm_pass():
+            for t in copies:
+                q.q8_gemm(t, layout, N, K, x1, Y=y1, dev_status=status)
+
+        us = timed(lm_pass, False) / R
+        res[f"q8_gemv_lm_head_m1_layout{layout}_stream"] = {
+            "us": us, "copies": R, "launches": 1, "weight_bytes": wbytes,
+            "weight_GBs": wbytes / (us * 1e-6) / 1e9, "GBs": (wbytes + 2 * K + 4 * N) / (us * 1e-6) / 1e9}
+        del copies
+        if layout == q.QMM_Q8_LAYOUT_KR:
+            x512 = I.q4_activations(9 * 7919 + 512, 512, K).to(dev)
+            y512 = torch.empty((512, N), dtype=torch.float32, device=dev)
+            ws = torch.empty(q.q8_gemm_workspace_size(512, K, N), dtype=torch.uint8, device=dev)
+            us = timed(lambda: q.q8_gemm(tiles, layout, N, K, x512, Y=y512, workspace=ws, dev_status=status), True)
+            res["q8_gemm_lm_head_m512"] = {"us": us, "launches": 2,
+                                           "TFLOPS": 2 * 512 * N * K / (us * 1e-6) / 1e12, "weight_bytes": wbytes}
+            del x512, y512, ws
+        del tiles
+    del W
+    torch.cuda.synchronize()
+    return res
+
+
 def cpu_int8_sample(rows: int):
     """The oracle (as it stands) on `rows` rows of the M=4096 K=N=4608 GEMM."""
     import numpy as np
@@ -578,6 +642,14 @@ def main():
         d = w8[name]
         rooflines[name] = {"bound": "tensor", "achieved": d["TFLOPS"], "peak": tensor_peak, "unit": "TFLOP/s",
                            "frac": d["TFLOPS"] / tensor_peak, "traffic": traffic.get(name)}
+    q8 = streams["q8"]
+    for name, d in q8.items():
+        if "gemv" in name:
+            rooflines[name] = {"bound": "hbm", "achieved": d["GBs"], "peak": hbm_peak, "unit": "GB/s",
+                               "frac": d["GBs"] / hbm_peak, "traffic": traffic.get(name)}
+        else:
+            rooflines[name] = {"bound": "tensor", "achieved": d["TFLOPS"], "peak": tensor_peak, "unit": "TFLOP/s",
+                               "frac": d["TFLOPS"] / tensor_peak, "traffic": traffic.get(name)}
     c = hp.int8
     launches = sum(l for (_, _, l, _) in hp.calls) * args.steps
     line = {
@@ -602,6 +674,9 @@ def main():
         "w8a16": {"note": "int8 weights with one fp32 scale per row and 1,024 weights, bf16 activations; "
                           "timed apart from the step (median, L2 flushed before each single call)",
                   **w8},
+        "q8": {"note": "8-bit tiles (bf16 scale per row and 32 columns) in the chunk format's two code layouts; "
+                       "timed apart from the step (median, L2 flushed before each single call)",
+               **q8},
         "e2e": {"value": world * 2.0 * c.M * c.N * c.K / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
                 "h2d_bytes_per_step": c.M * c.K, "d2h_bytes_per_step": c.M * c.N},
         "gpu_launches": launches,

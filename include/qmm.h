@@ -1,11 +1,15 @@
 /*
  * qmm.h -- C ABI of the quantized projection matmul library for one GB300 (sm_103a).
  *
- * Two halves:
- *   (I)  an exact int8 GEMM with zero-point correction, per-column weight
- *        scale, optional int32 bias and float or requantised output;
- *   (II) a 4-bit block-weight GEMM/GEMV over 32x256 tiles of q4_1 blocks and
- *        its MUL_MAT_ID (mixture-of-experts) variant.
+ * Two halves, and two widenings of the second:
+ *   (I)   an exact int8 GEMM with zero-point correction, per-column weight
+ *         scale, optional int32 bias and float or requantised output, and the
+ *         int8 quantisation of its activations;
+ *   (II)  a 4-bit block-weight GEMM/GEMV over 32x256 tiles of q4_1 blocks and
+ *         its MUL_MAT_ID (mixture-of-experts) variant;
+ *   (III) W8A16: int8 weights with block scales times bf16 activations;
+ *   (IV)  more weight formats: Q4_K repacked into q4_1 tiles, and 8-bit (Q8)
+ *         tiles in two code layouts.
  *
  * Conventions shared by every entry point
  * ----------------------------------------
@@ -343,6 +347,85 @@ qmm_status qmm_w8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* w
  * QMM_ERR_UNSUPPORTED for K > 65536.
  */
 qmm_status qmm_w8_gemm(const void* codes, const float* scales, int64_t N, int64_t K, const void* X, int64_t M,
+                       int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                       cudaStream_t stream);
+
+/* ========================================================================
+ * (IV) More weight formats
+ *
+ * "NPU engine: full ELFs, no xclbin", section "Q4NX chunks":
+ *   - Q4_K weights are repacked into q4_1 tiles, exactly apart from rounding
+ *     S*scale and M*min to bf16, so the 4-bit kernels above run them unchanged;
+ *   - Q8 weights use the same 32 x 256 tile grid with 8-bit codes in one of
+ *     two layouts: code (row r, column k) at byte k*32 + r, or at
+ *     (r/16)*4096 + (k/32)*512 + (k%32)*16 + r%16.
+ * ======================================================================== */
+
+/* Repack Q4_K super-blocks into q4_1 tiles (the format of qmm_pack_q4).
+ *
+ * q4k       N rows of K/256 super-blocks (GGML's k-quant layout, 144 bytes per
+ *           256 weights of a row: fp16 d, fp16 dmin, twelve bytes of 6-bit
+ *           scale/min codes, 128 bytes of 4-bit codes; w = d*sc*q - dmin*mn).
+ *           Row n starts at byte n*row_bytes; row_bytes >= (K/256)*144 and a
+ *           multiple of 16, base 16-byte aligned.
+ * tiles     out, qmm_pack_q4_size(N, K) bytes, 16-byte aligned.
+ * Each 32-weight sub-block keeps its codes and gets scale bf16(d*sc) and min
+ * bf16(-(dmin*mn)), rounded to nearest even from the exact fp32 products, so
+ * every decoded weight is within 2^-8 (q|d*sc| + |dmin*mn|) of the Q4_K one.
+ * Errors: QMM_ERR_INVALID_ARG for null or misaligned pointers, a short row
+ * stride or tile buffer, N < 1 or K < 1; QMM_ERR_UNSUPPORTED unless N % 32 == 0
+ * and K % 256 == 0.
+ */
+qmm_status qmm_repack_q4k(const void* q4k, int64_t N, int64_t K, int64_t row_bytes, void* tiles,
+                          size_t tile_bytes, cudaStream_t stream);
+
+/* Q8 code layouts (the two of "Q4NX chunks"). */
+typedef enum {
+  QMM_Q8_LAYOUT_KR = 0,     /* code (r, k) at byte k*32 + r */
+  QMM_Q8_LAYOUT_SLAB16 = 1  /* code (r, k) at byte (r/16)*4096 + (k/32)*512 + (k%32)*16 + r%16 */
+} qmm_q8_layout;
+
+/* Q8 tile bytes of an N x K weight: (N/32) * (K/256) * 8704.  Each tile holds
+ * the 8192 code bytes (int8, in the chosen layout) followed by this library's
+ * scale bytes, which the pages do not give: one bf16 scale per (row r, block
+ * g of 32 columns) at byte 8192 + 2*(32 g + r).  w = code * scale. */
+qmm_status qmm_pack_q8_size(int64_t N, int64_t K, size_t* tile_bytes);
+
+/* Quantise fp32 W [N][K] (row stride ldw elements, ldw >= K, W finite) into
+ * Q8 tiles.  Per block of 32 consecutive k of one row (IEEE fp32 steps):
+ *   s = bf16_rne(amax / 127); q = clamp(rint_even(W / s), -127, 127), 0 where s == 0.
+ * Requires N % 32 == 0 and K % 256 == 0 (else QMM_ERR_UNSUPPORTED); tiles
+ * 16-byte aligned with tile_bytes >= qmm_pack_q8_size; QMM_ERR_INVALID_ARG for
+ * a bad layout or pointer.
+ */
+qmm_status qmm_pack_q8(const float* W, int64_t N, int64_t K, int64_t ldw, qmm_q8_layout layout, void* tiles,
+                       size_t tile_bytes, cudaStream_t stream);
+
+/* Workspace of qmm_q8_gemm: 0 for M <= 16, else N*K*2 bytes of bf16 weights
+ * plus N*ceil(K/1024)*4 bytes, each rounded up to 256. */
+qmm_status qmm_q8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes);
+
+/* Y[m][n] = sum_k X[m][k] * w[n][k] over Q8 tiles, fp32 accumulation.
+ *
+ * tiles  from qmm_pack_q8 (or any Q8 tile set) in the given layout, 16-byte
+ *        aligned; N % 32 == 0, K % 256 == 0.
+ * X      bf16 [M][K], row stride ldx elements (ldx >= K, ldx % 8 == 0, base
+ *        16-byte aligned).
+ * Y      fp32 [M][N], row stride ldy elements (ldy >= N), 4-byte aligned.
+ * workspace / ws_bytes  qmm_q8_gemm_workspace_size bytes, 256-byte aligned
+ *        (NULL when that size is 0), rewritten by the call.
+ * M <= 16 runs the decode GEMV, which forms every weight exactly
+ * (code * scale in fp32): max |y - y_exact| <= 2e-5 * sum_k |x||w| at the
+ * supported K.  Larger M decodes the tiles to bf16 weights (one rounding,
+ * <= 2^-8 relative per weight) for the tensor-core GEMM, within the 4-bit
+ * path's bound max |y - y_exact| <= 2e-3 * sum_k |x||w| for inputs whose
+ * rounding errors do not all share one sign.
+ * Errors: QMM_ERR_INVALID_ARG for null or misaligned pointers, bad sizes,
+ * strides or layout; QMM_ERR_WORKSPACE; QMM_ERR_UNSUPPORTED for N % 32 != 0,
+ * K % 256 != 0, or K > 65536 when M > 16.  Device status: QMM_ERR_TIMEOUT
+ * (M > 16 only).
+ */
+qmm_status qmm_q8_gemm(const void* tiles, qmm_q8_layout layout, int64_t N, int64_t K, const void* X, int64_t M,
                        int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes, int32_t* dev_status,
                        cudaStream_t stream);
 

@@ -310,4 +310,67 @@ qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_
   return cuda_status(launch_q4_moe(a, stream));
 }
 
+// ---------------------------------------------------------------------------
+// More weight formats: Q4_K repack, Q8 tiles
+// ---------------------------------------------------------------------------
+
+qmm_status qmm_repack_q4k(const void* q4k, int64_t N, int64_t K, int64_t row_bytes, void* tiles,
+                          size_t tile_bytes, cudaStream_t stream) {
+  if (q4k == nullptr || tiles == nullptr || N < 1 || K < 1) return QMM_ERR_INVALID_ARG;
+  if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+  if (N > INT32_MAX || K > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  if (row_bytes < (K / kTileCols) * 144 || row_bytes % 16 != 0) return QMM_ERR_INVALID_ARG;
+  if (!aligned(q4k, 16) || !aligned(tiles, 16)) return QMM_ERR_INVALID_ARG;
+  if (tile_bytes < (size_t)((N / kTileRows) * (K / kTileCols) * kTileBytes)) return QMM_ERR_INVALID_ARG;
+  if ((N * (K / kTileCols) + 255) / 256 > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  return cuda_status(launch_repack_q4k(static_cast<const uint8_t*>(q4k), row_bytes, (int)N, (int)K,
+                                       static_cast<uint8_t*>(tiles), stream));
+}
+
+qmm_status qmm_pack_q8_size(int64_t N, int64_t K, size_t* tile_bytes) {
+  if (tile_bytes == nullptr || N < 1 || K < 1) return QMM_ERR_INVALID_ARG;
+  if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+  *tile_bytes = (size_t)((N / kTileRows) * (K / kTileCols)) * kQ8TileBytes;
+  return QMM_OK;
+}
+
+qmm_status qmm_pack_q8(const float* W, int64_t N, int64_t K, int64_t ldw, qmm_q8_layout layout, void* tiles,
+                       size_t tile_bytes, cudaStream_t stream) {
+  if (W == nullptr || tiles == nullptr || N < 1 || K < 1 || ldw < K) return QMM_ERR_INVALID_ARG;
+  if (layout != QMM_Q8_LAYOUT_KR && layout != QMM_Q8_LAYOUT_SLAB16) return QMM_ERR_INVALID_ARG;
+  if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+  if (N > INT32_MAX || K > INT32_MAX || (N / kTileRows) * (K / kTileCols) > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  if (!aligned(W, 4) || !aligned(tiles, 16)) return QMM_ERR_INVALID_ARG;
+  if (tile_bytes < (size_t)((N / kTileRows) * (K / kTileCols)) * kQ8TileBytes) return QMM_ERR_INVALID_ARG;
+  return cuda_status(launch_pack_q8(W, ldw, (int)N, (int)K, (int)layout, static_cast<uint8_t*>(tiles), stream));
+}
+
+qmm_status qmm_q8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes) {
+  if (ws_bytes == nullptr || M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+  if (M > kQ8GemvMaxM && K > kQ8MaxK) return QMM_ERR_UNSUPPORTED;
+  *ws_bytes = M <= kQ8GemvMaxM ? 0 : q8_gemm_workspace_bytes(N, K);
+  return QMM_OK;
+}
+
+qmm_status qmm_q8_gemm(const void* tiles, qmm_q8_layout layout, int64_t N, int64_t K, const void* X, int64_t M,
+                       int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                       cudaStream_t stream) {
+  if (tiles == nullptr || X == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
+  if (N < 1 || K < 1 || M < 1 || ldx < K || ldy < N) return QMM_ERR_INVALID_ARG;
+  if (layout != QMM_Q8_LAYOUT_KR && layout != QMM_Q8_LAYOUT_SLAB16) return QMM_ERR_INVALID_ARG;
+  if (ldx % 8 != 0 || !aligned(X, 16) || !aligned(tiles, 16) || !aligned(Y, 4)) return QMM_ERR_INVALID_ARG;
+  if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  if (M > kQ8GemvMaxM) {
+    if (K > kQ8MaxK || (N + 255) / 256 > 65535 || (N / kTileRows) * (K / kTileCols) > INT32_MAX)
+      return QMM_ERR_UNSUPPORTED;
+    if (workspace == nullptr || ws_bytes < q8_gemm_workspace_bytes(N, K) || !aligned(workspace, 256))
+      return QMM_ERR_WORKSPACE;
+  }
+  return cuda_status(launch_q8_gemm(static_cast<const uint8_t*>(tiles), (int)layout, (int)N, (int)K,
+                                    static_cast<const __nv_bfloat16*>(X), ldx, (int)M, Y, ldy, workspace, dev_status,
+                                    stream));
+}
+
 }  // extern "C"

@@ -45,6 +45,7 @@ constexpr int kBK = 64;              // K per stage (one 128-byte swizzle row of
 constexpr int kStages = 6;
 constexpr int kChunkK = 1024;        // K per exact fp32 chunk
 constexpr int kChunkKB = kChunkK / kBK;
+static_assert(kChunkK == kPairChunkK, "the W8A16 chunk scales assume 1,024-k chunks");
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBNh * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -745,11 +746,27 @@ cudaError_t launch_w8_gemm_umma(const int8_t* codes, const float* scales, int N,
   const int wgrid = std::min(ngroups, 2 * pairs * per_sm);
   int8_widen_kernel<<<wgrid, kWidenThreads, wsmem, stream>>>(wp);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  return launch_bf16w_gemm_umma(B16, scales, (K + kChunkK - 1) / kChunkK, N, K, X, ldx, M, Y, ldy, dev_status,
+                                stream);
+}
 
+// The GEMM half of the above on bf16 weights B16 [N][Kp] (Kp = K rounded up
+// to 64, zero columns past K) that an earlier launch in the stream wrote:
+// Y = sum over 1,024-k chunks c of scales[n][c] * (X B16^T restricted to c).
+// Launched as a programmatic dependent; the kernel waits for the previous
+// grid before it reads B16.
+cudaError_t launch_bf16w_gemm_umma(const __nv_bfloat16* B16, const float* scales, int nb, int N, int K,
+                                   const __nv_bfloat16* X, int64_t ldx, int M, float* Y, int64_t ldy,
+                                   int32_t* dev_status, cudaStream_t stream) {
+  const int Kp = (int)padded_k(K);
+  int pairs = 0;
+  cudaError_t err = resident_pairs(&pairs);
+  if (err != cudaSuccess) return err;
   CUtensorMap tmA, tmB;
   if (!make_tmap_2d(&tmA, true, const_cast<__nv_bfloat16*>(X), (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2, kBK,
                     kBM) ||
-      !make_tmap_2d(&tmB, true, B16, (uint64_t)Kp, (uint64_t)N, (uint64_t)Kp * 2, kBK, kBNh))
+      !make_tmap_2d(&tmB, true, const_cast<__nv_bfloat16*>(B16), (uint64_t)Kp, (uint64_t)N, (uint64_t)Kp * 2, kBK,
+                    kBNh))
     return cudaErrorInvalidValue;
   Int8UmmaParams p{};
   p.M = M;
@@ -762,7 +779,7 @@ cudaError_t launch_w8_gemm_umma(const int8_t* codes, const float* scales, int N,
   p.epi.ldo = ldy;
   p.dev_status = dev_status;
   p.w8_scales = scales;
-  p.w8_nb = (K + kChunkK - 1) / kChunkK;
+  p.w8_nb = nb;
   if (pairs > p.ntiles) pairs = p.ntiles;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
@@ -771,7 +788,7 @@ cudaError_t launch_w8_gemm_umma(const int8_t* codes, const float* scales, int N,
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;   // overlap the widen grid
+  attr[0].val.programmaticStreamSerializationAllowed = 1;   // overlap the grid that wrote B16
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kUmmaKernels[kW8Kernel], tmA, tmB, p);

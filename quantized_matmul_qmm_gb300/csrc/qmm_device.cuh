@@ -40,6 +40,38 @@ QMM_DEV uint32_t ldg32(const void* p) {
   return r;
 }
 
+// Two fp32 lanes in one 64-bit register, for the packed f32x2 arithmetic of
+// sm_100+ (each lane rounds exactly as the scalar instruction would).
+QMM_DEV uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+QMM_DEV void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+QMM_DEV uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+QMM_DEV uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+QMM_DEV uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// int8 byte i of word xw (already XORed with 0x80808080) as fp32: the byte
+// becomes the low mantissa byte of 2^23, and 2^23 + 128 is subtracted (exact).
+QMM_DEV float s8_byte_to_f32(uint32_t xw, int i) {
+  return __uint_as_float(__byte_perm(xw, 0x4B000000u, 0x7540u + (uint32_t)i)) - 8388736.0f;
+}
+
 QMM_DEV uint32_t u4_get(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }

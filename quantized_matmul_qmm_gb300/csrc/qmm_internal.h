@@ -92,6 +92,26 @@ size_t w8_umma_workspace_bytes(int64_t K, int64_t N);
 cudaError_t launch_w8_gemm_umma(const int8_t* codes, const float* scales, int N, int K,
                                 const __nv_bfloat16* X, int64_t ldx, int M, float* Y, int64_t ldy,
                                 void* workspace, int32_t* dev_status, cudaStream_t stream);
+// The pair GEMM alone, on bf16 weights B16 [N][padded_k(K)] that an earlier
+// launch in the stream wrote; scales [N][nb] multiply each kPairChunkK-column
+// chunk of the accumulator.
+constexpr int kPairChunkK = 1024;
+cudaError_t launch_bf16w_gemm_umma(const __nv_bfloat16* B16, const float* scales, int nb, int N, int K,
+                                   const __nv_bfloat16* X, int64_t ldx, int M, float* Y, int64_t ldy,
+                                   int32_t* dev_status, cudaStream_t stream);
+
+// ---- more weight formats (formats.cu): Q4_K -> q4_1 repack, Q8 tiles ----
+constexpr int kQ8TileBytes = 8704;   // 8192 code bytes + 256 bf16 scales
+constexpr int kQ8CodeBytes = 8192;
+constexpr int64_t kQ8GemvMaxM = 16;
+constexpr int64_t kQ8MaxK = 65536;
+cudaError_t launch_repack_q4k(const uint8_t* src, int64_t row_bytes, int N, int K, uint8_t* tiles,
+                              cudaStream_t stream);
+cudaError_t launch_pack_q8(const float* W, int64_t ldw, int N, int K, int layout, uint8_t* tiles,
+                           cudaStream_t stream);
+size_t q8_gemm_workspace_bytes(int64_t N, int64_t K);   // the M > kQ8GemvMaxM route
+cudaError_t launch_q8_gemm(const uint8_t* tiles, int layout, int N, int K, const __nv_bfloat16* X, int64_t ldx,
+                           int M, float* Y, int64_t ldy, void* workspace, int32_t* dev_status, cudaStream_t stream);
 
 // ---- q4 kernels (q4_mma.cu, q4_umma.cu) ----
 struct Q4DenseArgs {

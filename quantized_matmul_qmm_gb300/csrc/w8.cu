@@ -10,8 +10,10 @@
 //
 // Decode GEMV (M <= 16): one warp per weight row at a time.  Each lane takes
 // 16 consecutive codes per step (512 bytes per warp load, four steps in
-// flight), converts them exactly, and multiplies them with x read through the
-// read-only cache.  Sixteen codes never straddle a 1,024 block, so each
+// flight), converts them exactly with a byte permute and one add (the
+// int-to-float unit runs at a quarter of the fma rate), and multiplies them
+// with x read through the read-only cache, even and odd columns as the two
+// lanes of packed f32x2 fmas.  Sixteen codes never straddle a 1,024 block, so each
 // group's partial sum is scaled by its own block's scale.
 #include <cuda_bf16.h>
 
@@ -58,12 +60,13 @@ pack_w8_kernel(const float* __restrict__ W, int64_t ldw, int K, int Kp, int8_t* 
 constexpr int kGvWarps = 8;
 constexpr int kGvSteps = 4;   // 16-byte code groups in flight per lane
 
+// 16 int8 codes as fp32 (exact), without the int-to-float unit.
 __device__ __forceinline__ void codes16_to_f32(const uint4 v, float (&c)[16]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) c[4 * i + j] = (float)(int8_t)(w[i] >> (8 * j));
+    for (int j = 0; j < 4; ++j) c[4 * i + j] = s8_byte_to_f32(w[i], j);
 }
 
 template <int kM>
@@ -105,11 +108,14 @@ w8_gemv_kernel(const int8_t* __restrict__ codes, const float* __restrict__ scale
             const uint4 x0 = __ldg(reinterpret_cast<const uint4*>(xr));
             const uint4 x1 = __ldg(reinterpret_cast<const uint4*>(xr) + 1);
             const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            // even and odd columns as the two lanes of packed f32x2 fmas
+            uint64_t pp = f2_mul(f2_pack(c[0], c[1]), f2_pack(bf16lo_to_f32(xw[0]), bf16hi_to_f32(xw[0])));
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              part = fmaf(c[2 * i], __uint_as_float(xw[i] << 16), part);
-              part = fmaf(c[2 * i + 1], __uint_as_float(xw[i] & 0xFFFF0000u), part);
-            }
+            for (int i = 1; i < 8; ++i)
+              pp = f2_fma(f2_pack(c[2 * i], c[2 * i + 1]), f2_pack(bf16lo_to_f32(xw[i]), bf16hi_to_f32(xw[i])), pp);
+            float pe, po;
+            f2_unpack(pp, pe, po);
+            part = pe + po;
           } else {
             for (int i = 0; k0 + i < K; ++i) part = fmaf(c[i], __bfloat162float(xr[i]), part);
           }

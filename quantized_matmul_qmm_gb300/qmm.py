@@ -56,7 +56,13 @@ SIGNATURES = {
     "qmm_pack_w8": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _sz, _vp, _sz, _vp]),
     "qmm_w8_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
     "qmm_w8_gemm": (_c.c_int, [_vp, _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_repack_q4k": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "qmm_pack_q8_size": (_c.c_int, [_i64, _i64, _szp]),
+    "qmm_pack_q8": (_c.c_int, [_vp, _i64, _i64, _i64, _c.c_int, _vp, _sz, _vp]),
+    "qmm_q8_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
+    "qmm_q8_gemm": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _vp]),
 }
+QMM_Q8_LAYOUT_KR, QMM_Q8_LAYOUT_SLAB16 = 0, 1
 
 
 class QmmError(RuntimeError):
@@ -282,5 +288,55 @@ def w8_gemm(codes: torch.Tensor, scales: torch.Tensor, N: int, K: int, X: torch.
             workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
     _check("qmm_w8_gemm", lib.qmm_w8_gemm(
         _ptr(codes), _ptr(scales), N, K, _ptr(X), M, X.stride(0), _ptr(Y), Y.stride(0), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
+    return Y
+
+
+# ---------------------------------------------------------------------------
+# More weight formats: Q4_K -> q4_1 tiles, Q8 tiles
+# ---------------------------------------------------------------------------
+
+def repack_q4k(q4k: torch.Tensor, N: int, K: int, tiles=None) -> torch.Tensor:
+    """q4k: device uint8 [N][row_bytes] of Q4_K super-blocks (row_bytes >= K/256*144).
+    Returns q4_1 tile bytes (uint8) for qmm_q4_gemm / qmm_q4_gemm_id."""
+    nbytes = pack_q4_size(N, K)
+    if tiles is None:
+        tiles = torch.empty(nbytes, dtype=torch.uint8, device=q4k.device)
+    row_bytes = q4k.stride(0) if q4k.dim() == 2 else K // 256 * 144
+    _check("qmm_repack_q4k", lib.qmm_repack_q4k(_ptr(q4k), N, K, row_bytes, _ptr(tiles),
+                                                tiles.numel(), _stream()))
+    return tiles
+
+
+def pack_q8_size(N: int, K: int) -> int:
+    return _size("qmm_pack_q8_size", N, K)
+
+
+def pack_q8(W: torch.Tensor, layout: int) -> torch.Tensor:
+    """W: device fp32 [N][K].  Returns Q8 tile bytes (uint8) in the given code layout."""
+    N, K = W.shape
+    nbytes = pack_q8_size(N, K)
+    tiles = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    _check("qmm_pack_q8", lib.qmm_pack_q8(_ptr(W), N, K, W.stride(0), int(layout), _ptr(tiles), nbytes,
+                                          _stream()))
+    return tiles
+
+
+def q8_gemm_workspace_size(M: int, K: int, N: int) -> int:
+    return _size("qmm_q8_gemm_workspace_size", M, K, N)
+
+
+def q8_gemm(tiles: torch.Tensor, layout: int, N: int, K: int, X: torch.Tensor, Y=None, workspace=None,
+            dev_status=None):
+    """Y[m][n] = sum_k X[m][k] w[n][k] over Q8 tiles; X bf16 [M][K] on the device."""
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        need = q8_gemm_workspace_size(M, K, N)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    _check("qmm_q8_gemm", lib.qmm_q8_gemm(
+        _ptr(tiles), int(layout), N, K, _ptr(X), M, X.stride(0), _ptr(Y), Y.stride(0), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
     return Y

@@ -153,3 +153,38 @@ def test_w8_sizes_and_host_validation(qmm):
     assert g(P, P, 64, 65544, P, 4, 65544, P, 64, None, 0, None, None) == qmm.QMM_ERR_UNSUPPORTED
     assert g(P, P, 64, 96, P, 17, 96, P, 64, None, 0, None, None) == qmm.QMM_ERR_WORKSPACE
     assert g(P, P, 64, 96, P, 17, 96, P, 64, P, 64 * 128 * 2 - 1, None, None) == qmm.QMM_ERR_WORKSPACE
+
+
+def test_format_sizes_and_host_validation(qmm):
+    # Q8 tiles: 8192 code bytes + 512 scale bytes per 32 x 256 tile
+    assert qmm.pack_q8_size(32, 256) == 8704
+    assert qmm.pack_q8_size(151936, 1024) == 4748 * 4 * 8704
+    assert qmm.q8_gemm_workspace_size(16, 1024, 64) == 0
+    assert qmm.q8_gemm_workspace_size(17, 1024, 64) == 64 * 1024 * 2 + 256
+    assert qmm.q8_gemm_workspace_size(17, 2048, 96) == 96 * 2048 * 2 + 768
+    L = qmm.lib
+    P = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: every call below fails on the host
+    sz = ctypes.c_size_t(0)
+    assert L.qmm_pack_q8_size(33, 256, ctypes.byref(sz)) == qmm.QMM_ERR_UNSUPPORTED
+    assert L.qmm_q8_gemm_workspace_size(17, 65792, 32, ctypes.byref(sz)) == qmm.QMM_ERR_UNSUPPORTED
+    # repack: off the tile grid, short row stride, row stride not a multiple of 16, short tiles, misaligned
+    rp = L.qmm_repack_q4k
+    assert rp(P, 33, 256, 144, P, 1 << 20, None) == qmm.QMM_ERR_UNSUPPORTED
+    assert rp(P, 32, 512, 272, P, 1 << 20, None) == qmm.QMM_ERR_INVALID_ARG
+    assert rp(P, 32, 256, 152, P, 1 << 20, None) == qmm.QMM_ERR_INVALID_ARG
+    assert rp(P, 32, 256, 144, P, 5119, None) == qmm.QMM_ERR_INVALID_ARG
+    assert rp(ctypes.c_void_p((1 << 20) + 8), 32, 256, 144, P, 5120, None) == qmm.QMM_ERR_INVALID_ARG
+    # pack_q8: bad layout, ldw < K, short tiles
+    pk = L.qmm_pack_q8
+    assert pk(P, 32, 256, 256, 2, P, 8704, None) == qmm.QMM_ERR_INVALID_ARG
+    assert pk(P, 32, 256, 255, 0, P, 8704, None) == qmm.QMM_ERR_INVALID_ARG
+    assert pk(P, 32, 256, 256, 1, P, 8703, None) == qmm.QMM_ERR_INVALID_ARG
+    g = L.qmm_q8_gemm
+    # bad layout, off the grid, ldx % 8, misaligned X, missing or short workspace (M > 16), K too large
+    assert g(P, 5, 32, 256, P, 1, 256, P, 32, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, 0, 48, 256, P, 1, 256, P, 48, None, 0, None, None) == qmm.QMM_ERR_UNSUPPORTED
+    assert g(P, 0, 32, 256, P, 1, 260, P, 32, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, 0, 32, 256, ctypes.c_void_p((1 << 20) + 2), 1, 256, P, 32, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, 1, 32, 256, P, 17, 256, P, 32, None, 0, None, None) == qmm.QMM_ERR_WORKSPACE
+    assert g(P, 1, 32, 256, P, 17, 256, P, 32, P, 32 * 256 * 2, None, None) == qmm.QMM_ERR_WORKSPACE
+    assert g(P, 1, 32, 65792, P, 17, 65792, P, 32, P, 1 << 30, None, None) == qmm.QMM_ERR_UNSUPPORTED
