@@ -152,6 +152,42 @@ def int8_gemm_y(A, a_type, zA, B, b_type, zB):
     return {"S": S, "rowSum": rowSum, "colSum": colSum, "Y": Y, "zAp": zAp, "zBp": zBp}
 
 
+def int8_gemm_y_axis(A, a_type, zA_rows, B, b_type, zB_cols):
+    """Per-axis zero points: one per activation row (zA_rows [M]) and one per
+    weight column (zB_cols [N]), each in its operand's own domain.
+
+    "The ONNX pack: weights to Q4NX, matmuls to our kernels, no VitisAI",
+    "What works today": the asymmetric corrections are per-tensor or per-axis
+    along the same axes as the scales (row zero points beside row scales,
+    column zero points beside column scales), exact in integers:
+
+        Y[m,n] = S - zA'[m] colSum[n] - zB'[n] (rowSum[m] - K zA'[m])
+
+    with the shifted zero points zA'[m] = zA[m] - 128 for uint8 A (B alike).
+    Asserts Y equals the direct definition sum_k (A[m,k] - zA[m])(B[k,n] - zB[n]).
+    """
+    Ap = shift(A, a_type)
+    Bp = shift(B, b_type)
+    M, K = Ap.shape
+    K2, N = Bp.shape
+    assert K == K2
+    zA = np.asarray(zA_rows, dtype=np.int64).reshape(M)
+    zB = np.asarray(zB_cols, dtype=np.int64).reshape(N)
+    lo_a, hi_a = (0, 255) if a_type == U8 else (-128, 127)
+    lo_b, hi_b = (0, 255) if b_type == U8 else (-128, 127)
+    assert zA.min(initial=lo_a) >= lo_a and zA.max(initial=hi_a) <= hi_a
+    assert zB.min(initial=lo_b) >= lo_b and zB.max(initial=hi_b) <= hi_b
+    zAp = zA - (128 if a_type == U8 else 0)
+    zBp = zB - (128 if b_type == U8 else 0)
+    S = Ap @ Bp
+    rowSum = Ap.sum(axis=1)
+    colSum = Bp.sum(axis=0)
+    Y = S - zAp[:, None] * colSum[None, :] - zBp[None, :] * (rowSum[:, None] - K * zAp[:, None])
+    Ydirect = (np.asarray(A, np.int64) - zA[:, None]) @ (np.asarray(B, np.int64) - zB[None, :])
+    assert np.array_equal(Y, Ydirect), "zero-point identity violated"
+    return {"S": S, "rowSum": rowSum, "colSum": colSum, "Y": Y, "zAp": zAp, "zBp": zBp}
+
+
 def int8_epilogue(Y, out_type: str, bias=None, s_x=None, s_w=None, s_y=1.0, zp_y=0):
     """Epilogue after the zero-point correction (int8 inference "Product kernel"
     and the ONNX pack page's fused QuantizeLinear).

@@ -268,3 +268,71 @@ def test_activation_quant_per_tensor():
     assert np.array_equal(q[np.argmax(sr)], qr[np.argmax(sr)])  # that row is coded as per row
     q1, s1 = O.quantize_activations_f32(X[2:3], per_row=False)
     assert np.array_equal(q1, qr[2:3]) and s1[0] == sr[2]       # one row: the two modes agree
+
+
+# --------------------------------------------------------------------------
+# per-axis zero points (ONNX pack page, "What works today": per-axis along the
+# same axes as the scales; the fully per-axis proof uses 8 row scales and zero
+# points and 6 column scales and zero points)
+# --------------------------------------------------------------------------
+
+def brute_y_axis(A, zA, B, zB):
+    M, K, N = len(A), len(A[0]), len(B[0])
+    return [[sum((int(A[m][k]) - int(zA[m])) * (int(B[k][n]) - int(zB[n])) for k in range(K)) for n in range(N)]
+            for m in range(M)]
+
+
+@pytest.mark.parametrize("a_type,b_type", list(itertools.product(["u8", "s8"], repeat=2)))
+def test_axis_zp_brute_force_tiny(a_type, b_type):
+    rng = np.random.default_rng(21)
+    for M, K, N in [(1, 1, 1), (2, 3, 4), (4, 4, 4), (3, 1, 2), (1, 5, 3)]:
+        A = rand_codes(rng, a_type, (M, K))
+        B = rand_codes(rng, b_type, (K, N))
+        zA = rand_codes(rng, a_type, (M,))
+        zB = rand_codes(rng, b_type, (N,))
+        r = O.int8_gemm_y_axis(A, a_type, zA, B, b_type, zB)
+        assert r["Y"].tolist() == brute_y_axis(A.tolist(), zA.tolist(), B.tolist(), zB.tolist())
+
+
+def test_axis_zp_equal_entries_reduce_to_per_tensor():
+    rng = np.random.default_rng(22)
+    for a_type, b_type in itertools.product(["u8", "s8"], repeat=2):
+        A = rand_codes(rng, a_type, (7, 33))
+        B = rand_codes(rng, b_type, (33, 5))
+        zA = int(rand_codes(rng, a_type, ()))
+        zB = int(rand_codes(rng, b_type, ()))
+        axis = O.int8_gemm_y_axis(A, a_type, np.full(7, zA), B, b_type, np.full(5, zB))
+        tensor = O.int8_gemm_y(A, a_type, zA, B, b_type, zB)
+        assert np.array_equal(axis["Y"], tensor["Y"])
+
+
+def test_axis_zp_page_proof_shape(golden):
+    """8 row zero points and 6 column zero points (the fully per-axis proof),
+    on the 8 x 16 x 6 proof shape; checked against an fp64 BLAS product of the
+    shifted operands and against brute force."""
+    g = golden("onnx_pack_qdq_constants.txt")
+    M, K, N = g["proof_shape"]
+    assert (M, N) == (g["per_axis_rows"], g["per_axis_cols"])
+    rng = np.random.default_rng(23)
+    A = rng.integers(-128, 128, (M, K))
+    B = rng.integers(-128, 128, (K, N))
+    zA = g["zp_x"] + rng.integers(-3, 4, M)
+    zB = g["zp_w"] + rng.integers(-3, 4, N)
+    r = O.int8_gemm_y_axis(A, "s8", zA, B, "s8", zB)
+    direct = (A - zA[:, None]).astype(np.float64) @ (B - zB[None, :]).astype(np.float64)
+    assert np.array_equal(r["Y"], direct.astype(np.int64))
+    assert r["Y"].tolist() == brute_y_axis(A.tolist(), zA.tolist(), B.tolist(), zB.tolist())
+
+
+def test_axis_zp_transposed_zero_points_are_caught():
+    """A plausible mistake, the row zero points applied along columns and the
+    column ones along rows, gives a different Y; the brute-force pin tells
+    the two apart (square shape, so both versions are well formed)."""
+    rng = np.random.default_rng(24)
+    A = rng.integers(-128, 128, (6, 9))
+    B = rng.integers(-128, 128, (9, 6))
+    zA = rng.integers(-128, 128, 6)
+    zB = rng.integers(-128, 128, 6)
+    good = O.int8_gemm_y_axis(A, "s8", zA, B, "s8", zB)["Y"].tolist()
+    assert good == brute_y_axis(A.tolist(), zA.tolist(), B.tolist(), zB.tolist())
+    assert good != brute_y_axis(A.tolist(), zB.tolist(), B.tolist(), zA.tolist())
