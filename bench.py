@@ -322,6 +322,9 @@ def run_ours(args, rank, world, dev):
     streams["w8"] = run_w8(q, I, args, dev, stream, hp.status, flush_l2)
     if int(hp.status.item()) != 0:
         raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
+    streams["axis"] = run_axis_zp(q, hp, args, dev, stream, hp.status, flush_l2)
+    if int(hp.status.item()) != 0:
+        raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
     streams["q8"] = run_q8(q, I, args, dev, stream, hp.status, flush_l2)
     if int(hp.status.item()) != 0:
         raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
@@ -531,6 +534,35 @@ def run_q8(q, I, args, dev, stream, status, flush_l2):
     return res
 
 
+def run_axis_zp(q, hp, args, dev, stream, status, flush_l2):
+    """The int8 GEMM with per-axis zero points (one per row of A, one per
+    column of B) on the step's M=4096 K=N=4608 operands, int8 out, one call
+    after an L2 flush; median over `args.steps` after `args.warmup`."""
+    import torch
+    c = hp.int8
+    g = torch.Generator().manual_seed(4096)
+    zA = torch.randint(0, 256, (c.M,), generator=g, dtype=torch.int32).to(dev)
+    zB = torch.randint(-8, 9, (c.N,), generator=g, dtype=torch.int32).to(dev)
+    ws = torch.empty(q.int8_gemm_axis_zp_workspace_size(c.M, c.K, c.N), dtype=torch.uint8, device=dev)
+    out = torch.empty((c.M, c.N), dtype=torch.int8, device=dev)
+    times = []
+    for i in range(args.warmup + args.steps):
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
+        flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q.int8_gemm_axis_zp(hp.A, c.a_type, zA, hp.packed, hp.col_sum, c.N, c.b_type, zB, "s8", bias=hp.bias,
+                            s_x=hp.s_x, s_w=hp.s_w, s_y=c.s_y, zp_y=c.zp_y, out=out, workspace=ws,
+                            dev_status=status)
+        e1.record(stream)
+        if i >= args.warmup:
+            times.append((e0, e1))
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in times)
+    return {"int8_gemm_axis_zp_m4096": {"us": us, "launches": 4, "TOPS": 2.0 * c.M * c.N * c.K / (us * 1e-6) / 1e12,
+                                        "shape": f"M={c.M} K={c.K} N={c.N}, zero point per row of A and per column of B"}}
+
+
 def cpu_int8_sample(rows: int):
     """The oracle (as it stands) on `rows` rows of the M=4096 K=N=4608 GEMM."""
     import numpy as np
@@ -642,6 +674,9 @@ def main():
         d = w8[name]
         rooflines[name] = {"bound": "tensor", "achieved": d["TFLOPS"], "peak": tensor_peak, "unit": "TFLOP/s",
                            "frac": d["TFLOPS"] / tensor_peak, "traffic": traffic.get(name)}
+    for name, d in streams["axis"].items():
+        rooflines[name] = {"bound": "tensor", "achieved": d["TOPS"], "peak": tensor_peak, "unit": "TFLOP/s",
+                           "frac": d["TOPS"] / tensor_peak, "traffic": traffic.get(name)}
     q8 = streams["q8"]
     for name, d in q8.items():
         if "gemv" in name:
@@ -674,6 +709,8 @@ def main():
         "w8a16": {"note": "int8 weights with one fp32 scale per row and 1,024 weights, bf16 activations; "
                           "timed apart from the step (median, L2 flushed before each single call)",
                   **w8},
+        "int8_axis_zp": {"note": "per-axis zero points: the exact GEMM to int32 in the workspace, row sums, "
+                                 "then one correction + output pass; timed apart from the step", **streams["axis"]},
         "q8": {"note": "8-bit tiles (bf16 scale per row and 32 columns) in the chunk format's two code layouts; "
                        "timed apart from the step (median, L2 flushed before each single call)",
                **q8},

@@ -27,9 +27,10 @@
  *   check fails.
  * - Errors found on the device go to `dev_status`, a device int32 that the
  *   caller sets to 0 (it may be NULL).  These are a bounded wait that ran out
- *   (QMM_ERR_TIMEOUT) and an expert id outside [0, n_expert)
- *   (QMM_ERR_BAD_EXPERT_ID).  The library only ever replaces a 0 there with
- *   an error code, so the caller reads it after synchronising.
+ *   (QMM_ERR_TIMEOUT), an expert id outside [0, n_expert)
+ *   (QMM_ERR_BAD_EXPERT_ID), and a per-axis zero point outside its operand's
+ *   domain (QMM_ERR_INVALID_ARG).  The library only ever replaces a 0 there
+ *   with an error code, so the caller reads it after synchronising.
  * - Shapes the library has no kernel for return QMM_ERR_UNSUPPORTED.  There
  *   is no fallback path.
  */
@@ -149,6 +150,38 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
                          qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out,
                          int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
                          cudaStream_t stream);
+
+/* Workspace of qmm_int8_gemm_axis_zp: the int32 product [M][N] and the row
+ * sums [M], each rounded up to 256 bytes, plus qmm_int8_gemm_workspace_size. */
+qmm_status qmm_int8_gemm_axis_zp_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes);
+
+/* qmm_int8_gemm with per-axis zero points: one per activation row and one per
+ * weight column ("The ONNX pack...", "What works today": the asymmetric
+ * corrections are per-tensor or per-axis along the same axes as the scales,
+ * exact in integers):
+ *     Y[m,n] = sum_k (A[m,k] - zA[m]) (B[k,n] - zB[n])
+ *            = S - zA'[m] colSum[n] - zB'[n] (rowSum[m] - K zA'[m])
+ * then the same bias and output conversion as qmm_int8_gemm (bit-exact).
+ *
+ * zA   device int32 [M], each in A's domain (0..255 for QMM_U8, -128..127 for
+ *      QMM_S8), or NULL for all zeros.
+ * zB   device int32 [N] in the domain of b_orig_type (QMM_U8 / QMM_S8), or NULL
+ *      for all zeros; must be NULL for QMM_F32 weights (symmetric).
+ * All other arguments as qmm_int8_gemm, except the workspace, which must hold
+ * qmm_int8_gemm_axis_zp_workspace_size(M, K, N) bytes (256-byte aligned).
+ * The exact product goes through the per-tensor GEMM into the workspace
+ * (int32), and one more pass applies the corrections, the bias and the output
+ * conversion: the call costs an int32 write and read of M x N more than
+ * qmm_int8_gemm.
+ * Errors: as qmm_int8_gemm.  Zero points are device data: one outside its
+ * domain sets QMM_ERR_INVALID_ARG in dev_status, and the outputs are then
+ * unspecified.
+ */
+qmm_status qmm_int8_gemm_axis_zp(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int64_t lda,
+                                 const int32_t* zA, const void* packedB, const int32_t* col_sum, int64_t N,
+                                 qmm_dtype b_orig_type, const int32_t* zB, const qmm_epilogue* ep, void* out,
+                                 int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                 cudaStream_t stream);
 
 /* Workspace of qmm_quantize_act_int8: 256 bytes for per-tensor scaling, 0 per row. */
 qmm_status qmm_quantize_act_int8_workspace_size(int64_t M, int64_t K, int per_row, size_t* ws_bytes);

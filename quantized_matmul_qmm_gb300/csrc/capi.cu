@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 
+#include "int8_axis.h"
 #include "qmm_internal.h"
 
 using namespace qmm;
@@ -139,6 +140,81 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
   }
   if ((M + 31) / 32 > 65535) return QMM_ERR_UNSUPPORTED;
   return cuda_status(launch_int8_gemm_mma(a, stream));
+}
+
+namespace {
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+}  // namespace
+
+qmm_status qmm_int8_gemm_axis_zp_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes) {
+  if (ws_bytes == nullptr || M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (!k_bound_ok(K)) return QMM_ERR_OVERFLOW_BOUND;
+  if (M > INT32_MAX || N > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  *ws_bytes = round256((size_t)M * N * 4) + round256((size_t)M * 4) + int8_umma_workspace_bytes(M, K, N);
+  return QMM_OK;
+}
+
+qmm_status qmm_int8_gemm_axis_zp(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int64_t lda,
+                                 const int32_t* zA, const void* packedB, const int32_t* col_sum, int64_t N,
+                                 qmm_dtype b_orig_type, const int32_t* zB, const qmm_epilogue* ep, void* out,
+                                 int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                 cudaStream_t stream) {
+  if (A == nullptr || packedB == nullptr || col_sum == nullptr || ep == nullptr || out == nullptr)
+    return QMM_ERR_INVALID_ARG;
+  if (M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (a_type != QMM_U8 && a_type != QMM_S8) return QMM_ERR_INVALID_ARG;
+  if (b_orig_type != QMM_U8 && b_orig_type != QMM_S8 && b_orig_type != QMM_F32)
+    return QMM_ERR_INVALID_ARG;
+  if (b_orig_type == QMM_F32 && zB != nullptr) return QMM_ERR_INVALID_ARG;   // symmetric weights
+  if (!k_bound_ok(K)) return QMM_ERR_OVERFLOW_BOUND;
+  if (lda < K || lda % 16 != 0 || !aligned(A, 16) || !aligned(packedB, 16)) return QMM_ERR_INVALID_ARG;
+  if ((zA != nullptr && !aligned(zA, 4)) || (zB != nullptr && !aligned(zB, 4)) || !aligned(col_sum, 4))
+    return QMM_ERR_INVALID_ARG;
+  const qmm_dtype ot = ep->out_type;
+  if (ot != QMM_S32 && ot != QMM_F32 && ot != QMM_S8 && ot != QMM_U8) return QMM_ERR_INVALID_ARG;
+  if (ldo < N) return QMM_ERR_INVALID_ARG;
+  if (ep->s_x != nullptr && ep->s_x_stride != 0 && ep->s_x_stride != 1) return QMM_ERR_INVALID_ARG;
+  if ((ot == QMM_S8 || ot == QMM_U8) && !(ep->s_y > 0.0f)) return QMM_ERR_INVALID_ARG;
+  const size_t osz = (ot == QMM_S32 || ot == QMM_F32) ? 4 : 1;
+  if (!aligned(out, osz)) return QMM_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  const size_t s_bytes = round256((size_t)M * N * 4), r_bytes = round256((size_t)M * 4);
+  const size_t g_bytes = int8_umma_workspace_bytes(M, K, N);
+  if (workspace == nullptr || !aligned(workspace, 256) || ws_bytes < s_bytes + r_bytes + g_bytes)
+    return QMM_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  int32_t* S = reinterpret_cast<int32_t*>(ws);
+  int32_t* row_sum = reinterpret_cast<int32_t*>(ws + s_bytes);
+  // S' = sum_k A'B' exactly: zero points that shift to 0, int32 output, no bias
+  const qmm_epilogue eps = {QMM_S32, nullptr, nullptr, 0, nullptr, 1.0f, 0};
+  const qmm_status st = qmm_int8_gemm(A, a_type, M, K, lda, a_type == QMM_U8 ? 128 : 0, packedB, col_sum, N,
+                                      b_orig_type, b_orig_type == QMM_U8 ? 128 : 0, &eps, S, N,
+                                      g_bytes ? ws + s_bytes + r_bytes : nullptr, g_bytes, dev_status, stream);
+  if (st != QMM_OK) return st;
+  Int8AxisArgs a{};
+  a.A = static_cast<const uint8_t*>(A);
+  a.lda = lda;
+  a.a_u8 = a_type == QMM_U8;
+  a.b_u8 = b_orig_type == QMM_U8;
+  a.M = (int)M;
+  a.K = (int)K;
+  a.N = (int)N;
+  a.zA = zA;
+  a.zB = zB;
+  a.S = S;
+  a.row_sum = row_sum;
+  a.epi.out_type = (int)ot;
+  a.epi.bias = ep->bias;
+  a.epi.s_x = ep->s_x;
+  a.epi.s_x_stride = (int)ep->s_x_stride;
+  a.epi.s_w = ep->s_w;
+  a.epi.s_y = ep->s_y;
+  a.epi.zp_y = ep->zp_y;
+  a.epi.col_sum = col_sum;
+  a.epi.out = out;
+  a.epi.ldo = ldo;
+  a.dev_status = dev_status;
+  return cuda_status(launch_int8_axis_zp(a, stream));
 }
 
 qmm_status qmm_quantize_act_int8_workspace_size(int64_t M, int64_t K, int per_row, size_t* ws_bytes) {

@@ -41,6 +41,9 @@ SIGNATURES = {
     "qmm_int8_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
     "qmm_int8_gemm": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _c.c_int,
                                  _i32, _c.POINTER(QmmEpilogue), _vp, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_int8_gemm_axis_zp_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
+    "qmm_int8_gemm_axis_zp": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _c.c_int,
+                                         _vp, _c.POINTER(QmmEpilogue), _vp, _i64, _vp, _sz, _vp, _vp]),
     "qmm_quantize_act_int8_workspace_size": (_c.c_int, [_i64, _i64, _c.c_int, _szp]),
     "qmm_quantize_act_int8": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _c.c_int, _vp, _i64, _vp, _vp, _sz,
                                          _vp]),
@@ -153,6 +156,30 @@ def int8_gemm(A: torch.Tensor, a_type: str, zA: int, packed: torch.Tensor, col_s
         DTYPES[b_orig_type], int(zB), ctypes.byref(ep), _ptr(out), out.stride(0), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream()))
+    return out
+
+
+def int8_gemm_axis_zp_workspace_size(M: int, K: int, N: int) -> int:
+    return _size("qmm_int8_gemm_axis_zp_workspace_size", M, K, N)
+
+
+def int8_gemm_axis_zp(A: torch.Tensor, a_type: str, zA, packed: torch.Tensor, col_sum: torch.Tensor,
+                      N: int, b_orig_type: str, zB, out_type: str = "s32", bias=None, s_x=None,
+                      s_x_stride: int = 0, s_w=None, s_y: float = 1.0, zp_y: int = 0, out=None,
+                      workspace=None, dev_status=None):
+    """qmm_int8_gemm with per-axis zero points: zA a device int32 [M] (or None:
+    all 0), zB a device int32 [N] (or None).  Returns the output tensor."""
+    M, K = A.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=TORCH_OUT[out_type], device=A.device)
+    if workspace is None:
+        workspace = torch.empty(int8_gemm_axis_zp_workspace_size(M, K, N), dtype=torch.uint8, device=A.device)
+    ep = QmmEpilogue(DTYPES[out_type], _ptr(bias), _ptr(s_x), s_x_stride, _ptr(s_w),
+                     float(s_y), int(zp_y))
+    _check("qmm_int8_gemm_axis_zp", lib.qmm_int8_gemm_axis_zp(
+        _ptr(A), DTYPES[a_type], M, K, A.stride(0), _ptr(zA), _ptr(packed), _ptr(col_sum), N,
+        DTYPES[b_orig_type], _ptr(zB), ctypes.byref(ep), _ptr(out), out.stride(0), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
     return out
 
 

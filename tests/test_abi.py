@@ -188,3 +188,27 @@ def test_format_sizes_and_host_validation(qmm):
     assert g(P, 1, 32, 256, P, 17, 256, P, 32, None, 0, None, None) == qmm.QMM_ERR_WORKSPACE
     assert g(P, 1, 32, 256, P, 17, 256, P, 32, P, 32 * 256 * 2, None, None) == qmm.QMM_ERR_WORKSPACE
     assert g(P, 1, 32, 65792, P, 17, 65792, P, 32, P, 1 << 30, None, None) == qmm.QMM_ERR_UNSUPPORTED
+
+
+def test_axis_zp_sizes_and_host_validation(qmm):
+    # int32 product [M][N] + row sums [M] (each rounded up to 256) + the GEMM's own workspace
+    assert qmm.int8_gemm_axis_zp_workspace_size(16, 1024, 1024) == 16 * 1024 * 4 + 256 + \
+        qmm.int8_gemm_workspace_size(16, 1024, 1024)
+    assert qmm.int8_gemm_axis_zp_workspace_size(300, 64, 7) == 8448 + 1280 + qmm.int8_gemm_workspace_size(300, 64, 7)
+    L = qmm.lib
+    P = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: every call below fails on the host
+    ep = qmm.QmmEpilogue(qmm.QMM_S32, None, None, 0, None, 1.0, 0)
+    epb = ctypes.byref(ep)
+    g = L.qmm_int8_gemm_axis_zp
+    big = 1 << 30
+    # column zero points with fp32 (symmetric) weights; misaligned zero points; missing workspace;
+    # K beyond the int32 bound; bad output type
+    assert g(P, qmm.QMM_S8, 4, 16, 16, None, P, P, 8, qmm.QMM_F32, P, epb, P, 8, P, big, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, qmm.QMM_S8, 4, 16, 16, ctypes.c_void_p((1 << 20) + 2), P, P, 8, qmm.QMM_S8, P, epb, P, 8, P, big,
+             None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert g(P, qmm.QMM_S8, 4, 16, 16, P, P, P, 8, qmm.QMM_S8, P, epb, P, 8, None, 0, None, None) == qmm.QMM_ERR_WORKSPACE
+    assert g(P, qmm.QMM_S8, 4, 16, 16, P, P, P, 8, qmm.QMM_S8, P, epb, P, 8, P, 255, None, None) == qmm.QMM_ERR_WORKSPACE
+    assert g(P, qmm.QMM_S8, 4, 70000, 70000, P, P, P, 8, qmm.QMM_S8, P, epb, P, 8, P, big, None, None) == qmm.QMM_ERR_OVERFLOW_BOUND
+    bad = qmm.QmmEpilogue(qmm.QMM_BF16, None, None, 0, None, 1.0, 0)
+    assert g(P, qmm.QMM_S8, 4, 16, 16, P, P, P, 8, qmm.QMM_S8, P, ctypes.byref(bad), P, 8, P, big, None,
+             None) == qmm.QMM_ERR_INVALID_ARG
