@@ -229,6 +229,24 @@ class HotPath:
                                          m.T, Y=Y, workspace=ws, dev_status=self.status)
 
 
+def max_over_ranks(values, world, device):
+    """Elementwise max of `values` over the ranks.  The replicas run the same
+    work, so the job is as slow as its slowest rank: every timing is the
+    maximum over ranks before any rate is derived from it."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replicas_rate(per_replica_rate, world):
+    """Whole-job throughput of `world` replicas, each at the rate taken from
+    the slowest rank's time (weak scaling: the work per GPU is fixed)."""
+    return world * per_replica_rate
+
+
 def run_ours(args, rank, world, dev):
     import torch
     import torch.distributed as dist
@@ -286,10 +304,8 @@ def run_ours(args, rank, world, dev):
             ms = evs[2 * i].elapsed_time(evs[2 * i + 1])
             per_call[i] += ms
             total += ms
-    t = torch.tensor(per_call + [total], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    per_call, total = t[:-1].tolist(), float(t[-1])
+    red = max_over_ranks(per_call + [total], world, dev)
+    per_call, total = red[:-1], red[-1]
 
     # end to end through the public API: pinned host A in, int8 result out
     c = hp.int8
@@ -310,10 +326,7 @@ def run_ours(args, rank, world, dev):
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_times.append(e0.elapsed_time(e1))
-    te = torch.tensor([sum(e2e_times)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms = float(te) / args.steps
+    e2e_ms = max_over_ranks([sum(e2e_times)], world, dev)[0] / args.steps
     if int(hp.status.item()) != 0:
         raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
     streams = run_gemv_streams(hp, q, args, dev, stream)
@@ -643,7 +656,7 @@ def main():
     tensor_peak = peaks["bf16_tflops"]
     hbm_peak = peaks["hbm_gbs"]
     traffic = load_traffic()
-    value = world * i8["TOPS"]
+    value = replicas_rate(i8["TOPS"], world)
     lm = kern["q4_gemv_lm_head_m1"]
     st_lm, st_ps = streams["lm_head"], streams["projection_set"]
     roof = {"bound": "tensor", "achieved": i8["TOPS"], "peak": tensor_peak, "unit": "TFLOP/s",
@@ -696,7 +709,7 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
         "rooflines": rooflines,
-        "gemv": {"value": world * st_lm["weight_GBs"], "unit": "GB/s", "kernel": "q4_gemv_lm_head_m1",
+        "gemv": {"value": replicas_rate(st_lm["weight_GBs"], world), "unit": "GB/s", "kernel": "q4_gemv_lm_head_m1",
                  "frac_hbm": st_lm["GBs"] / hbm_peak, "peak_source": peak_kind,
                  "method": f"lm_head M=1, back-to-back launches over {st_lm['copies']} rotating weight copies "
                            f"(>= 4x the {streams['l2_bytes'] >> 20} MiB L2), median over passes",
@@ -714,7 +727,7 @@ def main():
         "q8": {"note": "8-bit tiles (bf16 scale per row and 32 columns) in the chunk format's two code layouts; "
                        "timed apart from the step (median, L2 flushed before each single call)",
                **q8},
-        "e2e": {"value": world * 2.0 * c.M * c.N * c.K / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+        "e2e": {"value": replicas_rate(2.0 * c.M * c.N * c.K / (e2e_ms * 1e-3) / 1e12, world), "unit": "TOPS",
                 "h2d_bytes_per_step": c.M * c.K, "d2h_bytes_per_step": c.M * c.N},
         "gpu_launches": launches,
         "clocks": clk,

@@ -21,7 +21,10 @@
 // the decode GEMV reads.
 //
 // Decode GEMV (M <= 16): a warp owns one slab (16 output rows) of a tile row
-// and walks its tiles, or every wpu-th of them when wpu warps share a slab.
+// and walks its tiles, or every wpu-th of them when wpu warps share a slab
+// (small N).  With one warp per slab the grid is one resident wave and each
+// warp streams slab after slab, loading the next tile while it computes the
+// current one, across slab boundaries too.
 // Lane l reads the eight groups of columns 8l .. 8l+7 (one 32-column block,
 // so one scale per row), forms each row's 8-term partial dot product per
 // activation row, scales it, and a reduce-scatter across the warp (16 + 1
@@ -245,100 +248,148 @@ __device__ __forceinline__ void q8_rows_dot(const uint32_t (&xw)[8][4], const ui
   }
 }
 
+// One tile of a slab: the lane's 16 row sums over its 8 columns, scaled.
+// With one activation row they accumulate in racc (pairs of rows) for the
+// reduction at the end of the slab; otherwise each activation row is reduced
+// across the warp here and added to acc[m] (row l & 15 in lane l).
+template <int kM>
+__device__ __forceinline__ void q8_tile_compute(const Q8Group& cur, int tc, int lane, const __nv_bfloat16* X,
+                                                int64_t ldx, int M, uint64_t (&racc)[8], float (&acc)[kM]) {
+  uint64_t sc[8];   // scales of rows (2p, 2p+1)
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const uint32_t sw = u4_get(cur.s[p >> 2], p & 3);
+    sc[p] = f2_pack(bf16lo_to_f32(sw), bf16hi_to_f32(sw));
+  }
+  uint32_t xw[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    xw[j][0] = cur.v[j].x ^ 0x80808080u;
+    xw[j][1] = cur.v[j].y ^ 0x80808080u;
+    xw[j][2] = cur.v[j].z ^ 0x80808080u;
+    xw[j][3] = cur.v[j].w ^ 0x80808080u;
+  }
+  const int k0 = 256 * tc + 8 * lane;
+  if constexpr (kM == 1) {
+    uint64_t pr[8];
+    q8_rows_dot(xw, ldg128(X + k0), pr);
+#pragma unroll
+    for (int p = 0; p < 8; ++p) racc[p] = f2_fma(pr[p], sc[p], racc[p]);
+  } else {
+#pragma unroll
+    for (int m = 0; m < kM; ++m) {
+      if (m >= M) break;
+      uint64_t pr[8];
+      q8_rows_dot(xw, ldg128(X + (int64_t)m * ldx + k0), pr);
+      float v[16];
+#pragma unroll
+      for (int p = 0; p < 8; ++p) f2_unpack(f2_mul(pr[p], sc[p]), v[2 * p], v[2 * p + 1]);
+      acc[m] += warp_rows16(v, lane);
+    }
+  }
+}
+
+// The slab's results: row 16u + l in lane l < 16.
+template <int kM>
+__device__ __forceinline__ void q8_slab_finish(int lane, uint64_t (&racc)[8], float (&acc)[kM]) {
+  if constexpr (kM == 1) {
+    float v[16];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      f2_unpack(racc[p], v[2 * p], v[2 * p + 1]);
+      racc[p] = 0ull;
+    }
+    acc[0] = warp_rows16(v, lane);
+  }
+}
+
 template <int kM, int kLayout>
 __global__ void __launch_bounds__(kQ8GvWarps * 32)
 q8_gemv_kernel(const uint8_t* __restrict__ tiles, int TR, int TC, const __nv_bfloat16* __restrict__ X, int64_t ldx,
                float* __restrict__ Y, int64_t ldy, int M, int wpu) {
   __shared__ float red[kQ8GvWarps][kM][16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nunits = 2 * TR;
+  uint64_t racc[8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) racc[p] = 0ull;
+  float acc[kM];
+#pragma unroll
+  for (int m = 0; m < kM; ++m) acc[m] = 0.f;
+
+  if (wpu == 1) {
+    // every warp on its own: one stream of (slab, tile) pairs, slab u, u + the
+    // grid's warp count, ...; the next pair's loads are issued before the
+    // current one is computed, across slab boundaries too
+    const int tw = (int)gridDim.x * kQ8GvWarps;
+    int u = (int)blockIdx.x * kQ8GvWarps + warp;
+    if (u >= nunits) return;
+    int tc = 0;
+    Q8Group nxt;
+    q8_load<kLayout>(nxt, tiles + (int64_t)(u >> 1) * TC * kQ8TileBytes, lane, u & 1);
+    while (true) {
+      const Q8Group cur = nxt;
+      int nu = u, ntc = tc + 1;
+      if (ntc == TC) {
+        nu = u + tw;
+        ntc = 0;
+      }
+      if (nu < nunits) q8_load<kLayout>(nxt, tiles + ((int64_t)(nu >> 1) * TC + ntc) * kQ8TileBytes, lane, nu & 1);
+      q8_tile_compute<kM>(cur, tc, lane, X, ldx, M, racc, acc);
+      if (ntc == 0) {
+        q8_slab_finish<kM>(lane, racc, acc);
+        if (lane < 16) {
+          const int n = 16 * u + lane;
+#pragma unroll
+          for (int m = 0; m < kM; ++m)
+            if (m < M) Y[(int64_t)m * ldy + n] = acc[m];
+        }
+#pragma unroll
+        for (int m = 0; m < kM; ++m) acc[m] = 0.f;
+      }
+      if (nu >= nunits) break;
+      u = nu;
+      tc = ntc;
+    }
+    return;
+  }
+
+  // wpu warps share a slab, each taking every wpu-th tile; the block adds
+  // their partial sums in a fixed order
   const int upb = kQ8GvWarps / wpu;                 // slabs per block
   const int unit_l = warp / wpu, part = warp % wpu;
-  const int nunits = 2 * TR;
   const int ngroups = (nunits + upb - 1) / upb;
   for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
     const int u = grp * upb + unit_l;
-    float acc[kM];
-#pragma unroll
-    for (int m = 0; m < kM; ++m) acc[m] = 0.f;
     if (u < nunits) {
-      const int tr = u >> 1, h = u & 1;
-      const uint8_t* row_tiles = tiles + (int64_t)tr * TC * kQ8TileBytes;
-      // one activation row: the scaled per-row sums stay in the lane across
-      // tiles (the lane's columns are in the same 32-column block of every
-      // tile), and the warp reduces them once at the end
-      uint64_t racc[8];
-#pragma unroll
-      for (int p = 0; p < 8; ++p) racc[p] = 0ull;
+      const uint8_t* row_tiles = tiles + (int64_t)(u >> 1) * TC * kQ8TileBytes;
       Q8Group nxt;
-      if (part < TC) q8_load<kLayout>(nxt, row_tiles + (int64_t)part * kQ8TileBytes, lane, h);
+      if (part < TC) q8_load<kLayout>(nxt, row_tiles + (int64_t)part * kQ8TileBytes, lane, u & 1);
       for (int tc = part; tc < TC; tc += wpu) {
         const Q8Group cur = nxt;
-        if (tc + wpu < TC) q8_load<kLayout>(nxt, row_tiles + (int64_t)(tc + wpu) * kQ8TileBytes, lane, h);
-        uint64_t sc[8];   // scales of rows (2p, 2p+1)
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const uint32_t sw = u4_get(cur.s[p >> 2], p & 3);
-          sc[p] = f2_pack(bf16lo_to_f32(sw), bf16hi_to_f32(sw));
-        }
-        uint32_t xw[8][4];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          xw[j][0] = cur.v[j].x ^ 0x80808080u;
-          xw[j][1] = cur.v[j].y ^ 0x80808080u;
-          xw[j][2] = cur.v[j].z ^ 0x80808080u;
-          xw[j][3] = cur.v[j].w ^ 0x80808080u;
-        }
-        const int k0 = 256 * tc + 8 * lane;
-        if constexpr (kM == 1) {
-          uint64_t pr[8];
-          q8_rows_dot(xw, ldg128(X + k0), pr);
-#pragma unroll
-          for (int p = 0; p < 8; ++p) racc[p] = f2_fma(pr[p], sc[p], racc[p]);
-        } else {
-#pragma unroll
-          for (int m = 0; m < kM; ++m) {
-            if (m >= M) break;
-            uint64_t pr[8];
-            q8_rows_dot(xw, ldg128(X + (int64_t)m * ldx + k0), pr);
-            float v[16];
-#pragma unroll
-            for (int p = 0; p < 8; ++p) f2_unpack(f2_mul(pr[p], sc[p]), v[2 * p], v[2 * p + 1]);
-            acc[m] += warp_rows16(v, lane);
-          }
-        }
+        if (tc + wpu < TC) q8_load<kLayout>(nxt, row_tiles + (int64_t)(tc + wpu) * kQ8TileBytes, lane, u & 1);
+        q8_tile_compute<kM>(cur, tc, lane, X, ldx, M, racc, acc);
       }
-      if constexpr (kM == 1) {
-        float v[16];
+      q8_slab_finish<kM>(lane, racc, acc);
+    }
+    if (lane < 16) {
 #pragma unroll
-        for (int p = 0; p < 8; ++p) f2_unpack(racc[p], v[2 * p], v[2 * p + 1]);
-        acc[0] = warp_rows16(v, lane);
+      for (int m = 0; m < kM; ++m) red[warp][m][lane] = acc[m];
+    }
+    __syncthreads();
+    if (part == 0 && u < nunits && lane < 16) {
+      const int n = 16 * u + lane;
+#pragma unroll
+      for (int m = 0; m < kM; ++m) {
+        if (m >= M) break;
+        float a = 0.f;
+        for (int p = 0; p < wpu; ++p) a += red[warp + p][m][lane];
+        Y[(int64_t)m * ldy + n] = a;
       }
     }
-    if (wpu == 1) {
-      if (u < nunits && lane < 16) {
-        const int n = 16 * u + lane;
 #pragma unroll
-        for (int m = 0; m < kM; ++m)
-          if (m < M) Y[(int64_t)m * ldy + n] = acc[m];
-      }
-    } else {
-      if (lane < 16) {
-#pragma unroll
-        for (int m = 0; m < kM; ++m) red[warp][m][lane] = acc[m];
-      }
-      __syncthreads();
-      if (part == 0 && u < nunits && lane < 16) {
-        const int n = 16 * u + lane;
-#pragma unroll
-        for (int m = 0; m < kM; ++m) {
-          if (m >= M) break;
-          float a = 0.f;
-          for (int p = 0; p < wpu; ++p) a += red[warp + p][m][lane];
-          Y[(int64_t)m * ldy + n] = a;
-        }
-      }
-      __syncthreads();
-    }
+    for (int m = 0; m < kM; ++m) acc[m] = 0.f;
+    __syncthreads();
   }
 }
 
@@ -376,12 +427,21 @@ q8_decode_bf16_kernel(const uint8_t* __restrict__ tiles, int TC, int K, __nv_bfl
 }
 
 template <int kM>
-cudaError_t q8_gemv_launch(int layout, int grid, const uint8_t* tiles, int TR, int TC, const __nv_bfloat16* X,
-                           int64_t ldx, float* Y, int64_t ldy, int M, int wpu, cudaStream_t stream) {
-  if (layout == 0)
-    q8_gemv_kernel<kM, 0><<<grid, kQ8GvWarps * 32, 0, stream>>>(tiles, TR, TC, X, ldx, Y, ldy, M, wpu);
-  else
-    q8_gemv_kernel<kM, 1><<<grid, kQ8GvWarps * 32, 0, stream>>>(tiles, TR, TC, X, ldx, Y, ldy, M, wpu);
+cudaError_t q8_gemv_launch(int layout, int units, int sms, const uint8_t* tiles, int TR, int TC,
+                           const __nv_bfloat16* X, int64_t ldx, float* Y, int64_t ldy, int M, int wpu,
+                           cudaStream_t stream) {
+  auto kern = layout == 0 ? q8_gemv_kernel<kM, 0> : q8_gemv_kernel<kM, 1>;
+  const int upb = kQ8GvWarps / wpu;
+  const int ngroups = (units + upb - 1) / upb;
+  int grid = std::min(ngroups, 8 * sms);
+  if (wpu == 1) {
+    // one resident wave: each warp streams several slabs without a relaunch
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQ8GvWarps * 32, 0);
+    if (err != cudaSuccess) return err;
+    grid = std::min(ngroups, std::max(1, per_sm) * sms);
+  }
+  kern<<<std::max(1, grid), kQ8GvWarps * 32, 0, stream>>>(tiles, TR, TC, X, ldx, Y, ldy, M, wpu);
   return cudaGetLastError();
 }
 
@@ -421,14 +481,11 @@ cudaError_t launch_q8_gemm(const uint8_t* tiles, int layout, int N, int K, const
     const int units = 2 * TR;
     int wpu = 1;
     while (wpu < kQ8GvWarps && wpu < TC && (int64_t)units * wpu < (int64_t)16 * sms) wpu *= 2;
-    const int upb = kQ8GvWarps / wpu;
-    const int ngroups = (units + upb - 1) / upb;
-    const int grid = std::max(1, std::min(ngroups, 8 * sms));
-    if (M <= 1) return q8_gemv_launch<1>(layout, grid, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
-    if (M <= 2) return q8_gemv_launch<2>(layout, grid, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
-    if (M <= 4) return q8_gemv_launch<4>(layout, grid, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
-    if (M <= 8) return q8_gemv_launch<8>(layout, grid, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
-    return q8_gemv_launch<16>(layout, grid, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
+    if (M <= 1) return q8_gemv_launch<1>(layout, units, sms, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
+    if (M <= 2) return q8_gemv_launch<2>(layout, units, sms, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
+    if (M <= 4) return q8_gemv_launch<4>(layout, units, sms, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
+    if (M <= 8) return q8_gemv_launch<8>(layout, units, sms, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
+    return q8_gemv_launch<16>(layout, units, sms, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
   }
   char* ws = static_cast<char*>(workspace);
   __nv_bfloat16* B16 = reinterpret_cast<__nv_bfloat16*>(ws);

@@ -52,21 +52,42 @@ axis_rowsum_kernel(const uint8_t* __restrict__ A, int64_t lda, int M, int K, boo
   }
 }
 
+// Four consecutive columns per thread (one 16-byte load of S' when the row
+// stride allows), rows strided over the grid's y dimension.
 __global__ void __launch_bounds__(kEpiThreads)
 axis_epilogue_kernel(const int32_t* __restrict__ S, int M, int N, int K, const int32_t* __restrict__ zA, int a_shift,
                      int za_lo, int za_hi, const int32_t* __restrict__ zB, int b_shift, int zb_lo, int zb_hi,
                      const int32_t* __restrict__ row_sum, const Int8Epi e, int32_t* dev_status) {
+  const bool vec = (N & 3) == 0;
   for (int m = blockIdx.y; m < M; m += gridDim.y) {
     const int32_t za = zA != nullptr ? zA[m] : 0;
     if ((za < za_lo || za > za_hi) && blockIdx.x == 0 && threadIdx.x == 0) set_status(dev_status, QMM_ERR_INVALID_ARG);
     const uint32_t zap = (uint32_t)(za - a_shift);
     const uint32_t r = (uint32_t)row_sum[m] - (uint32_t)K * zap;
-    for (int n = (int)blockIdx.x * kEpiThreads + (int)threadIdx.x; n < N; n += (int)gridDim.x * kEpiThreads) {
-      const int32_t zb = zB != nullptr ? zB[n] : 0;
-      if ((zb < zb_lo || zb > zb_hi) && m == (int)blockIdx.y) set_status(dev_status, QMM_ERR_INVALID_ARG);
-      const uint32_t zbp = (uint32_t)(zb - b_shift);
-      const uint32_t y = (uint32_t)S[(int64_t)m * N + n] - zap * (uint32_t)e.col_sum[n] - zbp * r;
-      int8_store(e, m, n, (int32_t)y);
+    const int32_t* srow = S + (int64_t)m * N;
+    for (int n0 = 4 * ((int)blockIdx.x * kEpiThreads + (int)threadIdx.x); n0 < N;
+         n0 += 4 * (int)gridDim.x * kEpiThreads) {
+      int32_t sv[4];
+      if (vec) {
+        const int4 v = *reinterpret_cast<const int4*>(srow + n0);
+        sv[0] = v.x;
+        sv[1] = v.y;
+        sv[2] = v.z;
+        sv[3] = v.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sv[i] = n0 + i < N ? srow[n0 + i] : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int n = n0 + i;
+        if (n >= N) break;
+        const int32_t zb = zB != nullptr ? zB[n] : 0;
+        if ((zb < zb_lo || zb > zb_hi) && m == (int)blockIdx.y) set_status(dev_status, QMM_ERR_INVALID_ARG);
+        const uint32_t zbp = (uint32_t)(zb - b_shift);
+        const uint32_t y = (uint32_t)sv[i] - zap * (uint32_t)e.col_sum[n] - zbp * r;
+        int8_store(e, m, n, (int32_t)y);
+      }
     }
   }
 }
@@ -80,8 +101,8 @@ cudaError_t launch_int8_axis_zp(const Int8AxisArgs& a, cudaStream_t stream) {
   axis_rowsum_kernel<<<rgrid, kRowSumWarps * 32, 0, stream>>>(a.A, a.lda, a.M, a.K, a.a_u8, a.row_sum);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const int gx = std::max(1, std::min((a.N + kEpiThreads - 1) / kEpiThreads, 64));
-  const int gy = std::max(1, std::min(a.M, 65535));
+  const int gx = std::max(1, std::min((a.N + 4 * kEpiThreads - 1) / (4 * kEpiThreads), 16));
+  const int gy = std::max(1, std::min(a.M, 1024));
   const int za_lo = a.a_u8 ? 0 : -128, za_hi = a.a_u8 ? 255 : 127;
   const int zb_lo = a.b_u8 ? 0 : -128, zb_hi = a.b_u8 ? 255 : 127;
   axis_epilogue_kernel<<<dim3(gx, gy), kEpiThreads, 0, stream>>>(a.S, a.M, a.N, a.K, a.zA, a.a_u8 ? 128 : 0, za_lo,

@@ -8,13 +8,14 @@
 // q = clamp(rint_even(fl(w / s)), -127, 127), 0 where s == 0.  Codes are
 // [N][Kp] (Kp = K rounded up to 64, zero padding), scales [N][ceil(K/1024)].
 //
-// Decode GEMV (M <= 16): one warp per weight row at a time.  Each lane takes
-// 16 consecutive codes per step (512 bytes per warp load, four steps in
-// flight), converts them exactly with a byte permute and one add (the
-// int-to-float unit runs at a quarter of the fma rate), and multiplies them
+// Decode GEMV (M <= 16): a warp streams 32/G rows at once with G lanes per
+// row, G sized so that every lane has about eight 16-byte groups of its row
+// (a K = 1024 row is 1 KB: four rows per warp, 4 KB in flight per warp).  Each
+// lane converts its codes exactly with a byte permute and one add (the
+// int-to-float unit runs at a quarter of the fma rate) and multiplies them
 // with x read through the read-only cache, even and odd columns as the two
-// lanes of packed f32x2 fmas.  Sixteen codes never straddle a 1,024 block, so each
-// group's partial sum is scaled by its own block's scale.
+// lanes of packed f32x2 fmas.  Sixteen codes never straddle a 1,024 block, so
+// each group's partial sum is scaled by its own block's scale.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -58,7 +59,7 @@ pack_w8_kernel(const float* __restrict__ W, int64_t ldw, int K, int Kp, int8_t* 
 }
 
 constexpr int kGvWarps = 8;
-constexpr int kGvSteps = 4;   // 16-byte code groups in flight per lane
+constexpr int kGvSteps = 8;   // 16-byte code groups in flight per lane
 
 // 16 int8 codes as fp32 (exact), without the int-to-float unit.
 __device__ __forceinline__ void codes16_to_f32(const uint4 v, float (&c)[16]) {
@@ -69,31 +70,38 @@ __device__ __forceinline__ void codes16_to_f32(const uint4 v, float (&c)[16]) {
     for (int j = 0; j < 4; ++j) c[4 * i + j] = s8_byte_to_f32(w[i], j);
 }
 
+// A warp works on 32 / G rows at once, G lanes per row (G a power of two
+// chosen so that a lane has about kGvSteps groups of its row): each load
+// instruction of the warp reads G consecutive 16-byte groups of every one of
+// its rows, and kGvSteps such loads are in flight before any is used.
 template <int kM>
 __global__ void __launch_bounds__(kGvWarps * 32)
 w8_gemv_kernel(const int8_t* __restrict__ codes, const float* __restrict__ scales, int N, int K, int Kp, int nb,
-               const __nv_bfloat16* __restrict__ X, int64_t ldx, float* __restrict__ Y, int64_t ldy, int M) {
+               const __nv_bfloat16* __restrict__ X, int64_t ldx, float* __restrict__ Y, int64_t ldy, int M, int G) {
   const int lane = threadIdx.x & 31;
+  const int R = 32 / G, sub = lane / G, sl = lane % G;
   const int warp_g = (int)blockIdx.x * kGvWarps + ((int)threadIdx.x >> 5);
   const int nwarps = (int)gridDim.x * kGvWarps;
   const int ngroups = Kp / 16;                       // 16-code groups of a row
-  for (int n = warp_g; n < N; n += nwarps) {
-    const uint4* row = reinterpret_cast<const uint4*>(codes + (int64_t)n * Kp);
-    const float* srow = scales + (int64_t)n * nb;
+  for (int n0 = warp_g * R; n0 < N; n0 += nwarps * R) {
+    const int n = n0 + sub;
+    const bool live = n < N;
+    const uint4* row = reinterpret_cast<const uint4*>(codes + (int64_t)(live ? n : 0) * Kp);
+    const float* srow = scales + (int64_t)(live ? n : 0) * nb;
     float acc[kM];
 #pragma unroll
     for (int m = 0; m < kM; ++m) acc[m] = 0.f;
-    for (int g0 = 0; g0 < ngroups; g0 += 32 * kGvSteps) {
+    for (int g0 = 0; g0 < ngroups; g0 += G * kGvSteps) {
       uint4 v[kGvSteps];
 #pragma unroll
       for (int u = 0; u < kGvSteps; ++u) {
-        const int g = g0 + 32 * u + lane;
-        v[u] = g < ngroups ? ldg128_stream(row + g) : make_uint4(0u, 0u, 0u, 0u);
+        const int g = g0 + G * u + sl;
+        v[u] = (live && g < ngroups) ? ldg128_stream(row + g) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int u = 0; u < kGvSteps; ++u) {
-        const int g = g0 + 32 * u + lane;
-        if (g >= ngroups) continue;
+        const int g = g0 + G * u + sl;
+        if (!live || g >= ngroups) continue;
         const int k0 = 16 * g;
         if (k0 >= K) continue;   // padding codes are zero; x past K is not read
         float c[16];
@@ -123,13 +131,14 @@ w8_gemv_kernel(const int8_t* __restrict__ codes, const float* __restrict__ scale
         }
       }
     }
+    // sum over the G lanes of each row (G is a power of two: the xor partners
+    // stay inside the row's lane group)
 #pragma unroll
     for (int m = 0; m < kM; ++m) {
       if (m >= M) break;
       float a = acc[m];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      if (lane == 0) Y[(int64_t)m * ldy + n] = a;
+      for (int o = G >> 1; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if (sl == 0 && live) Y[(int64_t)m * ldy + n] = a;
     }
   }
 }
@@ -149,11 +158,19 @@ cudaError_t launch_w8_gemv(const int8_t* codes, const float* scales, int N, int 
                            int64_t ldx, int M, float* Y, int64_t ldy, cudaStream_t stream) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = std::max(1, std::min((N + kGvWarps - 1) / kGvWarps, 8 * sms));
   const int Kp = (int)w8_padded_k(K), nb = (int)w8_blocks(K);
-  if (M <= 1) w8_gemv_kernel<1><<<grid, kGvWarps * 32, 0, stream>>>(codes, scales, N, K, Kp, nb, X, ldx, Y, ldy, M);
-  else if (M <= 4) w8_gemv_kernel<4><<<grid, kGvWarps * 32, 0, stream>>>(codes, scales, N, K, Kp, nb, X, ldx, Y, ldy, M);
-  else w8_gemv_kernel<16><<<grid, kGvWarps * 32, 0, stream>>>(codes, scales, N, K, Kp, nb, X, ldx, Y, ldy, M);
+  // lanes per row: about kGvSteps groups each, at least 4 lanes, at most 32
+  int G = 32;
+  while (G > 4 && G * kGvSteps > Kp / 16) G >>= 1;
+  const int R = 32 / G;
+  const int rows_per_block = kGvWarps * R;
+  const int grid = std::max(1, std::min((N + rows_per_block - 1) / rows_per_block, 8 * sms));
+  if (M <= 1)
+    w8_gemv_kernel<1><<<grid, kGvWarps * 32, 0, stream>>>(codes, scales, N, K, Kp, nb, X, ldx, Y, ldy, M, G);
+  else if (M <= 4)
+    w8_gemv_kernel<4><<<grid, kGvWarps * 32, 0, stream>>>(codes, scales, N, K, Kp, nb, X, ldx, Y, ldy, M, G);
+  else
+    w8_gemv_kernel<16><<<grid, kGvWarps * 32, 0, stream>>>(codes, scales, N, K, Kp, nb, X, ldx, Y, ldy, M, G);
   return cudaGetLastError();
 }
 
