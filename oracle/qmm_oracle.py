@@ -606,11 +606,11 @@ def repack_q4k(buf, N: int, K: int, row_bytes: int | None = None):
 # Q8 tiles.  The section gives the two code layouts of a 32 x 256 tile:
 #   layout 0: code (r, k) at byte k*32 + r;
 #   layout 1: code (r, k) at byte (r/16)*4096 + (k/32)*512 + (k%32)*16 + r%16.
-# It gives no scale bytes ("npu/q4nx.h has the byte layouts"), so these are
+# It gives no scale bytes (it defers them to a header the pages do not hold), so these are
 # the library's own: each tile is 8704 bytes, the 8192 code bytes followed by
 # one bf16 scale per (row r, block g of 32 columns) at byte
-# 8192 + 2*(32 g + r); codes are int8 and w = code * scale (Q8 does not fit
-# q4_1's code + min form).  Tiles are row-major over the [N/32][K/256] grid,
+# 8192 + 2*(32 g + r); codes are int8 and w = code * scale (the section rules
+# out expressing Q8 as q4_1's code + min form).  Tiles are row-major over the [N/32][K/256] grid,
 # as for q4.  Quantiser (the pages give none; packB's rule per block with the
 # scale kept in bf16):
 #   s = bf16(fl(amax / 127)); q = clamp(rint_even(fl(x / s)), -127, 127);
