@@ -237,3 +237,31 @@ def test_q8_gemm_brute_force_tiny():
             for k in range(256):
                 acc += X[m, k] * (q[n, k] * s[n, k // 32])
             assert abs(y[m, n] - acc) <= 1e-12 * norm[m, n]
+
+
+def test_q8_quantiser_hand_worked_block():
+    """A block with amax 127 has scale bf16(127/127) = 1, so the codes are the
+    weights rounded half to even; amax 1.0 gives bf16(1/127) = 2^-7 * (1 + 2^-7)
+    (bits 0x3C01), worked out by hand."""
+    W = np.zeros((32, 256), dtype=np.float32)
+    W[0, :8] = [127.0, 2.5, 3.5, -2.5, 126.5, -126.5, 0.5, -0.5]
+    W[1, 32:35] = [1.0, -1.0, 0.5]
+    q, s = O.q8_quantize_blocks(W)
+    assert s[0, 0] == 1.0
+    assert q[0, :8].tolist() == [127, 2, 4, -2, 126, -126, 0, 0]
+    assert O.bf16_bits(s[1, 1]) == 0x3C01 and s[1, 1] == 2.0 ** -7 * (1 + 2.0 ** -7)
+    # 1 / s = 127.0077.. -> 127; 0.5 / s = 63.5039.. -> 64
+    assert q[1, 32:35].tolist() == [127, -127, 64]
+    assert s[2, 0] == 0 and not q[2].any()
+
+
+def test_q8_quantiser_against_torch():
+    """Scales from torch's bf16 rounding of fp32 amax/127, codes from torch's
+    half-to-even rounding of the fp32 quotient, clamped to +-127."""
+    W = I.q4_weights(25, 64, 512)
+    Wb = W.reshape(64, 16, 32)
+    st = (Wb.abs().amax(2) / 127).to(torch.bfloat16).float()
+    qt = torch.clamp(torch.round(Wb / st[:, :, None]), -127, 127)
+    q, s = O.q8_quantize_blocks(W.numpy())
+    assert np.array_equal(s, st.double().numpy())
+    assert np.array_equal(q.reshape(64, 16, 32), qt.numpy().astype(np.int64))
