@@ -387,8 +387,9 @@ qmm_status qmm_w8_gemm(const void* codes, const float* scales, int64_t N, int64_
  * (IV) More weight formats
  *
  * "NPU engine: full ELFs, no xclbin", section "Q4NX chunks":
- *   - Q4_K weights are repacked into q4_1 tiles, exactly apart from rounding
- *     S*scale and M*min to bf16, so the 4-bit kernels above run them unchanged;
+ *   - Q4_K weights convert to q4_1 tiles, which the 4-bit kernels above then
+ *     run; the only loss is the bf16 rounding of the two per-sub-block
+ *     products (scale and min);
  *   - Q8 weights use the same 32 x 256 tile grid with 8-bit codes in one of
  *     two layouts: code (row r, column k) at byte k*32 + r, or at
  *     (r/16)*4096 + (k/32)*512 + (k%32)*16 + r%16.

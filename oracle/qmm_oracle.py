@@ -36,7 +36,8 @@ Sources (page title, section)
   the work": the ids of MUL_MAT_ID are a strided view, and down-projection
   experts read a per-slot src1 column i + t*n_expert_used.
 * NPU engine: full ELFs, no xclbin -- "Q4NX chunks": Q4_K weights are
-  repacked into q4_1 exactly apart from rounding S*scale and M*min to bf16;
+  converted to q4_1, losing only the bf16 rounding of the two per-sub-block
+  products (super-block scale times scale code, and the same for the min);
   Q8 tiles store code (r, k) at byte k*32 + r or at
   (r/16)*4096 + (k/32)*512 + (k%32)*16 + r%16.
 

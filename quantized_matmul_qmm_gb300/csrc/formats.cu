@@ -1,9 +1,10 @@
 // Two more weight formats ("NPU engine: full ELFs, no xclbin", section "Q4NX
 // chunks").
 //
-// Q4_K -> q4_1.  The section repacks Q4_K into q4_1 so that the kernels that
-// read q4_1 run Q4_K weights unchanged, exactly apart from rounding S*scale
-// and M*min to bf16.  A Q4_K super-block (GGML's published k-quant layout)
+// Q4_K -> q4_1.  The section converts Q4_K weights to q4_1 so that q4_1
+// kernels can use them; the only loss is the bf16 rounding of the two
+// per-sub-block products (super-block scale times scale code, super-block
+// min scale times min code).  A Q4_K super-block (GGML's published k-quant layout)
 // covers 256 weights of one row in 144 bytes: fp16 d and dmin, twelve bytes
 // of 6-bit scale and min codes for the eight 32-weight sub-blocks, and 128
 // bytes of 4-bit codes (byte 32c + l: weight 64c + l in the low nibble,
