@@ -414,7 +414,7 @@ def run_gemv_streams(hp, q, args, dev, stream):
 
 
 def run_w8(q, I, args, dev, stream, status, flush_l2):
-    """W8A16 (int8 weights, one fp32 scale per row and 1,024 weights, bf16
+    """W8A16 (int8 weights, an fp32 scale for every 1,024 weights of a row, bf16
     activations), timed apart from the step:
       * lm_head M=1 decode GEMV, back-to-back launches over rotating copies of
         the codes totalling >= 4x the L2 size (as for the q4 GEMV);
@@ -719,7 +719,7 @@ def main():
                  "single_call": {"weight_GBs": world * lm["weight_GBs"], "frac_hbm": lm["GBs"] / hbm_peak,
                                  "us": lm["us"], "note": "one launch timed alone after an L2 flush"}},
         "kernels": kern,
-        "w8a16": {"note": "int8 weights with one fp32 scale per row and 1,024 weights, bf16 activations; "
+        "w8a16": {"note": "int8 weights with an fp32 scale for every 1,024 weights of a row, bf16 activations; "
                           "timed apart from the step (median, L2 flushed before each single call)",
                   **w8},
         "int8_axis_zp": {"note": "per-axis zero points: the exact GEMM to int32 in the workspace, row sums, "

@@ -157,7 +157,7 @@ qmm_status qmm_int8_gemm_axis_zp_workspace_size(int64_t M, int64_t K, int64_t N,
 
 /* qmm_int8_gemm with per-axis zero points: one per activation row and one per
  * weight column ("The ONNX pack...", "What works today": the asymmetric
- * corrections are per-tensor or per-axis along the same axes as the scales,
+ * corrections come per tensor, or per row and per column wherever the scales are,
  * exact in integers):
  *     Y[m,n] = sum_k (A[m,k] - zA[m]) (B[k,n] - zB[n])
  *            = S - zA'[m] colSum[n] - zB'[n] (rowSum[m] - K zA'[m])
@@ -329,9 +329,9 @@ qmm_status qmm_q4_gemm_id_noalloc(const void* tiles, int64_t n_expert, int64_t N
  * (III) W8A16: int8 weights with block scales, bf16 activations
  *
  * "llama.cpp-xdna -- CPU, iGPU and XDNA1 NPU on AMD Ryzen APUs", sections
- * "The NPU worker" and "Running": the GGML_XDNA_NPU_W8 mode keeps the weights
- * as int8 with one scale per row and 1,024 weights, forms the partial sums
- * per block of inputs, and applies the block scales to them.
+ * "The NPU worker" and "Running": in the GGML_XDNA_NPU_W8 mode each
+ * 1,024-weight block of a row is int8 with its own scale, and that scale
+ * multiplies the block's partial sum.
  *
  * Layout (this library's own; the page gives the block size, not the bytes):
  *   codes   int8 [N][Kp], Kp = K rounded up to 64, row n = output n, zeros in

@@ -158,8 +158,8 @@ def int8_gemm_y_axis(A, a_type, zA_rows, B, b_type, zB_cols):
     weight column (zB_cols [N]), each in its operand's own domain.
 
     "The ONNX pack: weights to Q4NX, matmuls to our kernels, no VitisAI",
-    "What works today": the asymmetric corrections are per-tensor or per-axis
-    along the same axes as the scales (row zero points beside row scales,
+    "What works today": the asymmetric corrections come per tensor or per
+    axis, laid out like the scales (row zero points beside row scales,
     column zero points beside column scales), exact in integers:
 
         Y[m,n] = S - zA'[m] colSum[n] - zB'[n] (rowSum[m] - K zA'[m])
@@ -484,13 +484,12 @@ def normalized_error(y_test, y_ref, norm):
 
 
 # ----------------------------------------------------------------------------
-# W8A16: int8 weights with one scale per row and 1,024 weights, bf16 activations
+# W8A16: int8 weights with a scale for every 1,024 weights of a row, bf16 activations
 # ----------------------------------------------------------------------------
 # "llama.cpp-xdna -- CPU, iGPU and XDNA1 NPU on AMD Ryzen APUs", sections "The
-# NPU worker" and "Running" (GGML_XDNA_NPU_W8): weights as int8 with one scale
-# per row and 1,024 weights, activations bf16;
-# partial sums are formed per block of inputs and the int8 scales applied to
-# them.  The per-block quantisation rule is packB's (amax/127, round half to
+# NPU worker" and "Running" (GGML_XDNA_NPU_W8): each 1,024-weight block of a
+# row is int8 with its own scale, activations are bf16, and each scale
+# multiplies its block's partial sum.  The per-block quantisation rule is packB's (amax/127, round half to
 # even, clamp to +-127, zero block -> scale 0): the pages give the granularity,
 # not the rounding.
 

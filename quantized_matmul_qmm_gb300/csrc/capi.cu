@@ -238,7 +238,7 @@ qmm_status qmm_quantize_act_int8(const void* X, qmm_dtype x_type, int64_t M, int
 }
 
 // ---------------------------------------------------------------------------
-// W8A16: int8 weights, one fp32 scale per row and 1,024 weights
+// W8A16: int8 weights, an fp32 scale for every 1,024 weights of a row
 // ---------------------------------------------------------------------------
 
 qmm_status qmm_pack_w8_size(int64_t N, int64_t K, size_t* code_bytes, size_t* scale_bytes) {

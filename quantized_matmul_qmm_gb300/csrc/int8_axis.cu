@@ -1,8 +1,8 @@
 // Per-axis zero points for the int8 GEMM: one zero point per activation row
 // (zA[m]) and one per weight column (zB[n]) ("The ONNX pack: weights to Q4NX,
 // matmuls to our kernels, no VitisAI", section "What works today": the
-// asymmetric corrections are per-tensor or per-axis along the same axes as the
-// scales, exact in integers).
+// asymmetric corrections come per tensor or per axis, laid out like the
+// scales, and are exact in integers).
 //
 //   Y[m,n] = S'[m,n] - zA'[m] colSum'[n] - zB'[n] (rowSum'[m] - K zA'[m])
 //

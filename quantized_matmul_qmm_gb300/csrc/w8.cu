@@ -1,8 +1,8 @@
-// W8A16: int8 weights with one scale per row and 1,024 weights, bf16
+// W8A16: int8 weights with a scale for every 1,024 weights of a row, bf16
 // activations ("llama.cpp-xdna -- CPU, iGPU and XDNA1 NPU on AMD Ryzen
-// APUs", sections "The NPU worker" and "Running": GGML_XDNA_NPU_W8 keeps the
-// weights as int8 with one scale per row and 1,024 weights; partial sums are
-// formed per block of inputs and the int8 scales applied to them).
+// APUs", sections "The NPU worker" and "Running": in the GGML_XDNA_NPU_W8
+// mode each 1,024-weight block of a row is int8 with its own scale, and the
+// scale multiplies that block's partial sum).
 //
 // Pack: per (row n, block b of 1,024 k), packB's rule: s = fl(amax / 127),
 // q = clamp(rint_even(fl(w / s)), -127, 127), 0 where s == 0.  Codes are

@@ -203,7 +203,7 @@ def test_normalized_error():
 
 
 # ---------------------------------------------------------------------------
-# W8A16 (int8 weights, one scale per row and 1,024 weights)
+# W8A16 (int8 weights, a scale for every 1,024 weights of a row)
 # ---------------------------------------------------------------------------
 
 def test_w8_blocks_are_packb_columns():
