@@ -449,8 +449,9 @@ qmm_status qmm_q8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* w
  * workspace / ws_bytes  qmm_q8_gemm_workspace_size bytes, 256-byte aligned
  *        (NULL when that size is 0), rewritten by the call.
  * M <= 16 runs the decode GEMV, which forms every weight exactly
- * (code * scale in fp32): max |y - y_exact| <= 2e-5 * sum_k |x||w| at the
- * supported K.  Larger M decodes the tiles to bf16 weights (one rounding,
+ * (code * scale in fp32), so only fp32 summation rounds: about
+ * (K/256 + 14) * 2^-24 * sum_k |x||w| at worst, within 2e-5 * sum_k |x||w|
+ * for K <= 65536.  Larger M decodes the tiles to bf16 weights (one rounding,
  * <= 2^-8 relative per weight) for the tensor-core GEMM, within the 4-bit
  * path's bound max |y - y_exact| <= 2e-3 * sum_k |x||w| for inputs whose
  * rounding errors do not all share one sign.
