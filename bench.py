@@ -165,6 +165,7 @@ class HotPath:
         # q4 dense weights (lm_head + 7 projections), M=1 and M=512
         shapes = [I.QWEN3_06B_LM_HEAD] + list(I.QWEN3_06B_PROJ)
         self.q4 = []
+        self.q4_ws = {}
         for name, K, N in shapes:
             W = I.q4_weights(9 * 1000 + N % 997 + K, N, K).to(dev)
             tiles = q.pack_q4(W)
@@ -174,13 +175,15 @@ class HotPath:
             y1 = torch.empty((1, N), dtype=torch.float32, device=dev)
             y512 = torch.empty((512, N), dtype=torch.float32, device=dev)
             self.q4.append((name, K, N, tiles, x1, x512, y1, y512))
+            self.q4_ws[name] = torch.empty(max(256, q.q4_gemm_workspace_size(512, K, N)), dtype=torch.uint8,
+                                           device=dev)
         for name, K, N, tiles, x1, _, y1, _ in self.q4:
             wb = tiles.numel()
             self.calls.append((f"q4_gemv_{name}_m1", self._q4(tiles, N, K, x1, y1), 1,
                                {"weight_bytes": wb, "bytes": wb + 2 * K + 4 * N, "flops": 2 * N * K}))
         for name, K, N, tiles, _, x512, _, y512 in self.q4:
             wb = tiles.numel()
-            self.calls.append((f"q4_gemm_{name}_m512", self._q4(tiles, N, K, x512, y512),
+            self.calls.append((f"q4_gemm_{name}_m512", self._q4(tiles, N, K, x512, y512, self.q4_ws[name]),
                                self.q4_launches(512),
                                {"flops": 2 * 512 * N * K, "weight_bytes": wb,
                                 "bytes": wb + 2 * 512 * K + 4 * 512 * N}))
@@ -209,11 +212,12 @@ class HotPath:
         return 2 if self.q.int8_gemm_workspace_size(c.M, c.K, c.N) > 0 else 1
 
     def moe_launches(self, m):
-        # routing grid, packing grid, then the grouped kernel
+        # routing grid, packing grid (f16 rows and their scales), then the grouped kernel
         return 3
 
     def q4_launches(self, M):
-        return 1
+        # decode GEMV: one kernel; tensor-core route: f16 activation rows, then the GEMM
+        return 1 if M <= 16 else 2
 
     def run_int8(self):
         c = self.int8
@@ -221,8 +225,8 @@ class HotPath:
                          "s8", bias=self.bias, s_x=self.s_x, s_w=self.s_w, s_y=c.s_y, zp_y=c.zp_y,
                          out=self.out8, workspace=self.ws8, dev_status=self.status)
 
-    def _q4(self, tiles, N, K, X, Y):
-        return lambda: self.q.q4_gemm(tiles, N, K, X, Y=Y, dev_status=self.status)
+    def _q4(self, tiles, N, K, X, Y, ws=None):
+        return lambda: self.q.q4_gemm(tiles, N, K, X, Y=Y, workspace=ws, dev_status=self.status)
 
     def _moe(self, m, tiles, X, ids, Y, ws):
         return lambda: self.q.q4_gemm_id(tiles, m.n_expert, m.N, m.K, X, ids, m.ld_ids, m.n_used,
@@ -339,6 +343,11 @@ def run_ours(args, rank, world, dev):
     if int(hp.status.item()) != 0:
         raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
     streams["q8"] = run_q8(q, I, args, dev, stream, hp.status, flush_l2)
+    if int(hp.status.item()) != 0:
+        raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
+    streams["int8_small"] = run_int8_small(q, I, args, dev, stream, hp.status, flush_l2)
+    streams["q4_small_batch"] = run_q4_small_batch(q, hp, args, dev, stream, hp.status)
+    streams["probe"] = run_probe(q, args, dev, stream, hp.status)
     if int(hp.status.item()) != 0:
         raise RuntimeError(f"device status {q.status_string(int(hp.status.item()))}")
     return hp, per_call, total, clk, e2e_ms, streams
@@ -491,8 +500,9 @@ def run_q8(q, I, args, dev, stream, status, flush_l2):
     apart from the step like the W8A16 path:
       * lm_head M=1 decode GEMV in each layout, back-to-back launches over
         rotating copies of the tiles totalling >= 4x the L2 size;
-      * lm_head M=512 through the tensor-core route (tiles decoded to bf16,
-        then the pair GEMM), one call after an L2 flush.
+      * lm_head M=512 through the tensor-core route (tiles decoded to f16,
+        activation rows to scaled f16, then the pair GEMM), one call after an
+        L2 flush.
     Medians over `args.steps` timed repetitions after `args.warmup`."""
     import math
     import torch
@@ -538,11 +548,176 @@ def run_q8(q, I, args, dev, stream, status, flush_l2):
             y512 = torch.empty((512, N), dtype=torch.float32, device=dev)
             ws = torch.empty(q.q8_gemm_workspace_size(512, K, N), dtype=torch.uint8, device=dev)
             us = timed(lambda: q.q8_gemm(tiles, layout, N, K, x512, Y=y512, workspace=ws, dev_status=status), True)
-            res["q8_gemm_lm_head_m512"] = {"us": us, "launches": 2,
+            res["q8_gemm_lm_head_m512"] = {"us": us, "launches": 3,
                                            "TFLOPS": 2 * 512 * N * K / (us * 1e-6) / 1e12, "weight_bytes": wbytes}
             del x512, y512, ws
         del tiles
     del W
+    torch.cuda.synchronize()
+    return res
+
+
+def _timer(args, stream, flush_l2):
+    """Two ways to time a call: `alone(fn)` flushes L2 before each call and
+    brackets it with CUDA events on the launching stream; `passes(fn, n)` runs
+    a pass of n back-to-back launches after a ~2 ms host lead and divides.
+    Both return the median over `args.steps` timed repetitions after
+    `args.warmup`, in microseconds."""
+    import torch
+
+    def run(fn, flush):
+        out = []
+        for i in range(args.warmup + args.steps):
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
+            if flush:
+                flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= args.warmup:
+                out.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) * 1e3 for a, b in out)
+
+    return (lambda fn: run(fn, True)), (lambda fn, n: run(fn, False) / n)
+
+
+def run_probe(q, args, dev, stream, status):
+    """Load-only HBM read bandwidth (qmm_probe_hbm_read) over rotating 128 MiB
+    buffers totalling >= 4x L2, back to back, in both read styles the GEMVs
+    use.  The larger of the two is the load-only roofline."""
+    import math
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nb = 128 << 20
+    R = max(4, math.ceil(4 * l2 / nb))
+    bufs = [torch.ones(nb, dtype=torch.uint8, device=dev) for _ in range(R)]
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    _, passes = _timer(args, stream, None)
+    res = {}
+    for mode, name in ((0, "ld128"), (1, "bulk")):
+        us = passes(lambda: [q.probe_hbm_read(b, mode, sink, status) for b in bufs], R)
+        res[name] = {"us_per_buffer": us, "GBs": nb / (us * 1e-6) / 1e9}
+    res["buffers"] = R
+    res["buffer_bytes"] = nb
+    res["GBs"] = max(res["ld128"]["GBs"], res["bulk"]["GBs"])
+    del bufs
+    torch.cuda.synchronize()
+    return res
+
+
+def run_int8_small(q, I, args, dev, stream, status, flush_l2):
+    """The two small int8 workloads, timed apart from the step:
+      * M=16 K=N=1024 (uint8 x int8, zA = 128 +- 8): int32 out and fp32 out,
+        each one call after an L2 flush, and back to back over rotating copies
+        of the packed weights (>= 4x L2, every launch reads them from HBM);
+      * the seven Qwen3-0.6B projections at M=32 (int8 per-tensor activations x
+        packB weights, fp32 out): each alone after a flush, and the set of
+        seven launches captured in one CUDA graph over rotating weight copies;
+      * a mid-size M=128 K=N=4608 GEMM (the step's operands, first 128 rows),
+        one call after a flush.
+    TOPS = 2MNK / time; weight GB/s = packed weight bytes / time."""
+    import math
+    import torch
+    alone, passes = _timer(args, stream, flush_l2)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    res = {}
+    c = I.int8_gemm_small()
+    A = c.A.to(dev)
+    packed, _, col_sum = q.pack_b_int8(c.B.to(dev), c.b_type)
+    s_w = c.s_w.to(dev)
+    wb = packed.numel()
+    outs = {"s32": torch.empty((c.M, c.N), dtype=torch.int32, device=dev),
+            "f32": torch.empty((c.M, c.N), dtype=torch.float32, device=dev)}
+    R = max(2, math.ceil(4 * l2 / wb))
+    copies = [packed] + [packed.clone() for _ in range(R - 1)]
+    for ot in ("s32", "f32"):
+        sw = s_w if ot == "f32" else None
+        call = lambda pk=packed, ot=ot, sw=sw: q.int8_gemm(A, c.a_type, c.zA, pk, col_sum, c.N, c.b_type, c.zB, ot,
+                                                          s_w=sw, out=outs[ot], dev_status=status)
+        us = alone(call)
+        us_s = passes(lambda: [call(pk) for pk in copies], R)
+        ops = 2.0 * c.M * c.N * c.K
+        res[f"int8_m16_k1024_n1024_{ot}"] = {
+            "us": us, "TOPS": ops / (us * 1e-6) / 1e12, "weight_GBs": wb / (us * 1e-6) / 1e9, "launches": 1,
+            "stream": {"us": us_s, "copies": R, "TOPS": ops / (us_s * 1e-6) / 1e12,
+                       "weight_GBs": wb / (us_s * 1e-6) / 1e9}}
+    del copies
+    # the projection set at M = 32
+    projs = []
+    for idx in range(7):
+        cc = I.int8_qwen_projection(idx)
+        pk, cs, cols = q.pack_b_int8(cc.B.to(dev), cc.b_type)
+        projs.append((cc, cc.A.to(dev), pk, cs, cols, torch.tensor([cc.s_x], dtype=torch.float32, device=dev),
+                      torch.empty((cc.M, cc.N), dtype=torch.float32, device=dev)))
+    set_bytes = sum(p[2].numel() for p in projs)
+    set_ops = sum(2.0 * p[0].M * p[0].N * p[0].K for p in projs)
+    shapes = {}
+    for cc, Ad, pk, cs, cols, sx, Y in projs:
+        call = lambda cc=cc, Ad=Ad, pk=pk, cs=cs, cols=cols, sx=sx, Y=Y: q.int8_gemm(
+            Ad, cc.a_type, cc.zA, pk, cols, cc.N, cc.b_type, cc.zB, "f32", s_x=sx, s_w=cs, out=Y, dev_status=status)
+        us = alone(call)
+        shapes[cc.name] = {"us": us, "K": cc.K, "N": cc.N, "TOPS": 2.0 * cc.M * cc.N * cc.K / (us * 1e-6) / 1e12,
+                           "weight_GBs": pk.numel() / (us * 1e-6) / 1e9}
+    C = max(2, math.ceil(4 * l2 / set_bytes))
+    pcopies = [[p[2] if k == 0 else p[2].clone() for p in projs] for k in range(C)]
+
+    def set_pass():
+        for cp in pcopies:
+            for pk, (cc, Ad, _, cs, cols, sx, Y) in zip(cp, projs):
+                q.int8_gemm(Ad, cc.a_type, cc.zA, pk, cols, cc.N, cc.b_type, cc.zB, "f32", s_x=sx, s_w=cs, out=Y,
+                            dev_status=status)
+
+    set_pass()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        set_pass()
+    torch.cuda.synchronize()
+    us_set = passes(graph.replay, C)
+    res["int8_qwen3_projections_m32"] = {
+        "per_shape": shapes,
+        "graph": {"us_per_set": us_set, "copies": C, "launches_per_set": 7, "weight_bytes": set_bytes,
+                  "TOPS": set_ops / (us_set * 1e-6) / 1e12, "weight_GBs": set_bytes / (us_set * 1e-6) / 1e9}}
+    del graph, pcopies
+    # mid-size M
+    cl = I.int8_gemm_large()
+    M = 128
+    A128 = cl.A[:M].to(dev)
+    pkl, _, csl = q.pack_b_int8(cl.B.to(dev), cl.b_type)
+    out = torch.empty((M, cl.N), dtype=torch.int8, device=dev)
+    bias, swl = cl.bias.to(dev), cl.s_w.to(dev)
+    sxl = torch.tensor([cl.s_x], dtype=torch.float32, device=dev)
+    us = alone(lambda: q.int8_gemm(A128, cl.a_type, cl.zA, pkl, csl, cl.N, cl.b_type, cl.zB, "s8", bias=bias,
+                                   s_x=sxl, s_w=swl, s_y=cl.s_y, zp_y=cl.zp_y, out=out, dev_status=status))
+    res["int8_m128_k4608_n4608"] = {"us": us, "TOPS": 2.0 * M * cl.N * cl.K / (us * 1e-6) / 1e12,
+                                    "weight_GBs": pkl.numel() / (us * 1e-6) / 1e9, "launches": 1}
+    torch.cuda.synchronize()
+    return res
+
+
+def run_q4_small_batch(q, hp, args, dev, stream, status):
+    """q4 decode GEMV at M = 2, 8, 16 (lm_head), back to back over rotating
+    weight copies totalling >= 4x L2, like the M = 1 measurement."""
+    import math
+    import torch
+    _, passes = _timer(args, stream, None)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    name, K, N, tiles, _, x512, _, _ = hp.q4[0]
+    R = max(2, math.ceil(4 * l2 / tiles.numel()))
+    copies = [tiles] + [tiles.clone() for _ in range(R - 1)]
+    res = {}
+    for M in (2, 8, 16):
+        X = x512[:M].contiguous()
+        Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        us = passes(lambda: [q.q4_gemm(t, N, K, X, Y=Y, dev_status=status) for t in copies], R)
+        wb = tiles.numel()
+        res[f"q4_gemv_lm_head_m{M}_stream"] = {"us": us, "copies": R, "weight_bytes": wb,
+                                               "weight_GBs": wb / (us * 1e-6) / 1e9,
+                                               "GBs": (wb + 2 * M * K + 4 * M * N) / (us * 1e-6) / 1e9,
+                                               "TFLOPS": 2.0 * M * N * K / (us * 1e-6) / 1e12}
+    del copies
     torch.cuda.synchronize()
     return res
 
@@ -576,19 +751,91 @@ def run_axis_zp(q, hp, args, dev, stream, status, flush_l2):
                                         "shape": f"M={c.M} K={c.K} N={c.N}, zero point per row of A and per column of B"}}
 
 
-def cpu_int8_sample(rows: int):
-    """The oracle (as it stands) on `rows` rows of the M=4096 K=N=4608 GEMM."""
+def _cpu_int8_rows(rows):
+    """The oracle (as it stands) on the given rows of the M=4096 K=N=4608 GEMM;
+    returns (int ops, seconds of oracle work)."""
     import numpy as np
     import oracle.qmm_oracle as O
     from quantized_matmul_qmm_gb300 import inputs as I
     c = I.int8_gemm_large()
-    A = c.A[:rows].numpy().astype(np.int64)
+    A = c.A[rows[0]:rows[1]].numpy().astype(np.int64)
     B = c.B.numpy().astype(np.int64)
     t0 = time.perf_counter()
     r = O.int8_gemm_y(A, c.a_type, c.zA, B, c.b_type, c.zB)
     O.int8_epilogue(r["Y"], "s8", c.bias.numpy(), c.s_x, c.s_w.numpy(), c.s_y, c.zp_y)
-    dt = time.perf_counter() - t0
-    return 2.0 * rows * c.N * c.K / dt / 1e12, dt
+    return 2.0 * (rows[1] - rows[0]) * c.N * c.K, time.perf_counter() - t0
+
+
+def _cpu_q4_rows(rows):
+    """The oracle's q4 product for `rows` output rows of an lm_head-shaped
+    weight (K=1024) at M=1; returns (weight bytes covered, seconds)."""
+    import numpy as np
+    import oracle.qmm_oracle as O
+    from quantized_matmul_qmm_gb300 import inputs as I
+    name, K, N = I.QWEN3_06B_LM_HEAD
+    W = I.q4_weights(9 * 1000 + N % 997 + K, rows, K).numpy()   # a rows x K slice of the same distribution
+    x = I.q4_activations(9 * 7919 + 1, 1, K).float().double().numpy()
+    tiles = O.pack_q4(W)
+    t0 = time.perf_counter()
+    O.q4_gemm(tiles, rows, K, x)
+    return tiles.size, time.perf_counter() - t0
+
+
+def cpu_host():
+    """Host cores and CPU model of this machine."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return cores, model
+
+
+def cpu_baseline(rows_per_core: int, single_rows: int):
+    """The CPU oracle as it stands, on this machine's host cores: one thread on
+    `single_rows` rows of the int8 GEMM, then one process per core (spawned,
+    so no CUDA state is inherited) on `rows_per_core` rows each, timed by the
+    wall clock around the whole batch; and the q4 lm_head product on a sample
+    of 4,096 output rows per core the same way."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+    cores, model = cpu_host()
+    ops1, dt1 = _cpu_int8_rows((0, single_rows))
+    ctx = mp.get_context("spawn")
+    with ProcessPoolExecutor(max_workers=cores, mp_context=ctx) as ex:
+        # a first round warms the workers (imports, input generation)
+        list(ex.map(_cpu_int8_rows, [(0, 1)] * cores))
+        t0 = time.perf_counter()
+        res = list(ex.map(_cpu_int8_rows, [(i * rows_per_core, (i + 1) * rows_per_core) for i in range(cores)]))
+        wall = time.perf_counter() - t0
+        ops = sum(r[0] for r in res)
+        list(ex.map(_cpu_q4_rows, [32] * cores))
+        t0 = time.perf_counter()
+        q4 = list(ex.map(_cpu_q4_rows, [4096] * cores))
+        q4_wall = time.perf_counter() - t0
+    q4_bytes = sum(r[0] for r in q4)
+    return {"value": ops / wall / 1e12, "unit": "TOPS", "cores": cores, "kind": "oracle",
+            "cpu_model": model,
+            "sample": f"{rows_per_core} rows of the M=4096 K=N=4608 int8 GEMM per core, one process per core, "
+                      f"{cores * rows_per_core} rows in {wall:.1f} s wall (numpy int64)",
+            "single_thread": {"value": ops1 / dt1 / 1e12, "unit": "TOPS", "cores": 1,
+                              "sample": f"{single_rows} rows in {dt1:.1f} s"},
+            "q4_gemv": {"value": q4_bytes / q4_wall / 1e9, "unit": "GB/s of q4 weights", "cores": cores,
+                        "sample": f"lm_head-shaped q4 product at M=1 (K=1024), 4,096 output rows per core, "
+                                  f"{cores * 4096} rows in {q4_wall:.1f} s wall (numpy fp64 decode-then-dense)"}}
+
+
+def run_config(world):
+    """The workload description both arms print."""
+    return {"workload": WORKLOAD, "int8": f"u8xs8 M={INT8_M} K={INT8_K} N={INT8_N} int8 out",
+            "l2": "flushed before every timed call (256 MiB write, then 256 MiB read); decode GEMVs "
+                  "back to back over rotating weight copies >= 4x L2",
+            "parallelism": f"replicas x{world}"}
 
 
 def main():
@@ -597,7 +844,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["qmm", "reference"], default="qmm")
-    ap.add_argument("--cpu-rows", type=int, default=8, help="rows of the oracle's CPU sample")
+    ap.add_argument("--cpu-rows", type=int, default=2, help="rows per host core of the oracle's CPU sample")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -606,25 +853,34 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.impl == "reference":
-        # the CPU oracle as the reference arm: rank 0 alone, a bounded sample per step
+        # the CPU oracle as the reference arm: rank 0 alone; each step is a
+        # bounded sample of the int8 GEMM, one row per host core, one process
+        # per core
         if rank != 0:
             return
-        rows = 2
-        for _ in range(args.warmup):
-            cpu_int8_sample(rows)
-        tops, secs = [], 0.0
-        for _ in range(args.steps):
-            v, dt = cpu_int8_sample(rows)
-            tops.append(v)
-            secs += dt
-        value = args.steps * 2.0 * rows * INT8_N * INT8_K / secs / 1e12
+        import multiprocessing as mp
+        from concurrent.futures import ProcessPoolExecutor
+        cores, model = cpu_host()
+        with ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")) as ex:
+            for _ in range(args.warmup):
+                list(ex.map(_cpu_int8_rows, [(i, i + 1) for i in range(cores)]))
+            ops, secs = 0.0, 0.0
+            for st in range(args.steps):
+                t0 = time.perf_counter()
+                res = list(ex.map(_cpu_int8_rows, [((st * cores + i) % INT8_M, (st * cores + i) % INT8_M + 1)
+                                                   for i in range(cores)]))
+                secs += time.perf_counter() - t0
+                ops += sum(r[0] for r in res)
+        value = ops / secs / 1e12
+        sample = (f"{cores} of the 4096 rows of the M=4096 K=N=4608 int8 GEMM per step, one row per host core "
+                  f"(one process each, numpy int64)")
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
-                "config": {"workload": WORKLOAD, "reference": "CPU oracle (numpy int64/fp64)"},
-                "cpu_baseline": {"value": value, "unit": "TOPS", "cores": 1, "kind": "oracle",
-                                 "sample": f"{rows} of 4096 rows of the int8 GEMM per step"},
+                "config": run_config(world),
+                "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle",
+                                 "cpu_model": model, "sample": sample},
                 "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -659,6 +915,7 @@ def main():
     value = replicas_rate(i8["TOPS"], world)
     lm = kern["q4_gemv_lm_head_m1"]
     st_lm, st_ps = streams["lm_head"], streams["projection_set"]
+    probe = streams["probe"]
     roof = {"bound": "tensor", "achieved": i8["TOPS"], "peak": tensor_peak, "unit": "TFLOP/s",
             "frac": i8["TOPS"] / tensor_peak, "traffic": traffic.get("int8_gemm_m4096"),
             "kernel": "int8_gemm_m4096",
@@ -698,24 +955,43 @@ def main():
         else:
             rooflines[name] = {"bound": "tensor", "achieved": d["TFLOPS"], "peak": tensor_peak, "unit": "TFLOP/s",
                                "frac": d["TFLOPS"] / tensor_peak, "traffic": traffic.get(name)}
+    for name, d in rooflines.items():
+        if d["bound"] == "hbm":
+            d["peak_probe"] = probe["GBs"]
+            d["frac_probe"] = d["achieved"] / probe["GBs"]
+    small = streams["int8_small"]
+    for name in ("int8_m16_k1024_n1024_s32", "int8_m16_k1024_n1024_f32"):
+        d = small[name]["stream"]
+        rooflines[name + "_stream"] = {"bound": "hbm", "achieved": d["weight_GBs"], "peak": hbm_peak, "unit": "GB/s",
+                                       "frac": d["weight_GBs"] / hbm_peak, "peak_probe": probe["GBs"],
+                                       "frac_probe": d["weight_GBs"] / probe["GBs"], "traffic": None,
+                                       "note": "weight bytes only; back to back over rotating copies"}
+    pg = small["int8_qwen3_projections_m32"]["graph"]
+    rooflines["int8_qwen3_projections_m32_graph"] = {
+        "bound": "hbm", "achieved": pg["weight_GBs"], "peak": hbm_peak, "unit": "GB/s",
+        "frac": pg["weight_GBs"] / hbm_peak, "peak_probe": probe["GBs"], "frac_probe": pg["weight_GBs"] / probe["GBs"],
+        "traffic": None, "note": "weight bytes only; 7 launches per set in one CUDA graph, rotating copies"}
+    for name, d in streams["q4_small_batch"].items():
+        rooflines[name] = {"bound": "hbm", "achieved": d["GBs"], "peak": hbm_peak, "unit": "GB/s",
+                           "frac": d["GBs"] / hbm_peak, "peak_probe": probe["GBs"],
+                           "frac_probe": d["GBs"] / probe["GBs"], "traffic": None}
     c = hp.int8
     launches = sum(l for (_, _, l, _) in hp.calls) * args.steps
     line = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "int8": f"u8xs8 M={c.M} K={c.K} N={c.N} int8 out",
-                   "l2": "flushed before every timed call (256 MiB write, then 256 MiB read)",
-                   "parallelism": f"replicas x{world}"},
+        "config": run_config(world),
         "roofline": roof,
         "rooflines": rooflines,
         "gemv": {"value": replicas_rate(st_lm["weight_GBs"], world), "unit": "GB/s", "kernel": "q4_gemv_lm_head_m1",
                  "frac_hbm": st_lm["GBs"] / hbm_peak, "peak_source": peak_kind,
+                 "frac_probe": st_lm["GBs"] / probe["GBs"], "probe_GBs": probe["GBs"],
                  "method": f"lm_head M=1, back-to-back launches over {st_lm['copies']} rotating weight copies "
                            f"(>= 4x the {streams['l2_bytes'] >> 20} MiB L2), median over passes",
                  "projection_set_graph": {"weight_GBs": world * st_ps["weight_GBs"],
-                                          "frac_hbm": st_ps["GBs"] / hbm_peak, "us_per_set": st_ps["us"],
-                                          "copies": st_ps["copies"]},
+                                          "frac_hbm": st_ps["GBs"] / hbm_peak, "frac_probe": st_ps["GBs"] / probe["GBs"],
+                                          "us_per_set": st_ps["us"], "copies": st_ps["copies"]},
                  "single_call": {"weight_GBs": world * lm["weight_GBs"], "frac_hbm": lm["GBs"] / hbm_peak,
                                  "us": lm["us"], "note": "one launch timed alone after an L2 flush"}},
         "kernels": kern,
@@ -727,16 +1003,19 @@ def main():
         "q8": {"note": "8-bit tiles (bf16 scale per row and 32 columns) in the chunk format's two code layouts; "
                        "timed apart from the step (median, L2 flushed before each single call)",
                **q8},
+        "hbm_probe": {"note": "load-only reads of rotating 128 MiB buffers (>= 4x L2), back to back; the larger "
+                              "of the two read styles is the load-only roofline (peak_probe)", **probe},
+        "int8_small": {"note": "the M=16 and M=32 int8 workloads and a mid-size M=128 GEMM, timed apart from the step",
+                       **small},
+        "q4_small_batch": {"note": "q4 decode GEMV at M = 2, 8, 16 on lm_head, back to back over rotating weight copies",
+                           **streams["q4_small_batch"]},
         "e2e": {"value": replicas_rate(2.0 * c.M * c.N * c.K / (e2e_ms * 1e-3) / 1e12, world), "unit": "TOPS",
                 "h2d_bytes_per_step": c.M * c.K, "d2h_bytes_per_step": c.M * c.N},
         "gpu_launches": launches,
         "clocks": clk,
     }
     if rank == 0 and world == 1:
-        v, dt = cpu_int8_sample(args.cpu_rows)
-        line["cpu_baseline"] = {"value": v, "unit": "TOPS", "cores": 1, "kind": "oracle",
-                                "sample": f"{args.cpu_rows} of 4096 rows of the int8 GEMM "
-                                          f"({dt:.1f} s, numpy int64 matmul, one thread)"}
+        line["cpu_baseline"] = cpu_baseline(args.cpu_rows, 4)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -28,9 +28,10 @@
  * - Errors found on the device go to `dev_status`, a device int32 that the
  *   caller sets to 0 (it may be NULL).  These are a bounded wait that ran out
  *   (QMM_ERR_TIMEOUT), an expert id outside [0, n_expert)
- *   (QMM_ERR_BAD_EXPERT_ID), and a per-axis zero point outside its operand's
- *   domain (QMM_ERR_INVALID_ARG).  The library only ever replaces a 0 there
- *   with an error code, so the caller reads it after synchronising.
+ *   (QMM_ERR_BAD_EXPERT_ID), a per-axis zero point outside its operand's
+ *   domain (QMM_ERR_INVALID_ARG), and a weight block that the f16 tensor-core
+ *   route cannot form (QMM_ERR_RANGE).  The library only ever replaces a 0
+ *   there with an error code, so the caller reads it after synchronising.
  * - Shapes the library has no kernel for return QMM_ERR_UNSUPPORTED.  There
  *   is no fallback path.
  */
@@ -53,7 +54,9 @@ typedef enum {
   QMM_ERR_CUDA = 4,            /* a CUDA runtime call failed (e.g. launch) */
   QMM_ERR_TIMEOUT = 5,         /* device: a bounded pipeline wait gave up */
   QMM_ERR_BAD_EXPERT_ID = 6,   /* device: an expert id was outside [0, n_expert) */
-  QMM_ERR_WORKSPACE = 7        /* workspace pointer NULL, misaligned or smaller than required */
+  QMM_ERR_WORKSPACE = 7,       /* workspace pointer NULL, misaligned or smaller than required */
+  QMM_ERR_RANGE = 8            /* device: a weight block beyond f16's range (|w| could pass 65504) on a
+                                  route that forms f16 weights; the results of that call are not valid */
 } qmm_status;
 
 typedef enum {
@@ -248,30 +251,49 @@ qmm_status qmm_pack_q4_size(int64_t N, int64_t K, size_t* tile_bytes);
 qmm_status qmm_pack_q4(const float* W, int64_t N, int64_t K, int64_t ldw, void* tiles,
                        size_t tile_bytes, cudaStream_t stream);
 
+/* Workspace of qmm_q4_gemm: 0 for M <= 16 (the decode GEMV), else the
+ * activations as f16 rows (M*K*2 bytes) and one fp32 scale per row, each
+ * rounded up to 256 bytes. */
+qmm_status qmm_q4_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes);
+
 /* Y[m][n] = sum_k X[m][k] * w[n][k] with fp32 accumulation.
  *
  * tiles  one N x K tile set (16-byte aligned).  N % 32 == 0, K % 256 == 0.
  * X      bf16 [M][K], row stride ldx elements (ldx >= K, ldx % 8 == 0, base
  *        16-byte aligned).
  * Y      fp32 [M][N], row stride ldy elements (ldy >= N).
- * Small M runs the decode GEMV kernel, larger M the tensor-core GEMM; both
- * compute the same function, within the accuracy bound
- * max |y - y_exact| <= 2e-3 * sum_k |x||w|.
+ * workspace / ws_bytes  qmm_q4_gemm_workspace_size bytes, 256-byte aligned
+ *        (NULL when that size is 0), rewritten by the call.
+ * Small M (<= 16) runs the decode GEMV, which never rounds a weight: only
+ * fp32 summation rounds, within 2e-5 * sum_k |x||w|.  Larger M runs the
+ * tensor-core GEMM on f16 operands: each weight is rounded once to f16
+ * (<= 2^-11 of itself), and each activation row is scaled by a power of two
+ * before its f16 conversion, which makes that conversion exact for every
+ * element within a factor 2^31 of the row's largest.  With every block's
+ * scale and min in f16's normal range (|s|, |m| >= 2^-14, or 0), each weight
+ * is within max(2^-11 |w|, 2^-25) of its exact value, so for every input
+ *     |y - y_exact| <= (2^-11 + K * 2^-23) * sum_k |x||w| + 2^-25 * sum' |x|,
+ * where sum' runs over the weights with |w| < 2^-14 (K * 2^-23 bounds the
+ * fp32 accumulation even if every addition truncates).  The first term is
+ * below 2e-3 * sum_k |x||w| for K <= 12,544.  A block whose scale or min is
+ * below 2^-14 adds at most 17 * 2^-25 * |x| per weight.  A block with
+ * |m| + 15 |s| > 65504 cannot be formed in f16: dev_status gets QMM_ERR_RANGE.
  */
 qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, int64_t M,
-                       int64_t ldx, float* Y, int64_t ldy, int32_t* dev_status,
-                       cudaStream_t stream);
+                       int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                       int32_t* dev_status, cudaStream_t stream);
 
 /* Workspace of qmm_q4_gemm_id: routing tables for n_expert experts and
- * P = T*n_used (token, slot) pairs (int32 offsets [n_expert+1] and pair ids
- * [P], each padded to 256 bytes), followed by the pairs' activation rows
- * packed in expert order (bf16 [P][K]). */
+ * P = T*n_used (token, slot) pairs (int32 offsets [n_expert+1], int32 pair ids
+ * [P] and fp32 activation-row scales [P], each padded to 256 bytes), followed
+ * by the pairs' activation rows packed in expert order as f16 [P][K]. */
 qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64_t T, int64_t K,
                                          size_t* ws_bytes);
 
 /* MUL_MAT_ID over q4 experts ("Zaya 8B Q4NX on the AMD NPU": the new
  * MUL_MAT_ID_Q4NX op; "The bugs that were the work"; the down-projection fix
- * of the rounds 24-28 notes).
+ * of the rounds 24-28 notes).  It runs the tensor-core route of qmm_q4_gemm
+ * (f16 operands) with the same accuracy bound and QMM_ERR_RANGE report.
  *
  * tiles     n_expert consecutive N x K tile sets (expert e starts at byte
  *           e * qmm_pack_q4_size(N, K)).
@@ -285,9 +307,9 @@ qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64
  * workspace device scratch (256-byte aligned), rewritten on every call.
  *           qmm_q4_gemm_id_workspace_size bytes run the fastest path, which
  *           packs the activation rows in expert order.  A workspace that holds
- *           only the routing tables runs a path that gathers the rows inside
- *           the grouped kernel (same results); anything smaller returns
- *           QMM_ERR_WORKSPACE.
+ *           only the routing tables and row scales runs a path that gathers
+ *           the rows inside the grouped kernel (same results); anything
+ *           smaller returns QMM_ERR_WORKSPACE.
  * Y[t][i][n] = sum_k x(t,i)[k] * w_{ids(t,i)}[n][k].  A pair whose id is
  * outside [0, n_expert) is skipped (its output row is left untouched) and
  * dev_status gets QMM_ERR_BAD_EXPERT_ID.
@@ -306,9 +328,12 @@ qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_
  * inputs and outputs, and a latency-critical path where an allocation (which
  * may synchronise the device) is not allowed.  The call computes exactly what
  * qmm_q4_gemm_id computes, with the same arguments minus the workspace.  The
- * routing tables live in a fixed scratch array inside the library's own
- * device memory (266,496 bytes, held on every GPU that loads the library
- * until the process exits), so the call allocates nothing.
+ * routing tables and activation-row scales live in a fixed scratch array
+ * inside the library's own device memory (528,640 bytes, held on every GPU
+ * that loads the library until the process exits), so the call allocates
+ * nothing.  When the packed activation rows fit in the rest of the array
+ * (small calls) they are packed there; larger calls gather the rows inside
+ * the grouped kernel.
  *
  * Limits: n_expert <= 1024 and T * n_used <= 65536; larger requests return
  * QMM_ERR_WORKSPACE.
@@ -316,8 +341,8 @@ qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_
  *   address and caches it.  Make that first call before any stream capture.
  * - Every call on a device shares the one array.  Calls that overlap on the
  *   GPU (other streams, other host threads) race on it, so serialise them.
- *   The array keeps the last call's routing tables; nothing in it needs to
- *   start at zero, because each call rewrites what it reads.
+ *   The array keeps the last call's tables; nothing in it needs to start at
+ *   zero, because each call rewrites what it reads.
  */
 qmm_status qmm_q4_gemm_id_noalloc(const void* tiles, int64_t n_expert, int64_t N, int64_t K,
                                   const void* X, int64_t ldx_token, int64_t ldx_slot,
@@ -435,8 +460,9 @@ qmm_status qmm_pack_q8_size(int64_t N, int64_t K, size_t* tile_bytes);
 qmm_status qmm_pack_q8(const float* W, int64_t N, int64_t K, int64_t ldw, qmm_q8_layout layout, void* tiles,
                        size_t tile_bytes, cudaStream_t stream);
 
-/* Workspace of qmm_q8_gemm: 0 for M <= 16, else N*K*2 bytes of bf16 weights
- * plus N*ceil(K/1024)*4 bytes, each rounded up to 256. */
+/* Workspace of qmm_q8_gemm: 0 for M <= 16, else N*K*2 bytes of f16 weights,
+ * N*ceil(K/1024)*4 bytes of chunk scales, M*K*2 bytes of f16 activation rows
+ * and M*4 bytes of row scales, each rounded up to 256. */
 qmm_status qmm_q8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes);
 
 /* Y[m][n] = sum_k X[m][k] * w[n][k] over Q8 tiles, fp32 accumulation.
@@ -451,18 +477,56 @@ qmm_status qmm_q8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* w
  * M <= 16 runs the decode GEMV, which forms every weight exactly
  * (code * scale in fp32), so only fp32 summation rounds: about
  * (K/256 + 14) * 2^-24 * sum_k |x||w| at worst, within 2e-5 * sum_k |x||w|
- * for K <= 65536.  Larger M decodes the tiles to bf16 weights (one rounding,
- * <= 2^-8 relative per weight) for the tensor-core GEMM, within the 4-bit
- * path's bound max |y - y_exact| <= 2e-3 * sum_k |x||w| for inputs whose
- * rounding errors do not all share one sign.
+ * for K <= 65536.  Larger M decodes the tiles to f16 weights (one rounding,
+ * <= 2^-11 relative per weight) and the activation rows to power-of-two
+ * scaled f16 (exact, as for qmm_q4_gemm) for the tensor-core GEMM, which sums
+ * each 1,024-k chunk in fp32: the worst case is
+ * (2^-11 + 1024 * 2^-23 + K/1024 * 2^-24) * sum_k |x||w| < 6.2e-4 * sum_k |x||w|
+ * for scales in f16's normal range.  A block with 128 |s| > 65504 gives
+ * QMM_ERR_RANGE.
  * Errors: QMM_ERR_INVALID_ARG for null or misaligned pointers, bad sizes,
  * strides or layout; QMM_ERR_WORKSPACE; QMM_ERR_UNSUPPORTED for N % 32 != 0,
- * K % 256 != 0, or K > 65536 when M > 16.  Device status: QMM_ERR_TIMEOUT
- * (M > 16 only).
+ * K % 256 != 0, or K > 65536 when M > 16.  Device status: QMM_ERR_TIMEOUT,
+ * QMM_ERR_RANGE (M > 16 only).
  */
 qmm_status qmm_q8_gemm(const void* tiles, qmm_q8_layout layout, int64_t N, int64_t K, const void* X, int64_t M,
                        int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes, int32_t* dev_status,
                        cudaStream_t stream);
+
+/* ========================================================================
+ * Diagnostics
+ * ======================================================================== */
+
+/* Load-only read of `bytes` of device memory (a multiple of 32768, at least
+ * 32768; buf 16-byte aligned): the bandwidth a kernel that only streams data
+ * reaches, the roofline of the decode GEMVs besides the copy bandwidth ("Zaya
+ * 8B Q4NX on the AMD NPU", round 25q: a load-only kernel over a rotating ring
+ * of buffers).  mode 0 reads with per-thread 16-byte loads, mode 1 with bulk
+ * copies into a shared-memory ring (the two ways the GEMVs read).  The data
+ * is folded into one word; `sink` (device uint32) is written only when that
+ * word equals a fixed constant, so normally nothing is stored.  dev_status:
+ * QMM_ERR_TIMEOUT (mode 1).  QMM_ERR_INVALID_ARG for a bad pointer, size or
+ * mode. */
+qmm_status qmm_probe_hbm_read(const void* buf, size_t bytes, int mode, uint32_t* sink, int32_t* dev_status,
+                              cudaStream_t stream);
+
+/* Self-test of the device error path (no counterpart on the pages).
+ *
+ * Every pipeline wait of the tensor-core kernels is bounded in time: a wait
+ * that gives up raises its thread block's abort flag and writes
+ * QMM_ERR_TIMEOUT to dev_status, the block's other waits return at once, and
+ * the kernel frees its tensor memory and exits, leaving the context usable.
+ * This call runs that path on purpose in a one-block kernel: one wait with
+ * limit limit_ns (1 us .. 100 ms) on a barrier nothing arrives on, a second
+ * wait (with the kernels' normal limit) that must leave on the abort flag,
+ * and a tensor-memory allocation held across the abort and freed.
+ * out      device int64 [4]: [0] 1 if the short wait completed (it must not),
+ *          [1] 1 if the second wait completed (it must not), [2] ns the short
+ *          wait took, [3] ns from the abort to the second wait's return.
+ * dev_status gets QMM_ERR_TIMEOUT.  QMM_ERR_INVALID_ARG for a null or
+ * misaligned pointer or a limit outside the range.
+ */
+qmm_status qmm_selftest_wait_timeout(uint64_t limit_ns, int32_t* dev_status, int64_t* out, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -42,11 +42,12 @@ const char* qmm_status_string(qmm_status s) {
     case QMM_ERR_TIMEOUT: return "QMM_ERR_TIMEOUT";
     case QMM_ERR_BAD_EXPERT_ID: return "QMM_ERR_BAD_EXPERT_ID";
     case QMM_ERR_WORKSPACE: return "QMM_ERR_WORKSPACE";
+    case QMM_ERR_RANGE: return "QMM_ERR_RANGE";
   }
   return "QMM_ERR_UNKNOWN";
 }
 
-int qmm_version(void) { return 100; }
+int qmm_version(void) { return 200; }
 
 // ---------------------------------------------------------------------------
 // int8
@@ -306,9 +307,17 @@ qmm_status qmm_pack_q4(const float* W, int64_t N, int64_t K, int64_t ldw, void* 
   return cuda_status(launch_pack_q4(W, N, K, ldw, static_cast<uint8_t*>(tiles), stream));
 }
 
+qmm_status qmm_q4_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes) {
+  if (ws_bytes == nullptr || M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+  if (M > INT32_MAX || K > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  *ws_bytes = q4_umma_eligible(M, N, K) ? act_f16_bytes(M, K) : 0;
+  return QMM_OK;
+}
+
 qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, int64_t M,
-                       int64_t ldx, float* Y, int64_t ldy, int32_t* dev_status,
-                       cudaStream_t stream) {
+                       int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes,
+                       int32_t* dev_status, cudaStream_t stream) {
   if (tiles == nullptr || X == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
   if (N < 1 || K < 1 || M < 1 || ldx < K || ldy < N) return QMM_ERR_INVALID_ARG;
   if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
@@ -326,6 +335,9 @@ qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, i
   a.ldy = ldy;
   if (q4_umma_eligible(M, N, K)) {
     if ((M + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;
+    if (workspace == nullptr || ws_bytes < act_f16_bytes(M, K) || !aligned(workspace, 256))
+      return QMM_ERR_WORKSPACE;
+    a.act16 = workspace;
     return cuda_status(launch_q4_gemm_umma(a, dev_status, stream));
   }
   return cuda_status(launch_q4_gemv(a, dev_status, stream));
@@ -379,9 +391,12 @@ qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_
   a.ldy_token = ldy_token;
   a.ldy_slot = ldy_slot;
   char* ws = static_cast<char*>(workspace);
+  const size_t off_bytes = ((size_t)(n_expert + 1) * 4 + 255) / 256 * 256;
+  const size_t pair_bytes = ((size_t)(T * n_used) * 4 + 255) / 256 * 256;
   a.offsets = reinterpret_cast<int32_t*>(ws);
-  a.pairs = reinterpret_cast<int32_t*>(ws + (((size_t)(n_expert + 1) * 4 + 255) / 256 * 256));
-  a.xperm = packed ? reinterpret_cast<__nv_bfloat16*>(ws + tables) : nullptr;
+  a.pairs = reinterpret_cast<int32_t*>(ws + off_bytes);
+  a.xup = reinterpret_cast<float*>(ws + off_bytes + pair_bytes);
+  a.xperm = packed ? reinterpret_cast<__half*>(ws + tables) : nullptr;
   a.dev_status = dev_status;
   return cuda_status(launch_q4_moe(a, stream));
 }
@@ -425,7 +440,7 @@ qmm_status qmm_q8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* w
   if (ws_bytes == nullptr || M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
   if (N % kTileRows != 0 || K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
   if (M > kQ8GemvMaxM && K > kQ8MaxK) return QMM_ERR_UNSUPPORTED;
-  *ws_bytes = M <= kQ8GemvMaxM ? 0 : q8_gemm_workspace_bytes(N, K);
+  *ws_bytes = M <= kQ8GemvMaxM ? 0 : q8_gemm_workspace_bytes(M, N, K);
   return QMM_OK;
 }
 
@@ -441,12 +456,30 @@ qmm_status qmm_q8_gemm(const void* tiles, qmm_q8_layout layout, int64_t N, int64
   if (M > kQ8GemvMaxM) {
     if (K > kQ8MaxK || (N + 255) / 256 > 65535 || (N / kTileRows) * (K / kTileCols) > INT32_MAX)
       return QMM_ERR_UNSUPPORTED;
-    if (workspace == nullptr || ws_bytes < q8_gemm_workspace_bytes(N, K) || !aligned(workspace, 256))
+    if (workspace == nullptr || ws_bytes < q8_gemm_workspace_bytes(M, N, K) || !aligned(workspace, 256))
       return QMM_ERR_WORKSPACE;
   }
   return cuda_status(launch_q8_gemm(static_cast<const uint8_t*>(tiles), (int)layout, (int)N, (int)K,
                                     static_cast<const __nv_bfloat16*>(X), ldx, (int)M, Y, ldy, workspace, dev_status,
                                     stream));
+}
+
+// ---------------------------------------------------------------------------
+// Diagnostics
+// ---------------------------------------------------------------------------
+
+qmm_status qmm_probe_hbm_read(const void* buf, size_t bytes, int mode, uint32_t* sink, int32_t* dev_status,
+                              cudaStream_t stream) {
+  if (buf == nullptr || sink == nullptr || !aligned(buf, 16) || !aligned(sink, 4)) return QMM_ERR_INVALID_ARG;
+  if (mode != 0 && mode != 1) return QMM_ERR_INVALID_ARG;
+  if (bytes < 32768 || bytes % 32768 != 0) return QMM_ERR_INVALID_ARG;
+  return cuda_status(launch_probe_hbm_read(buf, bytes, mode, sink, dev_status, stream));
+}
+
+qmm_status qmm_selftest_wait_timeout(uint64_t limit_ns, int32_t* dev_status, int64_t* out, cudaStream_t stream) {
+  if (dev_status == nullptr || out == nullptr || !aligned(out, 8)) return QMM_ERR_INVALID_ARG;
+  if (limit_ns < 1000 || limit_ns > 100000000ull) return QMM_ERR_INVALID_ARG;
+  return cuda_status(launch_wait_timeout_selftest(limit_ns, dev_status, out, stream));
 }
 
 }  // extern "C"

@@ -43,6 +43,7 @@
 
 #include <algorithm>
 
+#include "f16_operands.cuh"
 #include "qmm_internal.h"
 
 namespace qmm {
@@ -394,12 +395,15 @@ q8_gemv_kernel(const uint8_t* __restrict__ tiles, int TR, int TC, const __nv_bfl
   }
 }
 
-// Q8 tiles -> bf16 weights bf16(code * scale) as rows [N][K] (the pair GEMM's
-// B operand), and unit chunk scales [N][nb].
+// Q8 tiles -> f16 weights f16(code * scale) as rows [N][K] (the pair GEMM's
+// B operand), and unit chunk scales [N][nb].  code * scale is exact in fp32
+// (8 by 8 significant bits), so each weight is rounded once.  A block whose
+// weights could pass f16's largest value (128 |s| > 65504) reports
+// QMM_ERR_RANGE.
 template <int kLayout>
 __global__ void __launch_bounds__(kTileThreads)
-q8_decode_bf16_kernel(const uint8_t* __restrict__ tiles, int TC, int K, __nv_bfloat16* __restrict__ B16,
-                      float* __restrict__ ones, int nb) {
+q8_decode_f16_kernel(const uint8_t* __restrict__ tiles, int TC, int K, __half* __restrict__ W16,
+                     float* __restrict__ ones, int nb, int32_t* dev_status) {
   __shared__ __align__(16) uint8_t img[kQ8TileBytes];
   const int tile_id = blockIdx.x;
   const int tr = tile_id / TC, tc = tile_id % TC;
@@ -409,7 +413,8 @@ q8_decode_bf16_kernel(const uint8_t* __restrict__ tiles, int TC, int K, __nv_bfl
   const int r = threadIdx.x & 31, g = threadIdx.x >> 5;
   const int n = 32 * tr + r;
   const float s = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(img + kQ8CodeBytes)[32 * g + r]);
-  uint4* dst = reinterpret_cast<uint4*>(B16 + (int64_t)n * K + 256 * tc + 32 * g);
+  if (128.0f * fabsf(s) > kF16Max) set_status(dev_status, QMM_ERR_RANGE);
+  uint4* dst = reinterpret_cast<uint4*>(W16 + (int64_t)n * K + 256 * tc + 32 * g);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t o[4];
@@ -418,8 +423,7 @@ q8_decode_bf16_kernel(const uint8_t* __restrict__ tiles, int TC, int K, __nv_bfl
       const int k = 32 * g + 8 * c + 2 * i;
       const float w0 = __fmul_rn((float)(int8_t)img[q8_offset<kLayout>(r, k)], s);
       const float w1 = __fmul_rn((float)(int8_t)img[q8_offset<kLayout>(r, k + 1)], s);
-      o[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w0)) |
-             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w1)) << 16);
+      o[i] = (uint32_t)__half_as_ushort(__float2half_rn(w0)) | ((uint32_t)__half_as_ushort(__float2half_rn(w1)) << 16);
     }
     dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
   }
@@ -466,10 +470,12 @@ cudaError_t launch_pack_q8(const float* W, int64_t ldw, int N, int K, int layout
   return cudaGetLastError();
 }
 
-size_t q8_gemm_workspace_bytes(int64_t N, int64_t K) {
-  const size_t b16 = (size_t)N * K * 2;
+// f16 weights [N][K], unit chunk scales [N][nb], then the f16 activation
+// rows and their scales, each padded to 256 bytes.
+size_t q8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const size_t w16 = (size_t)N * K * 2;
   const size_t ones = (size_t)N * ((K + kPairChunkK - 1) / kPairChunkK) * 4;
-  return (b16 + 255) / 256 * 256 + (ones + 255) / 256 * 256;
+  return (w16 + 255) / 256 * 256 + (ones + 255) / 256 * 256 + act_f16_bytes(M, K);
 }
 
 cudaError_t launch_q8_gemm(const uint8_t* tiles, int layout, int N, int K, const __nv_bfloat16* X, int64_t ldx,
@@ -489,15 +495,22 @@ cudaError_t launch_q8_gemm(const uint8_t* tiles, int layout, int N, int K, const
     return q8_gemv_launch<16>(layout, units, sms, tiles, TR, TC, X, ldx, Y, ldy, M, wpu, stream);
   }
   char* ws = static_cast<char*>(workspace);
-  __nv_bfloat16* B16 = reinterpret_cast<__nv_bfloat16*>(ws);
-  float* ones = reinterpret_cast<float*>(ws + ((size_t)N * K * 2 + 255) / 256 * 256);
+  __half* W16 = reinterpret_cast<__half*>(ws);
+  const size_t ones_off = ((size_t)N * K * 2 + 255) / 256 * 256;
   const int nb = (K + kPairChunkK - 1) / kPairChunkK;
+  float* ones = reinterpret_cast<float*>(ws + ones_off);
+  char* act = ws + ones_off + ((size_t)N * nb * 4 + 255) / 256 * 256;
   const int64_t ntiles = (int64_t)TR * TC;
-  if (layout == 0) q8_decode_bf16_kernel<0><<<(unsigned)ntiles, kTileThreads, 0, stream>>>(tiles, TC, K, B16, ones, nb);
-  else q8_decode_bf16_kernel<1><<<(unsigned)ntiles, kTileThreads, 0, stream>>>(tiles, TC, K, B16, ones, nb);
+  if (layout == 0)
+    q8_decode_f16_kernel<0><<<(unsigned)ntiles, kTileThreads, 0, stream>>>(tiles, TC, K, W16, ones, nb, dev_status);
+  else
+    q8_decode_f16_kernel<1><<<(unsigned)ntiles, kTileThreads, 0, stream>>>(tiles, TC, K, W16, ones, nb, dev_status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  return launch_bf16w_gemm_umma(B16, ones, nb, N, K, X, ldx, M, Y, ldy, dev_status, stream);
+  if ((err = launch_act_to_f16(X, ldx, M, K, act, stream)) != cudaSuccess) return err;
+  return launch_w16_gemm_umma(W16, true, ones, nb, N, K, act, K,
+                              reinterpret_cast<const float*>(act + act_f16_scale_offset(M, K)), M, Y, ldy,
+                              dev_status, stream);
 }
 
 }  // namespace qmm

@@ -70,14 +70,19 @@ struct Int8UmmaParams {
   const int32_t* row_sum;            // [M] (null when zB' == 0)
   Int8Epi epi;
   int32_t* dev_status;
-  const float* w8_scales;            // W8A16: [N][w8_nb], one per row and 1,024 k
+  const float* w8_scales;            // W8A16 and Q8: [N][w8_nb], one per row and 1,024 k
   int w8_nb;
+  const float* x_up;                 // Q8: inverse scale of each f16 activation row
 };
 
 // W8A16 instance of the kernel: bf16 activations x int8 weights widened to
 // bf16 (exact), each 1,024-k accumulator chunk scaled per column by its
 // block's weight scale, fp32 output.
 constexpr int kW8Out = 100;
+// Q8 instance: the same epilogue on f16 weights and f16 activation rows,
+// each output row multiplied by its activation row's inverse scale.
+constexpr int kQ8Out = 101;
+constexpr bool is_chunk_scaled(int out) { return out == kW8Out || out == kQ8Out; }
 
 // Output conversion of one element (fp32 steps with explicit IEEE rounding),
 // specialised on the output type; kPerRowMq: requantisation with a per-row
@@ -236,7 +241,7 @@ int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       // The issue loop is kept short (stage and phase counted, descriptors
       // offset from precomputed bases): the tensor pipe queues few MMAs, so
       // this thread's latency per 64-k block is on the critical path.
-      constexpr uint32_t idesc = idesc_f16(2 * kBM, kBN, kOut == kW8Out);   // bf16 operands for W8A16
+      constexpr uint32_t idesc = idesc_f16(2 * kBM, kBN, kOut == kW8Out);   // bf16 operands for W8A16 only
       const uint64_t adesc0 = desc_kmajor_sw128(smem_u32(sA)), bdesc0 = desc_kmajor_sw128(smem_u32(sB));
       int s = 0, gc = 0;  // stage; chunks issued (all tiles)
       uint32_t ph = 0;    // phase parity of the full barriers at stage s
@@ -271,10 +276,10 @@ int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       umma_commit_pair(done, 0x1);
       mbar_wait(done, 0, abort_flag, p.dev_status);
     }
-  } else if (kOut == kW8Out && warp >= kEpiWarp0) {
-    // W8A16 epilogue: each 1,024-k chunk of the accumulator, times the weight
-    // scale of that chunk's block for each column, is added in fp32.  A warp's
-    // 128 column scales are fetched one chunk ahead into shared memory.
+  } else if (is_chunk_scaled(kOut) && warp >= kEpiWarp0) {
+    // W8A16 / Q8 epilogue: each 1,024-k chunk of the accumulator, times the
+    // weight scale of that chunk's block for each column, is added in fp32.  A
+    // warp's 128 column scales are fetched one chunk ahead into shared memory.
     const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
     const int ew = warp - kEpiWarp0;
     float* scs = reinterpret_cast<float*>(sConst) + ew * 768;   // [2][128]
@@ -329,6 +334,11 @@ int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         __syncwarp();
       }
       if (ok && row < p.M) {
+        if (kOut == kQ8Out) {
+          const float xu = p.x_up[row];   // a power of two: exact
+#pragma unroll
+          for (int i = 0; i < 128; ++i) acc[i] *= xu;
+        }
         float* yrow = Yf + (int64_t)row * p.epi.ldo;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -347,7 +357,7 @@ int8_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
       }
       __syncwarp();
     }
-  } else if (kOut != kW8Out && warp >= kEpiWarp0) {
+  } else if (!is_chunk_scaled(kOut) && warp >= kEpiWarp0) {
     // epilogue: warp w reads TMEM lanes 32*(w%4).. and columns h*128..h*128+127
     const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
     const int ew = warp - kEpiWarp0;
@@ -598,12 +608,13 @@ WsLayout ws_layout(int64_t M, int64_t K, int64_t N) {
 
 using UmmaKernel = void (*)(CUtensorMap, CUtensorMap, Int8UmmaParams);
 // One instantiation per output conversion: S32, F32, S8, U8, then S8 and U8
-// with a per-row activation scale; last the W8A16 instance.
-constexpr UmmaKernel kUmmaKernels[7] = {
+// with a per-row activation scale; last the W8A16 and Q8 instances.
+constexpr UmmaKernel kUmmaKernels[8] = {
     int8_umma_kernel<QMM_S32, false>, int8_umma_kernel<QMM_F32, false>, int8_umma_kernel<QMM_S8, false>,
     int8_umma_kernel<QMM_U8, false>,  int8_umma_kernel<QMM_S8, true>,   int8_umma_kernel<QMM_U8, true>,
-    int8_umma_kernel<kW8Out, false>};
+    int8_umma_kernel<kW8Out, false>,  int8_umma_kernel<kQ8Out, false>};
 constexpr int kW8Kernel = 6;
+constexpr int kQ8Kernel = 7;
 
 // Clusters of two that fit on the device at once (a GPC with an odd SM count
 // leaves one SM over), with the kernel's shared-memory opt-in done: once per
@@ -746,27 +757,25 @@ cudaError_t launch_w8_gemm_umma(const int8_t* codes, const float* scales, int N,
   const int wgrid = std::min(ngroups, 2 * pairs * per_sm);
   int8_widen_kernel<<<wgrid, kWidenThreads, wsmem, stream>>>(wp);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  return launch_bf16w_gemm_umma(B16, scales, (K + kChunkK - 1) / kChunkK, N, K, X, ldx, M, Y, ldy, dev_status,
-                                stream);
+  return launch_w16_gemm_umma(B16, false, scales, (K + kChunkK - 1) / kChunkK, N, K, X, ldx, nullptr, M, Y, ldy,
+                              dev_status, stream);
 }
 
-// The GEMM half of the above on bf16 weights B16 [N][Kp] (Kp = K rounded up
-// to 64, zero columns past K) that an earlier launch in the stream wrote:
-// Y = sum over 1,024-k chunks c of scales[n][c] * (X B16^T restricted to c).
-// Launched as a programmatic dependent; the kernel waits for the previous
-// grid before it reads B16.
-cudaError_t launch_bf16w_gemm_umma(const __nv_bfloat16* B16, const float* scales, int nb, int N, int K,
-                                   const __nv_bfloat16* X, int64_t ldx, int M, float* Y, int64_t ldy,
-                                   int32_t* dev_status, cudaStream_t stream) {
+// The GEMM half of the above on 16-bit weights W16 [N][Kp] (Kp = K rounded
+// up to 64, zero columns past K) that an earlier launch in the stream wrote:
+// Y = sum over 1,024-k chunks c of scales[n][c] * (X W16^T restricted to c),
+// times x_up[m] for f16 operands.  Launched as a programmatic dependent; the
+// kernel waits for the previous grid before it reads W16 or X.
+cudaError_t launch_w16_gemm_umma(const void* W16, bool f16, const float* scales, int nb, int N, int K,
+                                 const void* X, int64_t ldx, const float* x_up, int M, float* Y, int64_t ldy,
+                                 int32_t* dev_status, cudaStream_t stream) {
   const int Kp = (int)padded_k(K);
   int pairs = 0;
   cudaError_t err = resident_pairs(&pairs);
   if (err != cudaSuccess) return err;
   CUtensorMap tmA, tmB;
-  if (!make_tmap_2d(&tmA, true, const_cast<__nv_bfloat16*>(X), (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2, kBK,
-                    kBM) ||
-      !make_tmap_2d(&tmB, true, const_cast<__nv_bfloat16*>(B16), (uint64_t)Kp, (uint64_t)N, (uint64_t)Kp * 2, kBK,
-                    kBNh))
+  if (!make_tmap_2d(&tmA, true, const_cast<void*>(X), (uint64_t)K, (uint64_t)M, (uint64_t)ldx * 2, kBK, kBM) ||
+      !make_tmap_2d(&tmB, true, const_cast<void*>(W16), (uint64_t)Kp, (uint64_t)N, (uint64_t)Kp * 2, kBK, kBNh))
     return cudaErrorInvalidValue;
   Int8UmmaParams p{};
   p.M = M;
@@ -780,6 +789,7 @@ cudaError_t launch_bf16w_gemm_umma(const __nv_bfloat16* B16, const float* scales
   p.dev_status = dev_status;
   p.w8_scales = scales;
   p.w8_nb = nb;
+  p.x_up = x_up;
   if (pairs > p.ntiles) pairs = p.ntiles;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
@@ -791,7 +801,7 @@ cudaError_t launch_bf16w_gemm_umma(const __nv_bfloat16* B16, const float* scales
   attr[0].val.programmaticStreamSerializationAllowed = 1;   // overlap the grid that wrote B16
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kUmmaKernels[kW8Kernel], tmA, tmB, p);
+  return cudaLaunchKernelEx(&cfg, kUmmaKernels[f16 ? kQ8Kernel : kW8Kernel], tmA, tmB, p);
 }
 
 }  // namespace qmm

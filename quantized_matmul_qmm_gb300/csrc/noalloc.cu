@@ -5,10 +5,12 @@
 // outputs.  Another is a latency-critical path that cannot afford a
 // cudaMalloc, which may synchronise the device.  For those callers,
 // qmm_q4_gemm_id_noalloc keeps the routing tables of the expert grouping
-// (per-expert offsets and the grouped (token, slot) list) in a fixed array in
-// the library's own device memory.  Every GPU that loads the library holds
-// that array until the process exits.  The rest of the call is
-// qmm_q4_gemm_id, unchanged.
+// (per-expert offsets, the grouped (token, slot) list and the activation-row
+// scales) in a fixed array in the library's own device memory.  Every GPU
+// that loads the library holds that array until the process exits.  The rest
+// of the call is qmm_q4_gemm_id, unchanged: when the packed activation rows
+// also fit in the array (small calls), it packs them there; otherwise the
+// grouped kernel gathers the rows itself.
 #include <mutex>
 
 #include "qmm_internal.h"
@@ -20,7 +22,8 @@ namespace {
 constexpr int64_t kNoAllocMaxExperts = 1024;
 constexpr int64_t kNoAllocMaxPairs = 65536;   // T * n_used
 constexpr size_t kOffsetsBytes = ((kNoAllocMaxExperts + 1) * 4 + 255) / 256 * 256;
-constexpr size_t kScratchBytes = kOffsetsBytes + (size_t)kNoAllocMaxPairs * 4;  // 266,496 bytes
+// offsets, pair ids, row scales: 528,640 bytes
+constexpr size_t kScratchBytes = kOffsetsBytes + 2 * (size_t)kNoAllocMaxPairs * 4;
 static_assert(kScratchBytes % 256 == 0, "pair table padding");
 
 // The routing scratch.  Host code must not pass this symbol to a kernel: on
@@ -62,8 +65,9 @@ extern "C" qmm_status qmm_q4_gemm_id_noalloc(const void* tiles, int64_t n_expert
   void* scratch = nullptr;
   const qmm_status st = scratch_address(&scratch);
   if (st != QMM_OK) return st;
-  // The router rewrites every offset and every grouped pair it reads later,
-  // so nothing in the scratch has to start at zero.
+  // The router and the packing grid rewrite every offset, grouped pair, row
+  // scale and packed row that later grids read, so nothing in the scratch has
+  // to start at zero.
   return qmm_q4_gemm_id(tiles, n_expert, N, K, X, ldx_token, ldx_slot, ids, ld_ids, n_used, T, Y,
                         ldy_token, ldy_slot, scratch, kScratchBytes, dev_status, stream);
 }

@@ -31,6 +31,14 @@
 // rows with cp.async.  The grouped kernel is launched as the last grid's
 // programmatic dependent, so it starts while that grid still runs.
 //
+// Operands are f16: each weight is formed once as f16(q * s + m) (one
+// rounding, 2^-11 relative), and each activation row is stored in f16 after a
+// power-of-two scale that makes the conversion exact and overflow-free; the
+// epilogue multiplies every output column back by its row's inverse scale.
+// The activation rows are converted by the grid before this one (the packing
+// grid, or for the dense GEMM a conversion grid); in the gather mode the
+// loader converts each gathered stage in place in shared memory.
+//
 // The contraction runs on the 5th-generation tensor cores with the weights as
 // the M = 128 side and the pairs as N (16..kTok).  The dequantised weights go
 // from registers straight into TMEM, which tcgen05.mma reads as its A
@@ -40,13 +48,13 @@
 //   transform  four or eight warps; warp (q, h) owns TMEM lane quarter q (one
 //              weight row per lane) and, with eight, 64-k half h of every
 //              128-k stage: it reads the rows' codes and pairs, forms
-//              w = bf16(q * s + m) with one rounding, and stores the stage into
+//              w = f16(q * s + m) with one rounding, and stores the stage into
 //              an A buffer (tcgen05.st).  With four, they also drain each
 //              job's accumulator into Y.
 //   epilogue   (one CTA per SM) four warps draining accumulators into Y.
 //   loader     TMA of the packed rows (or of X for the dense GEMM), or a
 //              cp.async gather, into the 128-byte-swizzle K-major layout.
-//   MMA        TMEM owner; lane 0 issues tcgen05.mma (kind::f16, bf16).
+//   MMA        TMEM owner; lane 0 issues tcgen05.mma (kind::f16, f16 operands).
 //   producer   TMA of whole tile columns: one box for the unit's 4 tiles'
 //              codes, one for their pairs, 128-byte swizzle.
 // Every wait is bounded; a timeout sets the caller's status word and the CTA
@@ -55,6 +63,7 @@
 
 #include <algorithm>
 
+#include "f16_operands.cuh"
 #include "qmm_internal.h"
 #include "umma.cuh"
 
@@ -91,7 +100,7 @@ struct Lay {
   static constexpr int kAStages = (kCtas == 2 || kTok > 128) ? 2 : 4;
   static constexpr int kRawStages = kCtas == 2 ? 3 : (kTok == 64 ? 4 : 3);
   static constexpr int kBStages = (kCtas == 2 || kTok > 128) ? 3 : 4;   // activation ring depth
-  static constexpr int kBAtomBytes = kTok * 128;           // kTok rows x 64 k bf16, 128-byte swizzle
+  static constexpr int kBAtomBytes = kTok * 128;           // kTok rows x 64 k f16, 128-byte swizzle
   static constexpr int kBBytes = 2 * kBAtomBytes;          // 128 k per stage
   static constexpr uint32_t kColA = 2 * kTok;              // after the two accumulators
   static constexpr uint32_t kTmemCols = kCtas == 2 ? 256 : 512;
@@ -120,7 +129,7 @@ static_assert(kNumBars * 8 + 8 <= 256, "barrier block");
 struct MoeParams {
   int64_t tiles_per_expert;
   int N, K;
-  const __nv_bfloat16* X;
+  const __nv_bfloat16* X;   // gather mode: the bf16 src1 rows
   int64_t ldx_token, ldx_slot;
   int n_used, n_expert, npairs;
   int n_units, nrb;         // units = experts x 128-row blocks, unit u = e * nrb + row block
@@ -130,19 +139,9 @@ struct MoeParams {
   const int32_t* pairs;     // grouped (token, slot) ids
   int dense_rows;           // dense GEMM: M
   int dense_chunks;         // dense GEMM: token chunks of kTok per row block; unit u = rb * chunks + chunk
+  const float* xup;         // inverse activation-row scales: per token (dense) or per grouped rank
   int32_t* dev_status;
 };
-
-// q * s + m in bf16 from a (128 + q) pair: the subtraction is exact, the fma
-// rounds once.
-__device__ __forceinline__ uint32_t dequant2(uint32_t q2_biased, uint32_t s2, uint32_t m2) {
-  __nv_bfloat162 q = *reinterpret_cast<__nv_bfloat162*>(&q2_biased);
-  const uint32_t c128 = 0x43004300u;
-  q = __hsub2(q, *reinterpret_cast<const __nv_bfloat162*>(&c128));
-  const __nv_bfloat162 w =
-      __hfma2(q, *reinterpret_cast<__nv_bfloat162*>(&s2), *reinterpret_cast<__nv_bfloat162*>(&m2));
-  return *reinterpret_cast<const uint32_t*>(&w);
-}
 
 __device__ __forceinline__ void pair_offsets(const MoeParams& p, int pr, int64_t& xo, int64_t& yo) {
   const int tok = pr / p.n_used, slot = pr % p.n_used;
@@ -207,36 +206,77 @@ __device__ __forceinline__ bool produce_weights(const CUtensorMap* tmC, const CU
   return true;
 }
 
+// kN accumulator columns (one TMEM load) of one lane's weight row n into Y,
+// each times its column's inverse activation scale.  The scales are read four
+// at a time (every lane reads the same address); dense rows of Y are
+// consecutive tokens, so the output pointer steps by ldy.
+template <int kN, int kMode>
+__device__ __forceinline__ void epilogue_store(const MoeParams& p, const uint32_t (&v)[kN], int c0, int nt, bool live,
+                                               float* ycol0, const int64_t* yoff_q, const float* ysc_q) {
+  float sc[kN];
+#pragma unroll
+  for (int j = 0; j < kN / 4; ++j) {
+    const float4 f = *reinterpret_cast<const float4*>(ysc_q + c0 + 4 * j);
+    sc[4 * j] = f.x;
+    sc[4 * j + 1] = f.y;
+    sc[4 * j + 2] = f.z;
+    sc[4 * j + 3] = f.w;
+  }
+  if (!live) return;
+  if (kMode == kDense) {
+    float* yp = ycol0 + (int64_t)c0 * p.ldy_token;
+#pragma unroll
+    for (int i = 0; i < kN; ++i) {
+      if (c0 + i < nt) *yp = __uint_as_float(v[i]) * sc[i];
+      yp += p.ldy_token;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kN / 2; ++j) {
+      const longlong2 o = *reinterpret_cast<const longlong2*>(yoff_q + c0 + 2 * j);
+      if (c0 + 2 * j < nt) ycol0[o.x] = __uint_as_float(v[2 * j]) * sc[2 * j];
+      if (c0 + 2 * j + 1 < nt) ycol0[o.y] = __uint_as_float(v[2 * j + 1]) * sc[2 * j + 1];
+    }
+  }
+}
+
 // Drain job `jb`'s accumulator (buffer njobs & 1) for TMEM lane quarter q into
 // Y: lane = weight row, column = pair.  Returns false after an abort.
 template <int kMode, int kTok>
 __device__ __forceinline__ bool epilogue_job(const MoeParams& p, const Jobs<kTok>& jb, int q, int lane, uint32_t tmem,
                                              int njobs, uint64_t* d_full, uint64_t* d_empty, int64_t* yoff_q,
-                                             volatile int* abort_flag) {
+                                             float* ysc_q, volatile int* abort_flag) {
   const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
   const int n = jb.n0 + 32 * q + lane;
   const int nt = jb.nt(), ncol = jb.ncol();
+  // column c is token pass0 + c (dense) or grouped rank first + pass0 + c
+  const int r0 = kMode == kDense ? jb.pass0 : jb.first + jb.pass0;
   for (int c = lane; c < nt; c += 32) {
-    int64_t xo;
-    if (kMode == kDense)
-      yoff_q[c] = (int64_t)(jb.pass0 + c) * p.ldy_token;
-    else
+    if (kMode != kDense) {
+      int64_t xo;
       pair_offsets(p, p.pairs[jb.first + jb.pass0 + c], xo, yoff_q[c]);
+    }
+    ysc_q[c] = p.xup[r0 + c];
   }
   __syncwarp();
   const int db = njobs & 1;
   if (!__all_sync(0xffffffffu, mbar_wait(&d_full[db], (njobs >> 1) & 1, abort_flag, p.dev_status))) return false;
   tc_fence_after();
   const bool live = n < p.N;
-  for (int c0 = 0; c0 < ncol; c0 += 16) {
-    uint32_t v[16];
-    tmem_ld16(trow + (uint32_t)(kTok * db) + c0, v);
+  float* ycol0 = p.Y + n + (kMode == kDense ? (int64_t)jb.pass0 * p.ldy_token : 0);
+  const uint32_t tacc = trow + (uint32_t)(kTok * db);
+  int c0 = 0;
+  for (; c0 + 32 <= ncol; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(tacc + c0, v);
     tmem_wait_ld();
-    if (live) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        if (c0 + i < nt) p.Y[yoff_q[c0 + i] + n] = __uint_as_float(v[i]);
-    }
+    epilogue_store<32, kMode>(p, v, c0, nt, live, ycol0, yoff_q, ysc_q);
+  }
+  if (c0 < ncol) {   // ncol is a multiple of 16
+    uint32_t v[16];
+    tmem_ld16(tacc + c0, v);
+    tmem_wait_ld();
+    epilogue_store<16, kMode>(p, v, c0, nt, live, ycol0, yoff_q, ysc_q);
   }
   tc_fence_before();
   __syncwarp();
@@ -264,8 +304,9 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
   constexpr int kHalves = kXW / 4;
   constexpr int kWEpi = kXW, kWLoad = kXW + (L::kSepEpi ? 4 : 0), kWMma = kWLoad + 1, kWProd = kWLoad + 2;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int64_t xoff[kTok];      // gather mode: the loader warp's rows of the current job
-  __shared__ int64_t yoff[4][kTok];   // each epilogue warp's output rows of its current job
+  __shared__ int64_t xoff[kMode == kTableGather ? kTok : 1];   // gather mode: the loader's rows of the current job
+  __shared__ __align__(16) int64_t yoff[4][kTok];   // each epilogue warp's output rows of its current job
+  __shared__ __align__(16) float ysc[4][kTok];      // and their inverse activation scales
   uint8_t* smem = smem_align(smem_raw, 1024);
   const uint32_t sB0 = smem_u32(smem);                              // [kBStages][2 atoms]
   const uint32_t raw0 = sB0 + kBStages * kBBytes;                   // [kRawStages][codes | pairs]
@@ -336,11 +377,12 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
   bool ok = true;
   int njobs = 0;
   if (warp < kXW) {
-    // ---- transform: raw tiles -> bf16 weights in TMEM; then the epilogue ----
+    // ---- transform: raw tiles -> f16 weights in TMEM; then the epilogue ----
     // Warp (q, hw): TMEM lane quarter q (its 32 weight rows), and of each
     // 128-k stage the 64-k half hw when two warps share a quarter.
     const int q = warp & 3, hw = warp >> 2;
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+    float wmax = 0.0f;   // largest |m| + 15|s| of the blocks this thread formed
     int gws = 0, gs = 0;
     if (first_empty) {
       for (; gws < pre && ok; ++gws) {
@@ -382,13 +424,14 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
 #pragma unroll
             for (int bb = 0; bb < 2; ++bb) {
               const int b = 4 * h + 2 * hh + bb;
-              const uint32_t pair = u4_get(b < 4 ? pr0 : pr1, b & 3);
-              const uint32_t s2 = __byte_perm(pair, 0, 0x1010), m2 = __byte_perm(pair, 0, 0x3232);
+              uint32_t s2, m2;
+              q4_pair_to_f16(u4_get(b < 4 ? pr0 : pr1, b & 3), s2, m2, wmax);
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
                 const uint32_t word = u4_get(cw[b], t);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) v[16 * bb + 4 * t + i] = dequant2(q4_pair_biased(word, i), s2, m2);
+                for (int i = 0; i < 4; ++i)
+                  v[16 * bb + 4 * t + i] = dequant2_f16(q4_pair_biased_f16(word, i), s2, m2);
               }
             }
             tmem_st32(trow + kColA + 64 * as + 32 * hh, v);
@@ -404,16 +447,18 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
         if (lane == 0) mbar_arrive(&w_empty[slot]);
       }
       if (!L::kSepEpi && ok) {
-        ok = epilogue_job<kMode, kTok>(p, jb, q, lane, tmem, njobs, d_full, d_empty, yoff[q], abort_flag);
+        ok = epilogue_job<kMode, kTok>(p, jb, q, lane, tmem, njobs, d_full, d_empty, yoff[q], ysc[q], abort_flag);
         ++njobs;
       }
     }
+    // a weight beyond f16's range would have become infinite
+    if (__any_sync(0xffffffffu, wmax > kF16Max) && lane == 0) set_status(p.dev_status, QMM_ERR_RANGE);
   } else if (L::kSepEpi && warp < kWEpi + 4) {
     // ---- epilogue: fp32 accumulator -> Y (lane = weight row, column = pair) ----
     const int q = warp & 3;
     Jobs<kTok> jb;
     while (ok && jb.next(p)) {
-      ok = epilogue_job<kMode, kTok>(p, jb, q, lane, tmem, njobs, d_full, d_empty, yoff[q], abort_flag);
+      ok = epilogue_job<kMode, kTok>(p, jb, q, lane, tmem, njobs, d_full, d_empty, yoff[q], ysc[q], abort_flag);
       ++njobs;
     }
   } else if (warp == kWLoad) {
@@ -441,7 +486,24 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
       }
       __syncwarp();
     } else {
+      // The rows are gathered in bf16 with cp.async and converted to f16 in
+      // place once they have landed (both are 16-bit, so the swizzled
+      // positions do not change).  Each lane converts the chunks it copied.
       int signalled = 0;   // stages whose b_full has been raised
+      int st_r0[kBStagesMax] = {}, st_nt[kBStagesMax] = {};   // grouped rank of column 0 and width, per stage
+      auto convert_stage = [&](int g) {
+        const int bs = g % kBStages;
+        const int r0 = st_r0[bs], nt = st_nt[bs];
+        const uint32_t sb = sB0 + bs * kBBytes;
+        for (int i = lane; i < nt * 16; i += 32) {
+          const int c = i >> 4, ch = i & 15;
+          const uint32_t dst = sb + (ch >> 3) * kBAtomBytes + (c >> 3) * 1024 + (c & 7) * 128 +
+                               (uint32_t)(((ch & 7) ^ (c & 7)) << 4);
+          // the inverse of a power of two in fp32's normal range
+          const float down = __uint_as_float((254u << 23) - __float_as_uint(p.xup[r0 + c]));
+          sts128(dst, bf16x8_to_f16x8_scaled(lds128(dst), down));
+        }
+      };
       while (ok && jb.next(p)) {
         const int nt = jb.nt(), ncol = jb.ncol();
         __syncwarp();   // the previous job's copies have read xoff
@@ -457,6 +519,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
             ok = false;
             break;
           }
+          st_r0[bs] = jb.first + jb.pass0;
+          st_nt[bs] = nt;
           const uint32_t sb = sB0 + bs * kBBytes;
           for (int i = lane; i < ncol * 16; i += 32) {
             const int c = i >> 4, ch = i & 15;
@@ -469,6 +533,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
           cp_async_commit();
           if (gs + 1 - signalled > kLoaderLag) {
             cp_async_wait<kLoaderLag>();
+            convert_stage(signalled);
             fence_proxy_async_smem();   // generic-proxy writes -> tcgen05 reads
             __syncwarp();
             if (lane == 0) mbar_arrive(&b_full[signalled % kBStages]);
@@ -477,6 +542,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
         }
       }
       cp_async_wait<0>();
+      if (ok)
+        for (int g = signalled; g < gs; ++g) convert_stage(g);
       fence_proxy_async_smem();
       __syncwarp();
       for (; signalled < gs; ++signalled)
@@ -496,7 +563,7 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
       Jobs<kTok> jb;
       while (ok && jb.next(p)) {
         const int db = njobs & 1;
-        const uint32_t idesc = idesc_f16(kRows, jb.ncol(), true);
+        const uint32_t idesc = idesc_f16(kRows, jb.ncol(), false);   // f16 A and B
         const uint32_t dt = tmem + (uint32_t)(kTok * db);
         if (!mbar_wait(&d_empty[db], ((njobs >> 1) & 1) ^ 1, abort_flag, p.dev_status)) {
           ok = false;
@@ -687,13 +754,15 @@ moe_route_kernel(const int32_t* __restrict__ ids, int64_t ld_ids, int n_used, in
   }
 }
 
-// Activation packing: the src1 row of every grouped pair, copied to its rank
-// so that each job's B operand is one dense block.  One warp per row, the
-// whole row's 16-byte loads in flight at once.
+// Activation packing: the src1 row of every grouped pair, as f16 operands at
+// its rank, so that each job's B operand is one dense block, and the row's
+// inverse scale up[rank].  With Xp null (the gather mode) only the scales are
+// written.  One warp per row; rows of up to 2,048 elements stay in registers
+// between the max and the conversion, longer ones are read twice.
 __global__ void __launch_bounds__(kRouteThreads)
 moe_pack_kernel(const int32_t* __restrict__ pairs, const int32_t* __restrict__ offsets, int n_expert, int n_used,
                 const __nv_bfloat16* __restrict__ X, int64_t ldx_token, int64_t ldx_slot, int K,
-                __nv_bfloat16* __restrict__ Xp) {
+                __half* __restrict__ Xp, float* __restrict__ up) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the pair list comes from the routing grid
   const int lane = threadIdx.x & 31;
@@ -704,18 +773,41 @@ moe_pack_kernel(const int32_t* __restrict__ pairs, const int32_t* __restrict__ o
     const int pr = pairs[r];
     const int t = pr / n_used, i = pr - t * n_used;
     const uint4* src = reinterpret_cast<const uint4*>(X + (int64_t)t * ldx_token + (int64_t)i * ldx_slot);
-    uint4* dst = reinterpret_cast<uint4*>(Xp + (int64_t)r * K);
+    uint4 v[8];
+    uint32_t am = 0;
     for (int c0 = 0; c0 < chunks; c0 += 8 * 32) {
-      uint4 v[8];
+      uint4 w[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int c = c0 + u * 32 + lane;
-        if (c < chunks) v[u] = ldg128(src + c);
+        w[u] = c < chunks ? ldg128(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        am = bf16x2_absmax_bits(am, w[u].x);
+        am = bf16x2_absmax_bits(am, w[u].y);
+        am = bf16x2_absmax_bits(am, w[u].z);
+        am = bf16x2_absmax_bits(am, w[u].w);
+        if (c0 == 0) v[u] = w[u];
+      }
+    }
+    float down, u_r;
+    f16_row_scale(__reduce_max_sync(0xffffffffu, bf16x2_absmax_fold(am)), down, u_r);
+    if (lane == 0) up[r] = u_r;
+    if (Xp == nullptr) continue;
+    uint4* dst = reinterpret_cast<uint4*>(Xp + (int64_t)r * K);
+    for (int c0 = 0; c0 < chunks; c0 += 8 * 32) {
+      if (c0 > 0) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int c = c0 + u * 32 + lane;
+          if (c < chunks) v[u] = ldg128(src + c);
+        }
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int c = c0 + u * 32 + lane;
-        if (c < chunks) dst[c] = v[u];
+        if (c < chunks) dst[c] = bf16x8_to_f16x8_scaled(v[u], down);
       }
     }
   }
@@ -737,9 +829,9 @@ cudaError_t launch_tc(const CUtensorMap& tmC, const CUtensorMap& tmP, const CUte
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;   // overlap the route-and-pack grid
+  attr[0].val.programmaticStreamSerializationAllowed = 1;   // overlap the packing or conversion grid
   cfg.attrs = attr;
-  cfg.numAttrs = kMode == kDense ? 0 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tmC, tmP, tmX, p);
 }
 
@@ -747,7 +839,7 @@ cudaError_t launch_tc(const CUtensorMap& tmC, const CUtensorMap& tmP, const CUte
 
 size_t q4_moe_table_bytes(int64_t n_expert, int64_t n_used, int64_t T) {
   const size_t off = ((size_t)(n_expert + 1) * 4 + 255) / 256 * 256;
-  return off + ((size_t)(T * n_used) * 4 + 255) / 256 * 256;
+  return off + 2 * (((size_t)(T * n_used) * 4 + 255) / 256 * 256);   // pair ids, then row scales
 }
 
 size_t q4_moe_workspace_bytes(int64_t n_expert, int64_t n_used, int64_t T, int64_t K) {
@@ -772,6 +864,7 @@ cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream) {
   p.ldy_slot = a.ldy_slot;
   p.offsets = a.offsets;
   p.pairs = a.pairs;
+  p.xup = a.xup;
   p.dev_status = a.dev_status;
   const uint64_t n_tiles = (uint64_t)a.n_expert * (uint64_t)p.tiles_per_expert;
   if (n_tiles > (uint64_t)INT32_MAX || (int64_t)a.n_expert * p.nrb > INT32_MAX) return cudaErrorInvalidValue;
@@ -796,12 +889,14 @@ cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream) {
                                                            a.offsets, a.pairs, a.dev_status);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  if (a.xperm != nullptr) {
+  {
+    // packed rows and their scales, or (gather mode) the scales alone
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int pgrid = std::max(1, std::min((npairs + kRouteWarps - 1) / kRouteWarps, 8 * sms));
     err = launch_pdl(moe_pack_kernel, dim3(pgrid), dim3(kRouteThreads), 0, stream, (const int32_t*)a.pairs,
-                     (const int32_t*)a.offsets, a.n_expert, a.n_used, a.X, a.ldx_token, a.ldx_slot, a.K, a.xperm);
+                     (const int32_t*)a.offsets, a.n_expert, a.n_used, a.X, a.ldx_token, a.ldx_slot, a.K, a.xperm,
+                     a.xup);
     if (err != cudaSuccess) return err;
   }
   if (a.xperm == nullptr) return launch_tc<kTableGather, 64, 2>(tmC, tmP, tmC, p, stream);
@@ -817,6 +912,7 @@ bool q4_umma_eligible(int64_t M, int64_t N, int64_t K) {
 }
 
 cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream) {
+  __half* Xh = static_cast<__half*>(a.act16);   // the activations as scaled f16 rows [M][K]
   MoeParams p{};
   p.tiles_per_expert = (int64_t)(a.N / 32) * (a.K / 256);
   p.N = a.N;
@@ -831,6 +927,7 @@ cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaS
   p.Y = a.Y;
   p.ldy_token = a.ldy;
   p.dense_rows = a.M;
+  p.xup = reinterpret_cast<const float*>(static_cast<const char*>(a.act16) + act_f16_scale_offset(a.M, a.K));
   p.dev_status = dev_status;
   if (p.tiles_per_expert > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
   CUtensorMap tmC, tmP, tmX;
@@ -845,12 +942,13 @@ cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaS
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int c192 = (a.M + 191) / 192, c128 = (a.M + 127) / 128;
   const int tok = a.M <= 64 ? 64 : (a.M > 128 && c192 < c128 && (int64_t)p.nrb * c192 >= sms ? 192 : 128);
-  if (!make_tmap_2d(&tmX, true, const_cast<__nv_bfloat16*>(a.X), (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.ldx * 2,
-                    64, (uint32_t)tok))
+  if (!make_tmap_2d(&tmX, true, Xh, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64, (uint32_t)tok))
     return cudaErrorInvalidValue;
   p.dense_chunks = (a.M + tok - 1) / tok;
   if ((int64_t)p.nrb * p.dense_chunks > INT32_MAX) return cudaErrorInvalidValue;
   p.n_units = p.nrb * p.dense_chunks;
+  const cudaError_t err = launch_act_to_f16(a.X, a.ldx, a.M, a.K, a.act16, stream);
+  if (err != cudaSuccess) return err;
   if (tok == 64) return launch_tc<kDense, 64, 1>(tmC, tmP, tmX, p, stream);
   if (tok == 192) return launch_tc<kDense, 192, 1>(tmC, tmP, tmX, p, stream);
   return launch_tc<kDense, 128, 1>(tmC, tmP, tmX, p, stream);

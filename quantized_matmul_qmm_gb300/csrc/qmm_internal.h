@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include <utility>
@@ -92,13 +93,15 @@ size_t w8_umma_workspace_bytes(int64_t K, int64_t N);
 cudaError_t launch_w8_gemm_umma(const int8_t* codes, const float* scales, int N, int K,
                                 const __nv_bfloat16* X, int64_t ldx, int M, float* Y, int64_t ldy,
                                 void* workspace, int32_t* dev_status, cudaStream_t stream);
-// The pair GEMM alone, on bf16 weights B16 [N][padded_k(K)] that an earlier
+// The pair GEMM alone, on 16-bit weights W16 [N][padded_k(K)] that an earlier
 // launch in the stream wrote; scales [N][nb] multiply each kPairChunkK-column
-// chunk of the accumulator.
+// chunk of the accumulator.  bf16 weights take bf16 activations X; f16
+// weights take f16 activation rows X (act16.cu) whose inverse scales x_up
+// multiply each output row.
 constexpr int kPairChunkK = 1024;
-cudaError_t launch_bf16w_gemm_umma(const __nv_bfloat16* B16, const float* scales, int nb, int N, int K,
-                                   const __nv_bfloat16* X, int64_t ldx, int M, float* Y, int64_t ldy,
-                                   int32_t* dev_status, cudaStream_t stream);
+cudaError_t launch_w16_gemm_umma(const void* W16, bool f16, const float* scales, int nb, int N, int K,
+                                 const void* X, int64_t ldx, const float* x_up, int M, float* Y, int64_t ldy,
+                                 int32_t* dev_status, cudaStream_t stream);
 
 // ---- more weight formats (formats.cu): Q4_K -> q4_1 repack, Q8 tiles ----
 constexpr int kQ8TileBytes = 8704;   // 8192 code bytes + 256 bf16 scales
@@ -109,9 +112,17 @@ cudaError_t launch_repack_q4k(const uint8_t* src, int64_t row_bytes, int N, int 
                               cudaStream_t stream);
 cudaError_t launch_pack_q8(const float* W, int64_t ldw, int N, int K, int layout, uint8_t* tiles,
                            cudaStream_t stream);
-size_t q8_gemm_workspace_bytes(int64_t N, int64_t K);   // the M > kQ8GemvMaxM route
+size_t q8_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);   // the M > kQ8GemvMaxM route
 cudaError_t launch_q8_gemm(const uint8_t* tiles, int layout, int N, int K, const __nv_bfloat16* X, int64_t ldx,
                            int M, float* Y, int64_t ldy, void* workspace, int32_t* dev_status, cudaStream_t stream);
+
+// ---- f16 activation operands (act16.cu) ----
+// Each bf16 row scaled by a power of two into [2^14, 2^15) and rounded to f16
+// (exact), with the inverse factor kept per row: f16 [rows][K], then fp32
+// [rows], each padded to 256 bytes.
+size_t act_f16_bytes(int64_t rows, int64_t K);
+inline size_t act_f16_scale_offset(int64_t rows, int64_t K) { return ((size_t)rows * K * 2 + 255) / 256 * 256; }
+cudaError_t launch_act_to_f16(const __nv_bfloat16* X, int64_t ldx, int rows, int K, void* out, cudaStream_t stream);
 
 // ---- q4 kernels (q4_mma.cu, q4_umma.cu) ----
 struct Q4DenseArgs {
@@ -121,6 +132,7 @@ struct Q4DenseArgs {
   int64_t ldx;
   float* Y;
   int64_t ldy;
+  void* act16;   // tensor-core route: act_f16_bytes(M, K) of workspace
 };
 cudaError_t launch_q4_gemv(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream);
 cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, int32_t* dev_status, cudaStream_t stream);
@@ -139,14 +151,23 @@ struct Q4MoEArgs {
   int64_t ldy_token, ldy_slot;
   int32_t* offsets;   // workspace: [n_expert + 1]
   int32_t* pairs;     // workspace: [T * n_used]
-  __nv_bfloat16* xperm;   // workspace: [T * n_used][K] packed activations, or null
+  float* xup;         // workspace: [T * n_used] inverse activation-row scales, by grouped rank
+  __half* xperm;      // workspace: [T * n_used][K] packed f16 activations, or null (gather mode)
   int32_t* dev_status;
 };
 constexpr int64_t kMaxExperts = 4096;
-// routing tables only (enough for the gather path)
+// routing tables and row scales only (enough for the gather path)
 size_t q4_moe_table_bytes(int64_t n_expert, int64_t n_used, int64_t T);
 // tables + packed activations (the full workspace)
 size_t q4_moe_workspace_bytes(int64_t n_expert, int64_t n_used, int64_t T, int64_t K);
 cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream);
+
+// ---- load-only HBM probe (probe.cu): mode 0 per-thread loads, 1 bulk copies ----
+cudaError_t launch_probe_hbm_read(const void* buf, size_t bytes, int mode, uint32_t* sink, int32_t* dev_status,
+                                  cudaStream_t stream);
+
+// ---- self-test of the bounded-wait error path (selftest.cu) ----
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* dev_status, int64_t* out,
+                                         cudaStream_t stream);
 
 }  // namespace qmm

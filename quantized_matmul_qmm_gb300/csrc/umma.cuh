@@ -158,6 +158,10 @@ QMM_DEV uint4 lds128(uint32_t addr) {
                : "r"(addr));
   return v;
 }
+QMM_DEV void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
 
 // ---- tcgen05 -----------------------------------------------------------------
 QMM_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqmm.so")
 
 QMM_OK, QMM_ERR_INVALID_ARG, QMM_ERR_UNSUPPORTED, QMM_ERR_OVERFLOW_BOUND = 0, 1, 2, 3
-QMM_ERR_CUDA, QMM_ERR_TIMEOUT, QMM_ERR_BAD_EXPERT_ID, QMM_ERR_WORKSPACE = 4, 5, 6, 7
+QMM_ERR_CUDA, QMM_ERR_TIMEOUT, QMM_ERR_BAD_EXPERT_ID, QMM_ERR_WORKSPACE, QMM_ERR_RANGE = 4, 5, 6, 7, 8
 QMM_U8, QMM_S8, QMM_S32, QMM_F32, QMM_BF16 = 1, 2, 3, 4, 5
 DTYPES = {"u8": QMM_U8, "s8": QMM_S8, "s32": QMM_S32, "f32": QMM_F32, "bf16": QMM_BF16}
 TORCH_OUT = {"s32": torch.int32, "f32": torch.float32, "s8": torch.int8, "u8": torch.uint8}
@@ -49,7 +49,8 @@ SIGNATURES = {
                                          _vp]),
     "qmm_pack_q4_size": (_c.c_int, [_i64, _i64, _szp]),
     "qmm_pack_q4": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _sz, _vp]),
-    "qmm_q4_gemm": (_c.c_int, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
+    "qmm_q4_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
+    "qmm_q4_gemm": (_c.c_int, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _vp]),
     "qmm_q4_gemm_id_workspace_size": (_c.c_int, [_i64, _i64, _i64, _i64, _szp]),
     "qmm_q4_gemm_id": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64, _i64,
                                   _vp, _i64, _i64, _vp, _sz, _vp, _vp]),
@@ -64,6 +65,8 @@ SIGNATURES = {
     "qmm_pack_q8": (_c.c_int, [_vp, _i64, _i64, _i64, _c.c_int, _vp, _sz, _vp]),
     "qmm_q8_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
     "qmm_q8_gemm": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_probe_hbm_read": (_c.c_int, [_vp, _sz, _c.c_int, _vp, _vp, _vp]),
+    "qmm_selftest_wait_timeout": (_c.c_int, [_c.c_uint64, _vp, _vp, _vp]),
 }
 QMM_Q8_LAYOUT_KR, QMM_Q8_LAYOUT_SLAB16 = 0, 1
 
@@ -224,13 +227,22 @@ def pack_q4(W: torch.Tensor) -> torch.Tensor:
     return tiles
 
 
-def q4_gemm(tiles: torch.Tensor, N: int, K: int, X: torch.Tensor, Y=None, dev_status=None):
+def q4_gemm_workspace_size(M: int, K: int, N: int) -> int:
+    return _size("qmm_q4_gemm_workspace_size", M, K, N)
+
+
+def q4_gemm(tiles: torch.Tensor, N: int, K: int, X: torch.Tensor, Y=None, workspace=None, dev_status=None):
     """Y[m][n] = sum_k X[m][k] w[n][k]; X bf16 [M][K] on the device."""
     M = X.shape[0]
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
-    _check("qmm_q4_gemm", lib.qmm_q4_gemm(_ptr(tiles), N, K, _ptr(X), M, X.stride(0), _ptr(Y),
-                                          Y.stride(0), _ptr(dev_status), _stream()))
+    if workspace is None:
+        need = q4_gemm_workspace_size(M, K, N)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    _check("qmm_q4_gemm", lib.qmm_q4_gemm(
+        _ptr(tiles), N, K, _ptr(X), M, X.stride(0), _ptr(Y), Y.stride(0), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
     return Y
 
 
@@ -264,7 +276,8 @@ def q4_gemm_id_noalloc(tiles: torch.Tensor, n_expert: int, N: int, K: int, X: to
                        dev_status=None):
     """MUL_MAT_ID through qmm_q4_gemm_id_noalloc: the same result as
     q4_gemm_id, for callers that cannot allocate device memory.  The library
-    keeps the routing tables in its own fixed device array, so the caller
+    keeps the routing tables and activation-row scales in its own fixed device
+    array (and packs the activation rows there when they fit), so the caller
     passes only inputs and the output Y [T][n_used][N] (preallocated).
     Limits: n_expert <= 1024, T * n_used <= 65536."""
     if X.dim() == 2:
@@ -367,3 +380,24 @@ def q8_gemm(tiles: torch.Tensor, layout: int, N: int, K: int, X: torch.Tensor, Y
         _ptr(tiles), int(layout), N, K, _ptr(X), M, X.stride(0), _ptr(Y), Y.stride(0), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
     return Y
+
+
+# ---------------------------------------------------------------------------
+# Diagnostics
+# ---------------------------------------------------------------------------
+
+def selftest_wait_timeout(limit_ns: int, dev_status: torch.Tensor, out: torch.Tensor):
+    """Run the bounded-wait error path on purpose (see qmm_selftest_wait_timeout):
+    dev_status (device int32 [1], zeroed by the caller) receives QMM_ERR_TIMEOUT
+    and out (device int64 [4]) the wait results and times."""
+    _check("qmm_selftest_wait_timeout", lib.qmm_selftest_wait_timeout(int(limit_ns), _ptr(dev_status), _ptr(out),
+                                                                      _stream()))
+    return out
+
+
+def probe_hbm_read(buf: torch.Tensor, mode: int, sink: torch.Tensor, dev_status=None):
+    """Load-only read of the whole of `buf` (see qmm_probe_hbm_read); sink is a
+    device int32/uint32 [1] that normally stays untouched."""
+    nbytes = buf.numel() * buf.element_size()
+    _check("qmm_probe_hbm_read", lib.qmm_probe_hbm_read(_ptr(buf), nbytes, int(mode), _ptr(sink),
+                                                        _ptr(dev_status), _stream()))

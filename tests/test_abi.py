@@ -27,6 +27,7 @@ def test_every_declared_symbol_is_exported(qmm):
 def test_status_strings(qmm):
     assert qmm.status_string(0) == "QMM_OK"
     assert qmm.status_string(6) == "QMM_ERR_BAD_EXPERT_ID"
+    assert qmm.status_string(8) == "QMM_ERR_RANGE"
     assert qmm.status_string(99) == "QMM_ERR_UNKNOWN"
 
 
@@ -37,8 +38,12 @@ def test_size_queries(qmm):
     assert qmm.pack_q4_size(32, 256) == 5120
     assert qmm.pack_q4_size(151936, 1024) == 97239040
     assert qmm.int8_gemm_workspace_size(16, 1024, 1024) >= 0
-    # MUL_MAT_ID: routing tables (256-byte padded) + packed bf16 activation rows
-    assert qmm.q4_gemm_id_workspace_size(128, 8, 512, 2048) == 768 + 16384 + 4096 * 2048 * 2
+    # MUL_MAT_ID: routing tables and row scales (256-byte padded) + packed f16 activation rows
+    assert qmm.q4_gemm_id_workspace_size(128, 8, 512, 2048) == 768 + 16384 + 16384 + 4096 * 2048 * 2
+    # dense q4: nothing for the decode GEMV; f16 activation rows + row scales for the tensor-core route
+    assert qmm.q4_gemm_workspace_size(16, 1024, 64) == 0
+    assert qmm.q4_gemm_workspace_size(17, 1024, 64) == 17 * 1024 * 2 + 256
+    assert qmm.q4_gemm_workspace_size(300, 2048, 96) == 300 * 2048 * 2 + 1280
     L = qmm.lib
     sz = ctypes.c_size_t(0)
     assert L.qmm_q4_gemm_id_workspace_size(128, 8, 512, 300, ctypes.byref(sz)) == qmm.QMM_ERR_UNSUPPORTED
@@ -89,8 +94,13 @@ def test_host_validation_before_launch(qmm):
     rq = qmm.QmmEpilogue(qmm.QMM_S8, None, None, 0, None, 0.0, 0)
     assert g(P, qmm.QMM_S8, 4, 16, 16, 0, P, P, 8, qmm.QMM_S8, 0, ctypes.byref(rq), P, 8, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
     # q4: shapes off the tile grid, X row stride not a multiple of 8
-    assert L.qmm_q4_gemm(P, 33, 256, P, 1, 256, P, 33, None, None) == qmm.QMM_ERR_UNSUPPORTED
-    assert L.qmm_q4_gemm(P, 32, 256, P, 1, 260, P, 32, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_q4_gemm(P, 33, 256, P, 1, 256, P, 33, None, 0, None, None) == qmm.QMM_ERR_UNSUPPORTED
+    assert L.qmm_q4_gemm(P, 32, 256, P, 1, 260, P, 32, None, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    # q4 tensor-core route (M >= 17): missing, short or misaligned workspace
+    assert L.qmm_q4_gemm(P, 32, 256, P, 17, 256, P, 32, None, 0, None, None) == qmm.QMM_ERR_WORKSPACE
+    assert L.qmm_q4_gemm(P, 32, 256, P, 17, 256, P, 32, P, 17 * 256 * 2, None, None) == qmm.QMM_ERR_WORKSPACE
+    assert L.qmm_q4_gemm(P, 32, 256, P, 17, 256, P, 32, ctypes.c_void_p((1 << 20) + 128), 1 << 20, None,
+                         None) == qmm.QMM_ERR_WORKSPACE
     # MUL_MAT_ID: ld_ids < n_used, missing workspace
     assert L.qmm_q4_gemm_id(P, 4, 32, 256, P, 256, 0, P, 2, 3, 5, P, 96, 32, P, 1 << 20, None, None) == qmm.QMM_ERR_INVALID_ARG
     assert L.qmm_q4_gemm_id(P, 4, 32, 256, P, 256, 0, P, 17, 3, 5, P, 96, 32, None, 0, None, None) == qmm.QMM_ERR_WORKSPACE
@@ -160,8 +170,9 @@ def test_format_sizes_and_host_validation(qmm):
     assert qmm.pack_q8_size(32, 256) == 8704
     assert qmm.pack_q8_size(151936, 1024) == 4748 * 4 * 8704
     assert qmm.q8_gemm_workspace_size(16, 1024, 64) == 0
-    assert qmm.q8_gemm_workspace_size(17, 1024, 64) == 64 * 1024 * 2 + 256
-    assert qmm.q8_gemm_workspace_size(17, 2048, 96) == 96 * 2048 * 2 + 768
+    # f16 weights, chunk scales, f16 activation rows, row scales (each rounded up to 256)
+    assert qmm.q8_gemm_workspace_size(17, 1024, 64) == 64 * 1024 * 2 + 256 + 17 * 1024 * 2 + 256
+    assert qmm.q8_gemm_workspace_size(17, 2048, 96) == 96 * 2048 * 2 + 768 + 17 * 2048 * 2 + 256
     L = qmm.lib
     P = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: every call below fails on the host
     sz = ctypes.c_size_t(0)

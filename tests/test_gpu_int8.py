@@ -183,8 +183,12 @@ def test_workload_qwen_projection_m32(qmm, cuda, idx):
 
 
 def test_workload_large_sampled(qmm, cuda):
-    """M=4096 K=N=4608 uint8 x int8, int8 output: 24 sampled rows in full and
-    the column sums/scales exactly."""
+    """M=4096 K=N=4608 uint8 x int8, int8 output, in the launch configuration
+    the benchmark times: one row from every 128-row half of each 256-row pair
+    tile (so every one of the 288 output tiles and both CTAs' halves of it are
+    compared, including the tiles each CTA pair reaches on its later passes),
+    plus the first, last and tile-boundary rows, each in full; and the column
+    sums exactly."""
     c = I.int8_gemm_large()
     dev = cuda
     Bd = c.B.to(dev)
@@ -194,8 +198,9 @@ def test_workload_large_sampled(qmm, cuda):
                         s_w=c.s_w.to(dev), s_y=c.s_y, zp_y=c.zp_y)
     torch.cuda.synchronize()
     got = out.cpu().numpy()
-    rows = np.array([0, 1, 127, 128, 1000, 2047, 2048, 4095] +
-                    list(np.random.default_rng(8).choice(4096, 8, replace=False)))
+    rng = np.random.default_rng(8)
+    halves = np.arange(0, 4096, 128) + rng.integers(0, 128, 32)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, 2047, 2048, 4095], halves]))
     ref = oracle_out(c.A[rows], c.a_type, c.zA, c.B, c.b_type, c.zB, "s8", bias=c.bias,
                      s_x=c.s_x, s_w=c.s_w.numpy(), s_y=c.s_y, zp_y=c.zp_y)
     assert_same(got[rows], ref, "s8")
@@ -222,6 +227,24 @@ def test_umma_route_s32_exact(qmm, cuda, a_type, b_type, M, K, N):
     zB = 0 if b_type == "f32" else 3
     got, _ = gpu_gemm(qmm, cuda, A, a_type, zA, B, b_type, zB, "s32")
     assert_same(got, oracle_out(A, a_type, zA, B, b_type, zB, "s32"), "s32")
+
+
+def test_umma_route_more_tiles_than_pairs_exact(qmm, cuda):
+    """110 output tiles of 256 x 256 (10 x 11), more than the CTA pairs that fit
+    on the GPU, so pairs walk several tiles, alternate their two accumulators
+    across tiles and prefetch the next tile's column constants; K = 1088
+    crosses a 1024-k accumulator chunk.  Every element against the oracle."""
+    M, K, N = 2560, 1088, 2816
+    g = torch.Generator().manual_seed(2560)
+    A = rand_codes(g, "u8", (M, K))
+    B = rand_codes(g, "s8", (K, N))
+    bias = torch.randint(-20000, 20000, (N,), generator=g, dtype=torch.int32)
+    s_w = (torch.rand(N, generator=g) * 9e-3 + 1e-3).float()
+    got, _ = gpu_gemm(qmm, cuda, A, "u8", 130, B, "s8", 5, "s8", bias=bias, s_x=[1.0 / 64], s_w=s_w,
+                      s_y=0.1, zp_y=3)
+    ref = oracle_out(A, "u8", 130, B, "s8", 5, "s8", bias=bias, s_x=1.0 / 64, s_w=s_w.numpy(), s_y=0.1, zp_y=3)
+    assert_same(got, ref, "s8")
+    assert (got == 127).any() and (got == -128).any()
 
 
 @pytest.mark.parametrize("out_type", ["f32", "s8", "u8"])

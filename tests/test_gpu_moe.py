@@ -11,10 +11,11 @@ TOL = 2e-3
 
 
 def table_bytes(E, n_used, T):
-    """Routing tables alone: offsets [E+1] and pair ids [T*n_used], int32,
-    each padded to 256 bytes (the documented workspace layout)."""
+    """Routing tables alone: offsets [E+1] and pair ids [T*n_used], int32, and
+    the activation-row scales [T*n_used], fp32, each padded to 256 bytes (the
+    documented workspace layout)."""
     pad = lambda b: (b + 255) // 256 * 256
-    return pad((E + 1) * 4) + pad(T * n_used * 4)
+    return pad((E + 1) * 4) + 2 * pad(T * n_used * 4)
 
 
 def run_moe(qmm, dev, W, X, ids_buf, ld_ids, n_used, T, status=None, ws_bytes=None):
@@ -152,8 +153,8 @@ def test_workload_moe_full(qmm, cuda, kind):
 
 @pytest.mark.parametrize("kind", ["gate", "down"])
 def test_workload_moe_tables_only_workspace(qmm, cuda, kind):
-    """A workspace holding only the routing tables runs the in-kernel gather
-    of the activation rows; every pair against the oracle."""
+    """A workspace holding only the routing tables and row scales runs the
+    in-kernel gather of the activation rows; every pair against the oracle."""
     c = I.moe_case(kind)
     full = qmm.q4_gemm_id_workspace_size(c.n_expert, c.n_used, c.T, c.K)
     tb = table_bytes(c.n_expert, c.n_used, c.T)

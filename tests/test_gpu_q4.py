@@ -150,3 +150,33 @@ def test_q4_prefill_192_token_chunks(qmm, cuda, M, N, K):
     y, norm = O.q4_gemm(ref_tiles, N, K, xnp(X))
     err = O.normalized_error(Y, y, norm)
     assert err <= TOL, err
+
+
+def test_bounded_wait_times_out_and_context_survives(qmm, cuda):
+    """The device error path of the pipelined kernels: a bounded wait on a
+    barrier nothing arrives on gives up after its limit, QMM_ERR_TIMEOUT
+    reaches dev_status, the block's other wait leaves on the abort flag, the
+    kernel frees its tensor memory and returns; the tensor-core kernels
+    (which allocate tensor memory) then still run correctly."""
+    limit = 5_000_000   # 5 ms
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    out = torch.full((4,), -1, dtype=torch.int64, device=cuda)
+    qmm.selftest_wait_timeout(limit, status, out)
+    torch.cuda.synchronize()
+    r = out.cpu().tolist()
+    assert int(status.item()) == qmm.QMM_ERR_TIMEOUT
+    assert r[0] == 0 and r[1] == 0, r
+    assert limit <= r[2] < limit + 50_000_000, r
+    assert -1_000_000 < r[3] < 20_000_000, r   # the second wait leaves within a suspend interval
+    # the context is usable: a tensor-core prefill GEMM and a second self-test
+    N, K, M = 256, 512, 64
+    g = torch.Generator().manual_seed(99)
+    W = torch.randn((N, K), generator=g) * 0.02
+    X = torch.randn((M, K), generator=g).to(torch.bfloat16)
+    status.zero_()
+    tiles, Y = gpu_q4(qmm, cuda, W, X)
+    y, norm = O.q4_gemm(O.pack_q4(W.numpy()), N, K, xnp(X))
+    assert O.normalized_error(Y, y, norm) <= TOL
+    qmm.selftest_wait_timeout(limit, status, out)
+    torch.cuda.synchronize()
+    assert int(status.item()) == qmm.QMM_ERR_TIMEOUT

@@ -2,9 +2,11 @@
 
 Plugins whose host framework owns all device memory, and latency-critical
 paths that must not call cudaMalloc, use qmm_q4_gemm_id_noalloc.  It keeps its
-routing tables in a fixed array inside the library instead of a workspace
-from the caller.  This file checks, through the C ABI, that two calls in a
-row give what the workspace entry point qmm_q4_gemm_id gives, and that
+routing tables and activation-row scales in a fixed array inside the library
+instead of a workspace from the caller.  Small calls also pack their
+activation rows into that array; larger ones gather the rows inside the
+grouped kernel.  This file checks, through the C ABI, that calls in a row give
+what the workspace entry point qmm_q4_gemm_id gives (both modes), and that
 requests beyond the array's limits are refused.  pytest collects this file
 last on purpose.
 """
@@ -27,9 +29,12 @@ def _case(seed, E, N, K, T, n_used, ld, shared, dev):
 
 
 def test_noalloc_matches_workspace_entry_point_twice(qmm, cuda):
-    # two calls in a row with different routing: the second must not see the first's tables
+    # calls in a row with different routing: each must not see the previous one's tables.
+    # The first two fit their packed activation rows in the array; the third
+    # (512 pairs x K=2048 x 2 bytes = 2 MiB of rows) runs the gather mode.
     for seed, (E, N, K, T, n_used, ld, shared) in ((1, (16, 64, 512, 61, 4, 9, True)),
-                                                   (2, (5, 96, 256, 23, 3, 3, False))):
+                                                   (2, (5, 96, 256, 23, 3, 3, False)),
+                                                   (3, (128, 256, 2048, 64, 8, 17, True))):
         W, ids, X = _case(seed, E, N, K, T, n_used, ld, shared, cuda)
         tiles = torch.cat([qmm.pack_q4(W[e].to(cuda)) for e in range(E)])
         Xd, idsd = X.to(cuda), ids.to(cuda)
