@@ -283,6 +283,37 @@ qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, i
                        int64_t ldx, float* Y, int64_t ldy, void* workspace, size_t ws_bytes,
                        int32_t* dev_status, cudaStream_t stream);
 
+/* One decode GEMV (M = 1) of a grouped call: y = W x for one q4 tile set. */
+typedef struct qmm_q4_gemv_problem {
+  const void* tiles; /* device: one N x K tile set, 16-byte aligned */
+  int64_t N;         /* N % 32 == 0 */
+  int64_t K;         /* K % 256 == 0 */
+  const void* x;     /* device: bf16 [K], 16-byte aligned */
+  float* y;          /* device: fp32 [N], 4-byte aligned */
+} qmm_q4_gemv_problem;
+
+/* Several independent decode GEMVs in one launch: y_i[n] = sum_k x_i[k] w_i[n][k]
+ * for each problem i, the function qmm_q4_gemm computes at M = 1 and with the
+ * same bound (weights never rounded; fp32 summation only, within
+ * 2e-5 * sum_k |x||w|).  Decode runs many small projections, each too small to
+ * keep the memory system busy by itself ("Zaya 8B Q4NX on the AMD NPU", round
+ * 25n: a launch-bound step; round 25p: one stream of packed weights feeding
+ * several matmuls).  The call spreads the tile rows of all problems over the
+ * GPU's SMs, balanced by bytes, so that the group streams as one weight set.
+ *
+ * problems  HOST array of `count` descriptors, read during the call only.
+ *           A y buffer must not overlap any tiles, x or other y of the group.
+ * count     1 <= count; any number of problems (the call launches one kernel
+ *           per 32 problems or per 6,144 tile rows; a problem with K > 16,384
+ *           or more than 6,144 tile rows runs as its own qmm_q4_gemm launch).
+ * Sizes are checked on the host; a bad descriptor returns QMM_ERR_INVALID_ARG
+ * (null pointer, misalignment) or QMM_ERR_UNSUPPORTED (N % 32, K % 256) before
+ * anything is queued.  Results are deterministic: each output is summed in a
+ * fixed order, with no atomics.
+ */
+qmm_status qmm_q4_gemv_group(const qmm_q4_gemv_problem* problems, int64_t count, int32_t* dev_status,
+                             cudaStream_t stream);
+
 /* Workspace of qmm_q4_gemm_id: routing tables for n_expert experts and
  * P = T*n_used (token, slot) pairs (int32 offsets [n_expert+1], int32 pair ids
  * [P] and fp32 activation-row scales [P], each padded to 256 bytes), followed

@@ -6,6 +6,7 @@
 // kernel returns QMM_ERR_UNSUPPORTED.
 #include <cstdio>
 #include <cstdlib>
+#include <vector>
 
 #include "int8_axis.h"
 #include "qmm_internal.h"
@@ -341,6 +342,58 @@ qmm_status qmm_q4_gemm(const void* tiles, int64_t N, int64_t K, const void* X, i
     return cuda_status(launch_q4_gemm_umma(a, dev_status, stream));
   }
   return cuda_status(launch_q4_gemv(a, dev_status, stream));
+}
+
+qmm_status qmm_q4_gemv_group(const qmm_q4_gemv_problem* problems, int64_t count, int32_t* dev_status,
+                             cudaStream_t stream) {
+  if (problems == nullptr || count < 1) return QMM_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < count; ++i) {
+    const qmm_q4_gemv_problem& q = problems[i];
+    if (q.tiles == nullptr || q.x == nullptr || q.y == nullptr || q.N < 1 || q.K < 1) return QMM_ERR_INVALID_ARG;
+    if (q.N % kTileRows != 0 || q.K % kTileCols != 0) return QMM_ERR_UNSUPPORTED;
+    if (q.N > INT32_MAX || q.K > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+    if (!aligned(q.tiles, 16) || !aligned(q.x, 16) || !aligned(q.y, 4)) return QMM_ERR_INVALID_ARG;
+  }
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Consecutive problems share a launch while it holds at most
+  // kMaxGroupProblems problems and kMaxGroupRows tile rows; a problem too
+  // large for the grouped kernel runs the single-problem GEMV.
+  std::vector<GemvGroupProblem> batch;
+  int rows = 0;
+  auto flush = [&]() -> cudaError_t {
+    cudaError_t e = cudaSuccess;
+    if (!batch.empty()) e = launch_q4_gemv_group(batch.data(), (int)batch.size(), sms, dev_status, stream);
+    batch.clear();
+    rows = 0;
+    return e;
+  };
+  for (int64_t i = 0; i < count; ++i) {
+    const qmm_q4_gemv_problem& q = problems[i];
+    const int r = (int)(q.N / kTileRows);
+    if (q.K > kMaxGroupK || r > kMaxGroupRows) {
+      Q4DenseArgs a{};
+      a.tiles = static_cast<const uint8_t*>(q.tiles);
+      a.N = (int)q.N;
+      a.K = (int)q.K;
+      a.M = 1;
+      a.X = static_cast<const __nv_bfloat16*>(q.x);
+      a.ldx = q.K;
+      a.Y = q.y;
+      a.ldy = q.N;
+      const cudaError_t e = launch_q4_gemv(a, dev_status, stream);
+      if (e != cudaSuccess) return cuda_status(e);
+      continue;
+    }
+    if ((int)batch.size() == kMaxGroupProblems || rows + r > kMaxGroupRows) {
+      const cudaError_t e = flush();
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+    batch.push_back({static_cast<const uint8_t*>(q.tiles), static_cast<const __nv_bfloat16*>(q.x), q.y,
+                     (int)q.N, (int)q.K});
+    rows += r;
+  }
+  return cuda_status(flush());
 }
 
 qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64_t T, int64_t K,

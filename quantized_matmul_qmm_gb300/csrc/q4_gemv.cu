@@ -29,6 +29,13 @@
 // row: TMA pays a fixed cost per request, so requests are made large).  Two
 // consumer warps share each row (one 16-row slab each), four rows at a time.  Loads kept in registers
 // (q4_gemv1_regs_kernel) remain for tile rows too long for a useful ring.
+#include <algorithm>
+#include <functional>
+#include <mutex>
+#include <queue>
+#include <utility>
+#include <vector>
+
 #include "qmm_internal.h"
 #include "umma.cuh"
 
@@ -427,6 +434,238 @@ __global__ void __launch_bounds__(kSThreads, 1) q4_gemv1_kernel(const Gemv1SPara
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Grouped M = 1 GEMV: the tile rows of several weight sets in one launch.
+//
+// The host balances whole tile rows over the CTAs by bytes (longest first,
+// each to the least loaded CTA) and passes every CTA its list of
+// (problem, tile row) entries in the launch parameters.  Before the
+// dependency wait a CTA builds its item table (entry, 16-row slab, tile
+// column) in shared memory and warms its rows in L2, so in a chain of
+// launches the next group's weights stream from HBM while this one computes.
+// After the wait one thread bulk-copies every row of the CTA and the x of
+// each of its problems into shared memory (all requests in flight at once,
+// one barrier per row), and the warps walk the items round-robin as their
+// rows land.  Item results go to shared memory and each output is summed
+// over its tile columns in column order, so the result does not depend on
+// which warp took which item.
+// ---------------------------------------------------------------------------
+constexpr int kGWarps = 16;
+constexpr int kGThreads = kGWarps * 32;
+constexpr int kMaxGroupCtas = 256;
+constexpr size_t kGroupSmemBudget = 110 * 1024;   // two CTAs per SM: this launch and the next
+
+template <int kEntries>
+struct GroupParams {
+  GemvGroupProblem prob[kMaxGroupProblems];
+  int32_t* dev_status;
+  int32_t cta_begin[kMaxGroupCtas + 1];   // entries of CTA c: [cta_begin[c], cta_begin[c+1])
+  uint32_t entry[kEntries];               // (problem << 24) | tile row, sorted within a CTA
+};
+
+struct GEnt {            // one tile row of one problem
+  float* y;              // its 32 outputs
+  int32_t ibase;         // first item
+  int32_t tc;            // tile columns
+};
+struct GItem {           // one 16-row slab of one tile
+  uint32_t tile;         // shared address of the tile
+  uint32_t xo;           // x element offset of the tile's 256 columns
+  uint32_t eh;           // entry << 1 | slab
+  uint32_t xbar;         // barrier of the tile's x
+};
+struct GCopy {           // one bulk copy into shared memory
+  uint64_t src;
+  uint32_t dst, bytes;
+};
+
+// One tile slab with x held in registers: xv is block g of x for the lanes
+// that carry it (g == t: the block goes to MMA columns 0..3, g == t + 4: to
+// columns 4..7), xs2 the x sums of the two blocks of this lane's D columns.
+QMM_DEV void g1_tile_rx(const G1Tile& d, const uint4 (&xv)[4], bool lo, bool hi, float2 xs2, int t, float& y0,
+                        float& y1) {
+  uint32_t xa[16], xb[16];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint32_t w[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      xa[4 * v + j] = lo ? w[j] : 0u;
+      xb[4 * v + j] = hi ? w[j] : 0u;
+    }
+  }
+  float acc[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[c][e] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int w = i >> 2, pi = i & 3;
+    const uint32_t a0 = q4_pair_biased(u4_get(d.c[0][0], w), pi);
+    const uint32_t a1 = q4_pair_biased(u4_get(d.c[1][0], w), pi);
+    const uint32_t a2 = q4_pair_biased(u4_get(d.c[0][1], w), pi);
+    const uint32_t a3 = q4_pair_biased(u4_get(d.c[1][1], w), pi);
+    mma_bf16_16816(acc[i & 3], a0, a1, a2, a3, xa[i], xb[i]);
+  }
+  float r[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) r[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
+  const float s00 = bf16lo_to_f32(d.p[0].x), s01 = bf16lo_to_f32(d.p[0].y);
+  const float s10 = bf16lo_to_f32(d.p[1].x), s11 = bf16lo_to_f32(d.p[1].y);
+  y0 = fmaf(s00, r[0], fmaf(fmaf(-128.0f, s00, bf16hi_to_f32(d.p[0].x)), xs2.x, y0));
+  y0 = fmaf(s01, r[1], fmaf(fmaf(-128.0f, s01, bf16hi_to_f32(d.p[0].y)), xs2.y, y0));
+  y1 = fmaf(s10, r[2], fmaf(fmaf(-128.0f, s10, bf16hi_to_f32(d.p[1].x)), xs2.x, y1));
+  y1 = fmaf(s11, r[3], fmaf(fmaf(-128.0f, s11, bf16hi_to_f32(d.p[1].y)), xs2.y, y1));
+}
+
+template <int kEntries>
+__global__ void __launch_bounds__(kGThreads, 2) q4_gemv_group_kernel(const __grid_constant__ GroupParams<kEntries> p) {
+  using namespace umma;
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = smem_align(sm_raw, 128);
+  const int e0 = p.cta_begin[blockIdx.x], e1 = p.cta_begin[blockIdx.x + 1];
+  const int ne = e1 - e0;
+  // layout (the host's size formula follows it): header, x offsets, barriers
+  // (rows, then the x of each problem), copies, entries, items, x behind a
+  // zero block, the rows, item results
+  int32_t* hdr = reinterpret_cast<int32_t*>(sm);                              // [0] items, [1] x elems, [2] row bytes, [3] problems
+  int32_t* xoff = hdr + 4;                                                    // [kMaxGroupProblems] x offset, [.. + 32] x barrier
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xoff + 2 * kMaxGroupProblems); // [ne + kMaxGroupProblems]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + ne + kMaxGroupProblems);
+  GCopy* copies = reinterpret_cast<GCopy*>(bars + ne + kMaxGroupProblems + 2); // [ne + kMaxGroupProblems]
+  GEnt* ents = reinterpret_cast<GEnt*>(copies + ne + kMaxGroupProblems);     // [ne]
+  GItem* items = reinterpret_cast<GItem*>(ents + ne);                         // [nitems]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+
+  pdl_launch_dependents();
+  // ---- before the wait: only the launch parameters are read ----
+  // Warm this CTA's rows in L2.  L2 is where global memory is coherent, so a
+  // row that the previous grid writes is still read correctly: the copies
+  // into shared memory come after the wait.
+  for (int e = (int)threadIdx.x; e < ne; e += kGThreads) {
+    const uint32_t en = p.entry[e0 + e];
+    const GemvGroupProblem& pr = p.prob[en >> 24];
+    const uint32_t row_bytes = (uint32_t)(pr.K / 256) * (uint32_t)kTileBytes;
+    bulk_prefetch_l2(pr.tiles + (int64_t)(en & 0xFFFFFFu) * row_bytes, row_bytes);
+  }
+  if (threadIdx.x == 0) {
+    int it = 0, nd = 0, xo = 32, last = -1, rb = 0;
+    for (int e = 0; e < ne; ++e) {
+      const uint32_t en = p.entry[e0 + e];
+      const int pi = (int)(en >> 24);
+      const int tc = p.prob[pi].K / 256;
+      if (pi != last) {
+        xoff[pi] = xo;
+        xoff[kMaxGroupProblems + pi] = ne + nd;
+        copies[ne + nd] = {reinterpret_cast<uint64_t>(p.prob[pi].X), (uint32_t)xo * 2u, (uint32_t)p.prob[pi].K * 2u};
+        mbar_init(&bars[ne + nd], 1);
+        ++nd;
+        xo += p.prob[pi].K;
+        last = pi;
+      }
+      ents[e].y = p.prob[pi].Y + (int64_t)(en & 0xFFFFFFu) * 32;
+      ents[e].ibase = it;
+      ents[e].tc = tc;
+      it += 2 * tc;
+      const uint32_t row_bytes = (uint32_t)tc * (uint32_t)kTileBytes;
+      copies[e] = {reinterpret_cast<uint64_t>(p.prob[pi].tiles + (int64_t)(en & 0xFFFFFFu) * row_bytes), (uint32_t)rb,
+                   row_bytes};
+      mbar_init(&bars[e], 1);
+      rb += (int)row_bytes;
+    }
+    hdr[0] = it;
+    hdr[1] = xo;
+    hdr[2] = rb;
+    hdr[3] = nd;
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int nitems = hdr[0], xelems = hdr[1], ncopies = ne + hdr[3];
+  uint8_t* xraw = reinterpret_cast<uint8_t*>(items + nitems);
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(xraw + ((16 - (smem_u32(xraw) & 15)) & 15));   // 32 zeros, then x's
+  uint8_t* rows = reinterpret_cast<uint8_t*>(xs + xelems);                     // the CTA's rows (16-byte aligned)
+  float* part = reinterpret_cast<float*>(rows + hdr[2]);                       // [nitems][16]
+  if ((int)threadIdx.x < ne) {
+    const int e = (int)threadIdx.x;   // the host keeps ne <= kGThreads
+    const int pi = (int)(p.entry[e0 + e] >> 24);
+    const int tc = ents[e].tc;
+    const uint32_t row = smem_u32(rows) + copies[e].dst;
+    GItem* it = items + ents[e].ibase;
+    for (int h = 0; h < 2; ++h)
+      for (int c = 0; c < tc; ++c)
+        it[h * tc + c] = {row + (uint32_t)c * (uint32_t)kTileBytes, (uint32_t)(xoff[pi] + 256 * c),
+                          (uint32_t)(e << 1 | h), (uint32_t)xoff[kMaxGroupProblems + pi]};
+  }
+  if (threadIdx.x < 4) reinterpret_cast<uint4*>(xs)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+
+  // ---- after the wait: tiles, x and y may belong to the previous grid ----
+  pdl_wait();
+  if (warp == 0) {
+    // every copy of the CTA in flight at once, issued by the lanes of one warp
+    const uint32_t xbase = smem_u32(xs), rbase = smem_u32(rows);
+    for (int c = lane; c < ncopies; c += 32) {
+      const GCopy cp = copies[c];
+      mbar_arrive_expect_tx(&bars[c], cp.bytes);
+      bulk_g2s((c < ne ? rbase : xbase) + cp.dst, reinterpret_cast<const void*>(cp.src), cp.bytes, &bars[c]);
+    }
+  }
+
+  const bool lo = (g == t), hi = (g == t + 4);
+  const bool owner = lo || hi;
+  // lanes 5b (b < 4) and 5b - 4 (b >= 4) carry block b of x
+  const int src0 = 2 * t < 4 ? 10 * t : 10 * t - 4, src1 = 2 * t + 1 < 4 ? 10 * t + 5 : 10 * t + 1;
+  for (int it = warp; it < nitems; it += kGWarps) {
+    const GItem im = items[it];
+    if (!__all_sync(0xffffffffu, mbar_wait(&bars[im.xbar], 0, abort_flag, p.dev_status) &&
+                                     mbar_wait(&bars[im.eh >> 1], 0, abort_flag, p.dev_status)))
+      break;
+    G1Tile d;
+    g1_lds(d, im.tile, 16 * (int)(im.eh & 1) + g, t);
+    uint4 xv[4];
+    const uint32_t xa = smem_u32(xs + (owner ? im.xo + 32 * g : 0u));
+#pragma unroll
+    for (int v = 0; v < 4; ++v) xv[v] = lds128(xa + 16u * v);
+    float own = 0.f;
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      own += (bf16lo_to_f32(xv[v].x) + bf16hi_to_f32(xv[v].x)) + (bf16lo_to_f32(xv[v].y) + bf16hi_to_f32(xv[v].y)) +
+             (bf16lo_to_f32(xv[v].z) + bf16hi_to_f32(xv[v].z)) + (bf16lo_to_f32(xv[v].w) + bf16hi_to_f32(xv[v].w));
+    const float2 xs2 = make_float2(__shfl_sync(0xffffffffu, own, src0), __shfl_sync(0xffffffffu, own, src1));
+    float y0 = 0.f, y1 = 0.f;
+    g1_tile_rx(d, xv, lo, hi, xs2, t, y0, y1);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+    if (t == 0) {
+      part[it * 16 + g] = y0;
+      part[it * 16 + g + 8] = y1;
+    }
+  }
+  __syncthreads();
+  if (*abort_flag) {
+    // copies nobody waited for may still be landing: let them land first
+    if (threadIdx.x == 0)
+      for (int c = 0; c < ncopies; ++c)
+        mbar_wait(&bars[c], 0, abort_flag, nullptr, 50000000ull) || mbar_try_wait(&bars[c], 0);
+    return;
+  }
+  // each output: its slab's items summed in tile-column order
+  for (int o = threadIdx.x; o < ne * 32; o += kGThreads) {
+    const int le = o >> 5, r = o & 31, h = r >> 4, i = r & 15;
+    const GEnt en = ents[le];
+    const float* pp = part + (en.ibase + h * en.tc) * 16 + i;
+    float s = 0.f;
+    for (int c = 0; c < en.tc; ++c) s += pp[c * 16];
+    en.y[r] = s;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, int32_t* dev_status, cudaStream_t stream) {
@@ -473,6 +712,128 @@ cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, int32_t* dev_status, 
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(q4_gemv1_regs_kernel, dim3(grid), dim3(kWarps * 32), smem, stream, p);
+}
+
+
+namespace {
+
+// Balanced assignment of tile rows to CTAs, cached by the group's shapes
+// (the pointers change from call to call, the plan does not).
+struct GroupPlan {
+  std::vector<int> key;                 // grid, then (N, K) per problem
+  std::vector<int32_t> cta_begin;       // [grid + 1]
+  std::vector<uint32_t> entry;          // (problem << 24) | tile row
+  size_t smem = 0;
+};
+
+void build_group_plan(const GemvGroupProblem* probs, int n, int grid, GroupPlan& plan) {
+  struct Row { int64_t bytes; int pi, tr; };
+  std::vector<Row> rows;
+  for (int pi = 0; pi < n; ++pi)
+    for (int tr = 0; tr < probs[pi].N / 32; ++tr) rows.push_back({(int64_t)(probs[pi].K / 256) * kTileBytes, pi, tr});
+  // longest first (stable, so rows of equal size keep problem and row order)
+  std::stable_sort(rows.begin(), rows.end(), [](const Row& a, const Row& b) { return a.bytes > b.bytes; });
+  using Load = std::pair<int64_t, int>;   // (bytes so far, cta): the least loaded, then the lowest index
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int c = 0; c < grid; ++c) heap.push({0, c});
+  std::vector<std::vector<uint32_t>> per(grid);
+  for (const Row& r : rows) {
+    Load l = heap.top();
+    heap.pop();
+    per[l.second].push_back(((uint32_t)r.pi << 24) | (uint32_t)r.tr);
+    l.first += r.bytes;
+    heap.push(l);
+  }
+  plan.cta_begin.assign(grid + 1, 0);
+  plan.entry.clear();
+  plan.smem = 0;
+  for (int c = 0; c < grid; ++c) {
+    std::sort(per[c].begin(), per[c].end());
+    plan.cta_begin[c] = (int32_t)plan.entry.size();
+    const int ne = (int)per[c].size();
+    int items = 0, last = -1;
+    size_t xk = 0, row_bytes = 0;
+    for (uint32_t en : per[c]) {
+      const int pi = (int)(en >> 24);
+      items += 2 * (probs[pi].K / 256);
+      row_bytes += (size_t)(probs[pi].K / 256) * kTileBytes;
+      if (pi != last) { xk += probs[pi].K; last = pi; }
+      plan.entry.push_back(en);
+    }
+    // must match the kernel's layout: alignment slack, header and x tables,
+    // barriers, copies, entries, items, zero block and x, rows, item results
+    const size_t smem = 128 + 16 + 8 * (size_t)kMaxGroupProblems + 8 * (size_t)(ne + kMaxGroupProblems + 2) +
+                        16 * (size_t)(ne + kMaxGroupProblems) + 16 * (size_t)ne + 16 * (size_t)items + 16 +
+                        2 * (32 + xk) + row_bytes + 64 * (size_t)items;
+    // one thread per entry builds the item table
+    plan.smem = std::max(plan.smem, ne > kGThreads ? SIZE_MAX : smem);
+  }
+  plan.cta_begin[grid] = (int32_t)plan.entry.size();
+}
+
+std::mutex g_plan_mu;
+std::vector<GroupPlan> g_plans;   // a few recent shapes, most recent last
+
+template <int kEntries>
+cudaError_t launch_group_instance(const GemvGroupProblem* probs, int n, const GroupPlan& plan, int32_t* dev_status,
+                                  cudaStream_t stream) {
+  static GroupParams<kEntries> p;   // host staging copy; the launch copies it into the parameter space
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < n; ++i) p.prob[i] = probs[i];
+  p.dev_status = dev_status;
+  const int grid = (int)plan.cta_begin.size() - 1;
+  std::copy(plan.cta_begin.begin(), plan.cta_begin.end(), p.cta_begin);
+  std::copy(plan.entry.begin(), plan.entry.end(), p.entry);
+  const cudaError_t e = cudaFuncSetAttribute(q4_gemv_group_kernel<kEntries>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(q4_gemv_group_kernel<kEntries>, dim3(grid), dim3(kGThreads), plan.smem, stream, p);
+}
+
+}  // namespace
+
+cudaError_t launch_q4_gemv_group(const GemvGroupProblem* probs, int n, int sms, int32_t* dev_status,
+                                 cudaStream_t stream) {
+  int rows = 0;
+  for (int i = 0; i < n; ++i) rows += probs[i].N / 32;
+  const int grid = std::min(std::min(rows, sms), kMaxGroupCtas);
+  std::vector<int> key{grid};
+  for (int i = 0; i < n; ++i) { key.push_back(probs[i].N); key.push_back(probs[i].K); }
+  GroupPlan plan;
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    bool hit = false;
+    for (size_t i = 0; i < g_plans.size(); ++i)
+      if (g_plans[i].key == key) { plan = g_plans[i]; hit = true; break; }
+    if (!hit) {
+      plan.key = key;
+      build_group_plan(probs, n, grid, plan);
+      if (g_plans.size() >= 8) g_plans.erase(g_plans.begin());
+      g_plans.push_back(plan);
+    }
+  }
+  if (plan.smem > kGroupSmemBudget) {
+    // too much per CTA in one launch: halve the group (a single problem this
+    // large runs the single-problem kernel)
+    if (n == 1) {
+      Q4DenseArgs a{};
+      a.tiles = probs[0].tiles;
+      a.N = probs[0].N;
+      a.K = probs[0].K;
+      a.M = 1;
+      a.X = probs[0].X;
+      a.ldx = probs[0].K;
+      a.Y = probs[0].Y;
+      a.ldy = probs[0].N;
+      return launch_q4_gemv1(a, sms, dev_status, stream);
+    }
+    const cudaError_t e = launch_q4_gemv_group(probs, n / 2, sms, dev_status, stream);
+    if (e != cudaSuccess) return e;
+    return launch_q4_gemv_group(probs + n / 2, n - n / 2, sms, dev_status, stream);
+  }
+  if (rows <= 1024) return launch_group_instance<1024>(probs, n, plan, dev_status, stream);
+  return launch_group_instance<kMaxGroupRows>(probs, n, plan, dev_status, stream);
 }
 
 }  // namespace qmm

@@ -136,6 +136,18 @@ struct Q4DenseArgs {
 };
 cudaError_t launch_q4_gemv(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream);
 cudaError_t launch_q4_gemv1(const Q4DenseArgs& a, int sms, int32_t* dev_status, cudaStream_t stream);
+// grouped M = 1 GEMV (q4_gemv.cu)
+struct GemvGroupProblem {
+  const uint8_t* tiles;
+  const __nv_bfloat16* X;
+  float* Y;
+  int N, K;
+};
+constexpr int kMaxGroupProblems = 32;   // problems per grouped launch
+constexpr int kMaxGroupRows = 6144;     // tile rows per grouped launch
+constexpr int kMaxGroupK = 16384;       // larger K runs the single-problem kernel
+cudaError_t launch_q4_gemv_group(const GemvGroupProblem* probs, int n, int sms, int32_t* dev_status,
+                                 cudaStream_t stream);
 bool q4_umma_eligible(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaStream_t stream);
 

@@ -33,6 +33,10 @@ class QmmEpilogue(ctypes.Structure):
                 ("s_w", _vp), ("s_y", _c.c_float), ("zp_y", _i32)]
 
 
+class QmmQ4GemvProblem(ctypes.Structure):
+    _fields_ = [("tiles", _vp), ("N", _i64), ("K", _i64), ("x", _vp), ("y", _vp)]
+
+
 SIGNATURES = {
     "qmm_status_string": (_c.c_char_p, [_c.c_int]),
     "qmm_version": (_c.c_int, []),
@@ -51,6 +55,7 @@ SIGNATURES = {
     "qmm_pack_q4": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "qmm_q4_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
     "qmm_q4_gemm": (_c.c_int, [_vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_q4_gemv_group": (_c.c_int, [_c.POINTER(QmmQ4GemvProblem), _i64, _vp, _vp]),
     "qmm_q4_gemm_id_workspace_size": (_c.c_int, [_i64, _i64, _i64, _i64, _szp]),
     "qmm_q4_gemm_id": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64, _i64,
                                   _vp, _i64, _i64, _vp, _sz, _vp, _vp]),
@@ -244,6 +249,17 @@ def q4_gemm(tiles: torch.Tensor, N: int, K: int, X: torch.Tensor, Y=None, worksp
         _ptr(tiles), N, K, _ptr(X), M, X.stride(0), _ptr(Y), Y.stride(0), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
     return Y
+
+
+def q4_gemv_group(problems, dev_status=None):
+    """Grouped decode GEMVs in one launch: problems is a list of
+    (tiles, N, K, x, y) with x bf16 [K] and y fp32 [N] on the device;
+    y_i = W_i x_i for every i.  Returns the list of y tensors."""
+    arr = (QmmQ4GemvProblem * len(problems))()
+    for i, (tiles, N, K, x, y) in enumerate(problems):
+        arr[i] = QmmQ4GemvProblem(tiles.data_ptr(), N, K, x.data_ptr(), y.data_ptr())
+    _check("qmm_q4_gemv_group", lib.qmm_q4_gemv_group(arr, len(problems), _ptr(dev_status), _stream()))
+    return [y for (_, _, _, _, y) in problems]
 
 
 def q4_gemm_id_workspace_size(n_expert: int, n_used: int, T: int, K: int) -> int:

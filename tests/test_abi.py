@@ -223,3 +223,26 @@ def test_axis_zp_sizes_and_host_validation(qmm):
     bad = qmm.QmmEpilogue(qmm.QMM_BF16, None, None, 0, None, 1.0, 0)
     assert g(P, qmm.QMM_S8, 4, 16, 16, P, P, P, 8, qmm.QMM_S8, P, ctypes.byref(bad), P, 8, P, big, None,
              None) == qmm.QMM_ERR_INVALID_ARG
+
+
+def test_q4_gemv_group_host_validation(qmm):
+    """The grouped decode GEMV checks every descriptor on the host: a bad one
+    fails the whole call before anything is queued."""
+    L = qmm.lib
+    P = 1 << 20   # aligned, never dereferenced
+    Pr = qmm.QmmQ4GemvProblem
+    good = Pr(P, 64, 512, P, P)
+
+    def call(*probs):
+        arr = (Pr * len(probs))(*probs)
+        return L.qmm_q4_gemv_group(arr, len(probs), None, None)
+
+    assert L.qmm_q4_gemv_group(None, 1, None, None) == qmm.QMM_ERR_INVALID_ARG
+    arr = (Pr * 1)(good)
+    assert L.qmm_q4_gemv_group(arr, 0, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(good, Pr(P, 48, 512, P, P)) == qmm.QMM_ERR_UNSUPPORTED        # N % 32
+    assert call(good, Pr(P, 64, 500, P, P)) == qmm.QMM_ERR_UNSUPPORTED        # K % 256
+    assert call(good, Pr(None, 64, 512, P, P)) == qmm.QMM_ERR_INVALID_ARG     # null tiles
+    assert call(Pr(P, 64, 512, P + 8, P), good) == qmm.QMM_ERR_INVALID_ARG    # x not 16-byte aligned
+    assert call(good, Pr(P, 64, 512, P, P + 2)) == qmm.QMM_ERR_INVALID_ARG    # y not 4-byte aligned
+    assert call(good, Pr(P, 0, 512, P, P)) == qmm.QMM_ERR_INVALID_ARG         # empty problem
