@@ -140,6 +140,7 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
     if ((M + 127) / 128 > INT32_MAX || (N + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;
     return cuda_status(launch_int8_gemm_umma(a, workspace, dev_status, stream));
   }
+  if (int8_small_eligible(M, K, N)) return cuda_status(launch_int8_small(a, stream));
   if ((M + 31) / 32 > 65535) return QMM_ERR_UNSUPPORTED;
   return cuda_status(launch_int8_gemm_mma(a, stream));
 }

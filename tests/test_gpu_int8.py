@@ -293,3 +293,41 @@ def test_umma_route_needs_workspace(qmm, cuda):
         qmm.int8_gemm(A, "u8", 0, packed, col_sum, N, "s8", 0, "s32",
                       workspace=torch.empty(16, dtype=torch.uint8, device=cuda))
     assert e.value.status == qmm.QMM_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------------------
+# small-M route (M <= 64): f16 MMA on exact integer codes, clusters of 8 CTAs
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M,K", [(16, 1024), (32, 2048), (48, 4608), (64, 4608), (16, 20000)])
+def test_small_route_extreme_codes_exact(qmm, cuda, M, K):
+    """Every product at its largest magnitude (A' = B' = -128, with one row at
+    A' = +127 and one column at B' = +127): the fp32 chunks of 1024 k reach
+    2^24 exactly and are drained into int32; K = 20000 spans 20 chunks."""
+    N = 72
+    A = torch.zeros((M, K), dtype=torch.uint8)
+    A[1] = 255
+    B = torch.full((K, N), -128, dtype=torch.int8)
+    B[:, 1] = 127
+    got, _ = gpu_gemm(qmm, cuda, A, "u8", 128, B, "s8", 0, "s32")
+    assert_same(got, oracle_out(A, "u8", 128, B, "s8", 0, "s32"), "s32")
+
+
+@pytest.mark.parametrize("a_type,b_type,out_type", [("u8", "s8", "s8"), ("s8", "u8", "f32"), ("u8", "f32", "u8")])
+@pytest.mark.parametrize("M,K,N", [(64, 4608, 200), (48, 3000, 65), (2, 130, 1), (31, 20000, 100)])
+def test_small_route_epilogues_exact(qmm, cuda, a_type, b_type, out_type, M, K, N):
+    """Zero points on both sides (row sums needed), bias, per-row s_x, every
+    output type; K not a multiple of 64 and N not a multiple of 64."""
+    g = torch.Generator().manual_seed(M + K + N)
+    A = rand_codes(g, a_type, (M, K))
+    B = torch.randn((K, N), generator=g) * 0.02 if b_type == "f32" else rand_codes(g, b_type, (K, N))
+    zA = 37 if a_type == "u8" else -21
+    zB = 0 if b_type == "f32" else (200 if b_type == "u8" else 5)
+    bias = torch.randint(-5000, 5000, (N,), generator=g, dtype=torch.int32)
+    s_x = (torch.rand(M, generator=g) * 0.01 + 0.001).numpy()
+    s_w = (torch.rand(N, generator=g) * 9e-3 + 1e-3).float()
+    s_y = 40.0 if out_type in ("s8", "u8") else 1.0
+    got, _ = gpu_gemm(qmm, cuda, A, a_type, zA, B, b_type, zB, out_type, bias=bias, s_x=s_x, s_x_stride=1,
+                      s_w=s_w, s_y=s_y, zp_y=3 if out_type == "u8" else -2)
+    ref = oracle_out(A, a_type, zA, B, b_type, zB, out_type, bias=bias, s_x=s_x, s_w=s_w.numpy(), s_y=s_y,
+                     zp_y=3 if out_type == "u8" else -2)
+    assert_same(got, ref, out_type)
