@@ -18,10 +18,11 @@
  *   pointers.
  * - The caller allocates and owns every buffer.  No entry point allocates or
  *   frees device memory, synchronises the stream, or keeps mutable state
- *   between calls.  There are two exceptions: a per-process cache of the
- *   driver entry point used to build TMA descriptors, and the fixed scratch
- *   array of qmm_q4_gemm_id_noalloc (see there).  Pointers are borrowed until
- *   the work queued on `stream` has finished.
+ *   between calls.  There are three exceptions: a per-process cache of the
+ *   driver entry point used to build TMA descriptors, a per-process cache of
+ *   the grouped GEMV's launch plans (keyed by the problems' shapes), and the
+ *   fixed scratch array of qmm_q4_gemm_id_noalloc (see there).  Pointers are
+ *   borrowed until the work queued on `stream` has finished.
  * - Work is queued on `stream` and runs asynchronously.  Argument errors are
  *   found on the host and returned at once, and nothing is launched when a
  *   check fails.
@@ -128,7 +129,10 @@ qmm_status qmm_int8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t*
 /* Y = A (x) packB with zero points, bias and the chosen output.
  *
  * A        [M][K] uint8 or int8 (a_type), row stride lda bytes: lda >= K,
- *          lda % 16 == 0, base 16-byte aligned.  zA in A's own domain.
+ *          lda % 16 == 0, base 16-byte aligned.  zA in A's own domain.  The
+ *          tensor-core route (M >= 256) reads whole 16-byte groups, so A must
+ *          be readable for (M - 1) * lda + roundup(K, 16) bytes, as an
+ *          [M][lda] tensor is; the bytes past K do not change the result.
  * packedB  from qmm_pack_b_int8 with the same K and N; col_sum from the same call.
  * b_orig_type  the b_type given to packB (QMM_U8, QMM_S8 or QMM_F32); zB is in
  *          that domain and must be 0 for QMM_F32 weights (symmetric).
@@ -153,6 +157,39 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
                          qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out,
                          int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
                          cudaStream_t stream);
+
+/* One int8 GEMM of a grouped call: the arguments of qmm_int8_gemm, with the
+ * epilogue held by value. */
+typedef struct qmm_int8_problem {
+  const void* A;
+  qmm_dtype a_type;
+  int64_t M, K, lda;
+  int32_t zA;
+  const void* packedB;
+  const int32_t* col_sum;
+  int64_t N;
+  qmm_dtype b_orig_type;
+  int32_t zB;
+  qmm_epilogue ep;
+  void* out;
+  int64_t ldo;
+} qmm_int8_problem;
+
+/* Several independent small-M int8 GEMMs in one launch (one per 16 problems):
+ * each computes exactly what qmm_int8_gemm computes for its arguments,
+ * bit-exact.  Small batches of tokens run several projections whose weight
+ * streams are each too short to keep the GPU busy ("The ONNX pack: weights to
+ * Q4NX, matmuls to our kernels, no VitisAI", "What works today": the per-call
+ * cost of the M = 16 / 32 projection GEMMs); one launch streams them together.
+ *
+ * problems  HOST array of `count` descriptors, read during the call only.
+ *           Every problem needs M <= 64 (else QMM_ERR_UNSUPPORTED) and passes
+ *           qmm_int8_gemm's checks (the first failing status is returned
+ *           before anything is queued).  No workspace is used.  An output
+ *           must not overlap any input or other output of the group.
+ */
+qmm_status qmm_int8_gemm_group(const qmm_int8_problem* problems, int64_t count, int32_t* dev_status,
+                               cudaStream_t stream);
 
 /* Workspace of qmm_int8_gemm_axis_zp: the int32 product [M][N] and the row
  * sums [M], each rounded up to 256 bytes, plus qmm_int8_gemm_workspace_size. */

@@ -84,11 +84,15 @@ qmm_status qmm_int8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t*
   return QMM_OK;
 }
 
-qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int64_t lda,
-                         int32_t zA, const void* packedB, const int32_t* col_sum, int64_t N,
-                         qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out,
-                         int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
-                         cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Host checks shared by qmm_int8_gemm and qmm_int8_gemm_group; fills the
+// kernel arguments.
+qmm_status int8_args(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int64_t lda, int32_t zA,
+                     const void* packedB, const int32_t* col_sum, int64_t N, qmm_dtype b_orig_type, int32_t zB,
+                     const qmm_epilogue* ep, void* out, int64_t ldo, Int8GemmArgs& a) {
   if (A == nullptr || packedB == nullptr || col_sum == nullptr || ep == nullptr || out == nullptr)
     return QMM_ERR_INVALID_ARG;
   if (M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
@@ -108,7 +112,7 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
   if (!aligned(out, osz)) return QMM_ERR_INVALID_ARG;
   if (M > INT32_MAX || N > INT32_MAX) return QMM_ERR_UNSUPPORTED;
 
-  Int8GemmArgs a{};
+  a = Int8GemmArgs{};
   a.A = static_cast<const int8_t*>(A);
   a.a_u8 = (a_type == QMM_U8);
   a.M = (int)M;
@@ -133,6 +137,21 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
   a.epi.col_sum = col_sum;
   a.epi.out = out;
   a.epi.ldo = ldo;
+  return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int64_t lda,
+                         int32_t zA, const void* packedB, const int32_t* col_sum, int64_t N,
+                         qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out,
+                         int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                         cudaStream_t stream) {
+  Int8GemmArgs a;
+  const qmm_status st = int8_args(A, a_type, M, K, lda, zA, packedB, col_sum, N, b_orig_type, zB, ep, out, ldo, a);
+  if (st != QMM_OK) return st;
   if (int8_umma_eligible(M, K, N)) {
     // tensor-core route: needs the caller's workspace (never a silent switch)
     const size_t need = int8_umma_workspace_bytes(M, K, N);
@@ -143,6 +162,21 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
   if (int8_small_eligible(M, K, N)) return cuda_status(launch_int8_small(a, stream));
   if ((M + 31) / 32 > 65535) return QMM_ERR_UNSUPPORTED;
   return cuda_status(launch_int8_gemm_mma(a, stream));
+}
+
+qmm_status qmm_int8_gemm_group(const qmm_int8_problem* problems, int64_t count, int32_t* dev_status,
+                               cudaStream_t stream) {
+  (void)dev_status;   // the small-M kernel has no device-side error
+  if (problems == nullptr || count < 1 || count > INT32_MAX) return QMM_ERR_INVALID_ARG;
+  std::vector<Int8GemmArgs> args((size_t)count);
+  for (int64_t i = 0; i < count; ++i) {
+    const qmm_int8_problem& q = problems[i];
+    const qmm_status st = int8_args(q.A, q.a_type, q.M, q.K, q.lda, q.zA, q.packedB, q.col_sum, q.N, q.b_orig_type,
+                                    q.zB, &q.ep, q.out, q.ldo, args[(size_t)i]);
+    if (st != QMM_OK) return st;
+    if (!int8_small_eligible(q.M, q.K, q.N)) return QMM_ERR_UNSUPPORTED;
+  }
+  return cuda_status(launch_int8_small_group(args.data(), (int)count, stream));
 }
 
 namespace {

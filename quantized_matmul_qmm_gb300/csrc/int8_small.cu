@@ -22,6 +22,8 @@
 // (distributed shared memory, one slot per source CTA), and after one
 // cluster barrier every CTA adds its 8 slots and applies the zero-point
 // correction, bias and output conversion to its own 8 columns.
+#include <mutex>
+
 #include "qmm_internal.h"
 #include "umma.cuh"
 
@@ -45,6 +47,16 @@ struct SmallParams {
   Int8Epi epi;
 };
 
+// Several problems in one launch: problem i owns clusters
+// [cluster_begin[i], cluster_begin[i + 1]), one per 64 output columns.
+constexpr int kMaxGroup = 16;
+struct SmallGroup {
+  SmallParams prob[kMaxGroup];
+  int32_t cluster_begin[kMaxGroup + 1];
+  int32_t nprob;
+};
+constexpr size_t kParamSlot = (sizeof(SmallParams) + 15) / 16 * 16;   // the problem's copy in shared memory
+
 // Four int8 codes (A' or B', two's complement) as two f16x2 pairs, exactly:
 // byte b + 128 becomes the low mantissa byte of 1024 (f16 0x6400), and
 // 1024 + 128 is subtracted.
@@ -66,13 +78,27 @@ QMM_DEV void st_dsmem(uint32_t cluster_addr, uint32_t a) {
 
 template <int MT>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWarps * 32)
-    int8_small_kernel(const SmallParams p) {
+    int8_small_kernel(const __grid_constant__ SmallGroup gp) {
   using namespace umma;
-  extern __shared__ __align__(16) uint8_t sm[];
+  extern __shared__ __align__(16) uint8_t sm_all[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int rank = (int)cluster_ctarank();
-  const int n0 = (int)(blockIdx.x / kCluster) * kCols;
+  // this cluster's problem and column block; the problem's parameters are
+  // copied into shared memory once (they are read throughout)
+  const int cl = (int)(blockIdx.x / kCluster);
+  int pi = 0;
+  while (pi + 1 < gp.nprob && gp.cluster_begin[pi + 1] <= cl) ++pi;
+  SmallParams* ps = reinterpret_cast<SmallParams*>(sm_all);
+  {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&gp.prob[pi]);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(ps);
+    for (int i = threadIdx.x; i < (int)(sizeof(SmallParams) / 4); i += kWarps * 32) dst[i] = src[i];
+  }
+  __syncthreads();
+  const SmallParams& p = *ps;
+  uint8_t* sm = sm_all + kParamSlot;
+  const int n0 = (cl - gp.cluster_begin[pi]) * kCols;
   const int S64 = (int)(p.Kp / 64);
   const int s0 = rank * S64 / kCluster, s1 = (rank + 1) * S64 / kCluster;
   const int nsteps = s1 - s0, klen = nsteps * 64;
@@ -234,29 +260,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWarps * 32)
   }
 }
 
-size_t small_smem(int M, int64_t Kp) {
-  const int MT = (M + 15) / 16;
+size_t small_smem(int MT, int64_t Kp) {
   const int S64 = (int)(Kp / 64);
   const int klen = (S64 + kCluster - 1) / kCluster * 64;
-  return (size_t)MT * 16 * (klen + 8) * 2 + (size_t)MT * 16 * (8 * kCluster + kCluster + 1) * 4;
+  return kParamSlot + (size_t)MT * 16 * (klen + 8) * 2 + (size_t)MT * 16 * (8 * kCluster + kCluster + 1) * 4;
 }
 
-template <int MT>
-cudaError_t launch_mt(const SmallParams& p, size_t smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(int8_small_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)((p.N + kCols - 1) / kCols) * kCluster;
-  return launch_pdl(int8_small_kernel<MT>, dim3(grid), dim3(kWarps * 32), smem, stream, p);
-}
-
-}  // namespace
-
-bool int8_small_eligible(int64_t M, int64_t K, int64_t N) {
-  return M >= 1 && M <= 64 && N >= 1 && (N + kCols - 1) / kCols * kCluster <= INT32_MAX &&
-         small_smem((int)M, padded_k(K)) <= kSmemBudget;
-}
-
-cudaError_t launch_int8_small(const Int8GemmArgs& a, cudaStream_t stream) {
+SmallParams small_params(const Int8GemmArgs& a) {
   SmallParams p{};
   p.A = a.A;
   p.lda = a.lda;
@@ -268,12 +278,59 @@ cudaError_t launch_int8_small(const Int8GemmArgs& a, cudaStream_t stream) {
   p.Kp = a.Kp;
   p.need_rowsum = a.need_rowsum ? 1 : 0;
   p.epi = a.epi;
-  const size_t smem = small_smem(a.M, a.Kp);
-  const int MT = (a.M + 15) / 16;
-  if (MT == 1) return launch_mt<1>(p, smem, stream);
-  if (MT == 2) return launch_mt<2>(p, smem, stream);
-  if (MT == 3) return launch_mt<3>(p, smem, stream);
-  return launch_mt<4>(p, smem, stream);
+  return p;
+}
+
+template <int MT>
+cudaError_t launch_mt(const SmallGroup& gp, size_t smem, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(int8_small_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)gp.cluster_begin[gp.nprob] * kCluster;
+  return launch_pdl(int8_small_kernel<MT>, dim3(grid), dim3(kWarps * 32), smem, stream, gp);
+}
+
+}  // namespace
+
+bool int8_small_eligible(int64_t M, int64_t K, int64_t N) {
+  return M >= 1 && M <= 64 && N >= 1 && (N + kCols - 1) / kCols * kCluster <= INT32_MAX &&
+         small_smem((int)(M + 15) / 16, padded_k(K)) <= kSmemBudget;
+}
+
+cudaError_t launch_int8_small_group(const Int8GemmArgs* probs, int n, cudaStream_t stream) {
+  // consecutive problems share a launch, up to kMaxGroup of them
+  for (int b = 0; b < n; b += kMaxGroup) {
+    const int cnt = n - b < kMaxGroup ? n - b : kMaxGroup;
+    static SmallGroup gp;   // host staging copy; the launch copies it into the parameter space
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    gp = SmallGroup{};
+    int MT = 1;
+    int64_t clusters = 0, kp_max = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const Int8GemmArgs& a = probs[b + i];
+      gp.prob[i] = small_params(a);
+      gp.cluster_begin[i] = (int32_t)clusters;
+      clusters += (a.N + kCols - 1) / kCols;
+      MT = MT > (a.M + 15) / 16 ? MT : (a.M + 15) / 16;
+      kp_max = kp_max > a.Kp ? kp_max : a.Kp;
+    }
+    gp.cluster_begin[cnt] = (int32_t)clusters;
+    gp.nprob = cnt;
+    if (clusters * kCluster > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const size_t smem = small_smem(MT, kp_max);
+    if (smem > kSmemBudget) return cudaErrorInvalidConfiguration;
+    cudaError_t e;
+    if (MT == 1) e = launch_mt<1>(gp, smem, stream);
+    else if (MT == 2) e = launch_mt<2>(gp, smem, stream);
+    else if (MT == 3) e = launch_mt<3>(gp, smem, stream);
+    else e = launch_mt<4>(gp, smem, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_int8_small(const Int8GemmArgs& a, cudaStream_t stream) {
+  return launch_int8_small_group(&a, 1, stream);
 }
 
 }  // namespace qmm

@@ -74,6 +74,8 @@ cudaError_t launch_int8_gemm_mma(const Int8GemmArgs& a, cudaStream_t stream);
 // small-M route (int8_small.cu): clusters of 8 CTAs, f16 MMA on exact integer codes
 bool int8_small_eligible(int64_t M, int64_t K, int64_t N);
 cudaError_t launch_int8_small(const Int8GemmArgs& a, cudaStream_t stream);
+// several small-M problems, one launch per 16 (each must be int8_small_eligible)
+cudaError_t launch_int8_small_group(const Int8GemmArgs* probs, int n, cudaStream_t stream);
 // tcgen05 route (int8_umma.cu)
 bool int8_umma_eligible(int64_t M, int64_t K, int64_t N);
 size_t int8_umma_workspace_bytes(int64_t M, int64_t K, int64_t N);

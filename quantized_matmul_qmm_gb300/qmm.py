@@ -33,6 +33,12 @@ class QmmEpilogue(ctypes.Structure):
                 ("s_w", _vp), ("s_y", _c.c_float), ("zp_y", _i32)]
 
 
+class QmmInt8Problem(ctypes.Structure):
+    _fields_ = [("A", _vp), ("a_type", _c.c_int), ("M", _i64), ("K", _i64), ("lda", _i64), ("zA", _i32),
+                ("packedB", _vp), ("col_sum", _vp), ("N", _i64), ("b_orig_type", _c.c_int), ("zB", _i32),
+                ("ep", QmmEpilogue), ("out", _vp), ("ldo", _i64)]
+
+
 class QmmQ4GemvProblem(ctypes.Structure):
     _fields_ = [("tiles", _vp), ("N", _i64), ("K", _i64), ("x", _vp), ("y", _vp)]
 
@@ -45,6 +51,7 @@ SIGNATURES = {
     "qmm_int8_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
     "qmm_int8_gemm": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _c.c_int,
                                  _i32, _c.POINTER(QmmEpilogue), _vp, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_int8_gemm_group": (_c.c_int, [_c.POINTER(QmmInt8Problem), _i64, _vp, _vp]),
     "qmm_int8_gemm_axis_zp_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
     "qmm_int8_gemm_axis_zp": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _c.c_int,
                                          _vp, _c.POINTER(QmmEpilogue), _vp, _i64, _vp, _sz, _vp, _vp]),
@@ -165,6 +172,32 @@ def int8_gemm(A: torch.Tensor, a_type: str, zA: int, packed: torch.Tensor, col_s
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream()))
     return out
+
+
+def int8_gemm_group(problems, dev_status=None):
+    """Several small-M int8 GEMMs (M <= 64) in one launch through
+    qmm_int8_gemm_group.  problems: list of dicts with int8_gemm's arguments
+    (A, a_type, zA, packed, col_sum, N, b_orig_type, zB, out_type, bias, s_x,
+    s_x_stride, s_w, s_y, zp_y, out); `out` is created when absent.  Returns
+    the list of outputs."""
+    arr = (QmmInt8Problem * len(problems))()
+    outs = []
+    for i, d in enumerate(problems):
+        A = d["A"]
+        M, K = A.shape
+        N, ot = d["N"], d.get("out_type", "s32")
+        out = d.get("out")
+        if out is None:
+            out = torch.empty((M, N), dtype=TORCH_OUT[ot], device=A.device)
+        outs.append(out)
+        ep = QmmEpilogue(DTYPES[ot], _ptr(d.get("bias")), _ptr(d.get("s_x")), d.get("s_x_stride", 0),
+                         _ptr(d.get("s_w")), float(d.get("s_y", 1.0)), int(d.get("zp_y", 0)))
+        ptr = lambda t: 0 if t is None else t.data_ptr()
+        arr[i] = QmmInt8Problem(ptr(A), DTYPES[d["a_type"]], M, K, A.stride(0), int(d["zA"]), ptr(d["packed"]),
+                                ptr(d["col_sum"]), N, DTYPES[d["b_orig_type"]], int(d["zB"]), ep, ptr(out),
+                                out.stride(0))
+    _check("qmm_int8_gemm_group", lib.qmm_int8_gemm_group(arr, len(problems), _ptr(dev_status), _stream()))
+    return outs
 
 
 def int8_gemm_axis_zp_workspace_size(M: int, K: int, N: int) -> int:

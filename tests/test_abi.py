@@ -246,3 +246,26 @@ def test_q4_gemv_group_host_validation(qmm):
     assert call(Pr(P, 64, 512, P + 8, P), good) == qmm.QMM_ERR_INVALID_ARG    # x not 16-byte aligned
     assert call(good, Pr(P, 64, 512, P, P + 2)) == qmm.QMM_ERR_INVALID_ARG    # y not 4-byte aligned
     assert call(good, Pr(P, 0, 512, P, P)) == qmm.QMM_ERR_INVALID_ARG         # empty problem
+
+
+def test_int8_gemm_group_host_validation(qmm):
+    """The grouped small-M int8 GEMM applies qmm_int8_gemm's host checks to
+    every problem and refuses M > 64, before anything is queued."""
+    L = qmm.lib
+    P = 1 << 20
+    ep = qmm.QmmEpilogue(qmm.QMM_S32, None, None, 0, None, 1.0, 0)
+
+    def prob(M=16, K=64, lda=64, zA=128, N=32, a_type=qmm.QMM_U8, b_type=qmm.QMM_S8, zB=0, out=P, ldo=32):
+        return qmm.QmmInt8Problem(P, a_type, M, K, lda, zA, P, P, N, b_type, zB, ep, out, ldo)
+
+    def call(*probs):
+        arr = (qmm.QmmInt8Problem * len(probs))(*probs)
+        return L.qmm_int8_gemm_group(arr, len(probs), None, None)
+
+    assert L.qmm_int8_gemm_group(None, 1, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(prob(), prob(M=65)) == qmm.QMM_ERR_UNSUPPORTED            # beyond the small-M route
+    assert call(prob(), prob(lda=72)) == qmm.QMM_ERR_INVALID_ARG          # lda % 16
+    assert call(prob(zA=300)) == qmm.QMM_ERR_INVALID_ARG                  # zero point outside uint8
+    assert call(prob(ldo=31)) == qmm.QMM_ERR_INVALID_ARG                  # ldo < N
+    assert call(prob(K=70000, lda=70016)) == qmm.QMM_ERR_OVERFLOW_BOUND
+    assert call(prob(out=P + 2)) == qmm.QMM_ERR_INVALID_ARG               # int32 output misaligned
