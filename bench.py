@@ -203,6 +203,17 @@ class HotPath:
             self.calls.append((f"q4_moe_{kind}", self._moe(m, tiles, X, ids, Y, wsb), self.moe_launches(m),
                                {"flops": 2 * m.T * m.n_used * m.N * m.K, "weight_bytes": touched * per,
                                 "bytes": touched * per + X.numel() * 2 + Y.numel() * 4}))
+        # the gate/up pair in one call: both weight sets over the gate case's src1 and ids
+        (_, mg, tg, Xg, idsg, _, wsg), (_, _, tu, _, _, _, _) = self.moe[0], self.moe[1]
+        self.Yg2 = torch.empty((mg.T, mg.n_used, mg.N), dtype=torch.float32, device=dev)
+        self.Yu2 = torch.empty_like(self.Yg2)
+        touched = int(torch.unique(mg.ids_buf[:, :mg.n_used]).numel())
+        per = tg.numel() // mg.n_expert
+        self.calls.append(("q4_moe_gateup", lambda: q.q4_gemm_id_pair(
+            tg, tu, mg.n_expert, mg.N, mg.K, Xg, idsg, mg.ld_ids, mg.n_used, mg.T, Y_gate=self.Yg2, Y_up=self.Yu2,
+            workspace=wsg, dev_status=self.status), self.moe_launches(mg),
+            {"flops": 2 * 2 * mg.T * mg.n_used * mg.N * mg.K, "weight_bytes": 2 * touched * per,
+             "bytes": 2 * touched * per + Xg.numel() * 2 + 2 * self.Yg2.numel() * 4}))
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         torch.cuda.synchronize()
 

@@ -388,6 +388,28 @@ qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_
                           int64_t ldy_slot, void* workspace, size_t ws_bytes,
                           int32_t* dev_status, cudaStream_t stream);
 
+/* The gate/up pair of a mixture-of-experts layer in one MUL_MAT_ID call:
+ * Y_gate = MUL_MAT_ID(tiles_gate) and Y_up = MUL_MAT_ID(tiles_up), each exactly
+ * what qmm_q4_gemm_id computes for its weights (same bound).  Both weight sets
+ * read the same ids and the same shared src1 row of each token, so the
+ * routing and the packed activations are built once and one grouped launch
+ * streams both sets ("Zaya 8B Q4NX on the AMD NPU", round 25p: one packed
+ * activation stream feeding several matmuls).
+ *
+ * tiles_gate, tiles_up  n_expert consecutive N x K tile sets each (same N, K).
+ * X       bf16 [T][K] with row stride ldx_token (the shared src1).
+ * Y_gate, Y_up  fp32 [T][n_used][N], both with strides ldy_token / ldy_slot.
+ * workspace  qmm_q4_gemm_id_workspace_size(n_expert, n_used, T, K) bytes (the
+ *         same as one qmm_q4_gemm_id call); a tables-only workspace runs the
+ *         gather mode as there.
+ * Other arguments, checks and device status as qmm_q4_gemm_id.
+ */
+qmm_status qmm_q4_gemm_id_pair(const void* tiles_gate, const void* tiles_up, int64_t n_expert, int64_t N,
+                               int64_t K, const void* X, int64_t ldx_token, const int32_t* ids, int64_t ld_ids,
+                               int64_t n_used, int64_t T, float* Y_gate, float* Y_up, int64_t ldy_token,
+                               int64_t ldy_slot, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                               cudaStream_t stream);
+
 /* MUL_MAT_ID for callers that cannot allocate device memory.  No counterpart
  * on the pages: this is a convenience of this library.
  *

@@ -440,11 +440,16 @@ qmm_status qmm_q4_gemm_id_workspace_size(int64_t n_expert, int64_t n_used, int64
   return QMM_OK;
 }
 
-qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_t K,
-                          const void* X, int64_t ldx_token, int64_t ldx_slot, const int32_t* ids,
-                          int64_t ld_ids, int64_t n_used, int64_t T, float* Y, int64_t ldy_token,
-                          int64_t ldy_slot, void* workspace, size_t ws_bytes,
-                          int32_t* dev_status, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// MUL_MAT_ID over one weight set, or over two (tiles2, Y2) that share the
+// routing and the packed activations: the gate/up pair.
+qmm_status q4_gemm_id_sets(const void* tiles, const void* tiles2, int64_t n_expert, int64_t N, int64_t K,
+                           const void* X, int64_t ldx_token, int64_t ldx_slot, const int32_t* ids, int64_t ld_ids,
+                           int64_t n_used, int64_t T, float* Y, float* Y2, int64_t ldy_token, int64_t ldy_slot,
+                           void* workspace, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
   if (tiles == nullptr || X == nullptr || ids == nullptr || Y == nullptr) return QMM_ERR_INVALID_ARG;
   if (n_expert < 1 || N < 1 || K < 1 || n_used < 1 || T < 1 || ld_ids < n_used)
     return QMM_ERR_INVALID_ARG;
@@ -465,6 +470,8 @@ qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_
   const bool packed = ws_bytes >= q4_moe_workspace_bytes(n_expert, n_used, T, K);
   Q4MoEArgs a{};
   a.tiles = static_cast<const uint8_t*>(tiles);
+  a.tiles2 = static_cast<const uint8_t*>(tiles2);
+  a.Y2 = Y2;
   a.n_expert = (int)n_expert;
   a.N = (int)N;
   a.K = (int)K;
@@ -487,6 +494,30 @@ qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_
   a.xperm = packed ? reinterpret_cast<__half*>(ws + tables) : nullptr;
   a.dev_status = dev_status;
   return cuda_status(launch_q4_moe(a, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+qmm_status qmm_q4_gemm_id(const void* tiles, int64_t n_expert, int64_t N, int64_t K,
+                          const void* X, int64_t ldx_token, int64_t ldx_slot, const int32_t* ids,
+                          int64_t ld_ids, int64_t n_used, int64_t T, float* Y, int64_t ldy_token,
+                          int64_t ldy_slot, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, cudaStream_t stream) {
+  return q4_gemm_id_sets(tiles, nullptr, n_expert, N, K, X, ldx_token, ldx_slot, ids, ld_ids, n_used, T, Y, nullptr,
+                         ldy_token, ldy_slot, workspace, ws_bytes, dev_status, stream);
+}
+
+qmm_status qmm_q4_gemm_id_pair(const void* tiles_gate, const void* tiles_up, int64_t n_expert, int64_t N,
+                               int64_t K, const void* X, int64_t ldx_token, const int32_t* ids, int64_t ld_ids,
+                               int64_t n_used, int64_t T, float* Y_gate, float* Y_up, int64_t ldy_token,
+                               int64_t ldy_slot, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                               cudaStream_t stream) {
+  if (tiles_up == nullptr || Y_up == nullptr) return QMM_ERR_INVALID_ARG;
+  if (!aligned(tiles_up, 16) || !aligned(Y_up, 4)) return QMM_ERR_INVALID_ARG;
+  return q4_gemm_id_sets(tiles_gate, tiles_up, n_expert, N, K, X, ldx_token, 0, ids, ld_ids, n_used, T, Y_gate, Y_up,
+                         ldy_token, ldy_slot, workspace, ws_bytes, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -132,8 +132,10 @@ struct MoeParams {
   const __nv_bfloat16* X;   // gather mode: the bf16 src1 rows
   int64_t ldx_token, ldx_slot;
   int n_used, n_expert, npairs;
-  int n_units, nrb;         // units = experts x 128-row blocks, unit u = e * nrb + row block
+  int n_units, nrb;         // units = sets x experts x 128-row blocks, unit u = (set * E + e) * nrb + row block
+  int units_per_set;        // experts x row blocks (MUL_MAT_ID); the dense GEMM has one set
   float* Y;
+  float* Y2;                // second weight set's output (the gate/up pair), else null
   int64_t ldy_token, ldy_slot;
   const int32_t* offsets;   // [n_expert + 1]; null for the dense GEMM
   const int32_t* pairs;     // grouped (token, slot) ids
@@ -152,27 +154,30 @@ __device__ __forceinline__ void pair_offsets(const MoeParams& p, int pr, int64_t
 // The CTA's jobs, in the same order for every role: units blockIdx.x,
 // blockIdx.x + gridDim.x, ...; each unit's pairs in passes of up to kTok.
 // Units without pairs are skipped.
-// Expert and first weight row of unit u.
-__device__ __forceinline__ void unit_rows(const MoeParams& p, int u, int& e, int& n0) {
+// Weight set, expert and first weight row of unit u.
+__device__ __forceinline__ void unit_rows(const MoeParams& p, int u, int& set, int& e, int& n0) {
   if (p.offsets == nullptr) {   // dense: u = row block * chunks + token chunk
+    set = 0;
     e = 0;
     n0 = (u / p.dense_chunks) * kRows;
-  } else {                      // MUL_MAT_ID: u = expert * row blocks + row block
-    e = u / p.nrb;
-    n0 = (u - e * p.nrb) * kRows;
+  } else {                      // MUL_MAT_ID: u = (set * experts + expert) * row blocks + row block
+    set = u >= p.units_per_set ? 1 : 0;
+    const int us = u - set * p.units_per_set;
+    e = us / p.nrb;
+    n0 = (us - e * p.nrb) * kRows;
   }
 }
 
 template <int kTok>
 struct Jobs {
-  int u, e, n0, first, total, pass0;
-  __device__ Jobs() : u((int)blockIdx.x - (int)gridDim.x), e(0), n0(0), first(0), total(0), pass0(0) {}
+  int u, set, e, n0, first, total, pass0;
+  __device__ Jobs() : u((int)blockIdx.x - (int)gridDim.x), set(0), e(0), n0(0), first(0), total(0), pass0(0) {}
   __device__ bool next(const MoeParams& p) {
     pass0 += kTok;
     while (pass0 >= total) {
       u += gridDim.x;
       if (u >= p.n_units) return false;
-      unit_rows(p, u, e, n0);
+      unit_rows(p, u, set, e, n0);
       if (p.offsets == nullptr) {   // one job: this unit's chunk of rows of X
         first = 0;
         pass0 = (u % p.dense_chunks) * kTok;
@@ -263,7 +268,7 @@ __device__ __forceinline__ bool epilogue_job(const MoeParams& p, const Jobs<kTok
   if (!__all_sync(0xffffffffu, mbar_wait(&d_full[db], (njobs >> 1) & 1, abort_flag, p.dev_status))) return false;
   tc_fence_after();
   const bool live = n < p.N;
-  float* ycol0 = p.Y + n + (kMode == kDense ? (int64_t)jb.pass0 * p.ldy_token : 0);
+  float* ycol0 = (jb.set ? p.Y2 : p.Y) + n + (kMode == kDense ? (int64_t)jb.pass0 * p.ldy_token : 0);
   const uint32_t tacc = trow + (uint32_t)(kTok * db);
   int c0 = 0;
   for (; c0 + 32 <= ncol; c0 += 32) {
@@ -287,6 +292,7 @@ __device__ __forceinline__ bool epilogue_job(const MoeParams& p, const Jobs<kTok
 template <int kMode, int kTok, int kCtas>
 __global__ void __launch_bounds__(32 * Lay<kTok, kCtas>::kWarps, kCtas)
 q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+             const __grid_constant__ CUtensorMap tmC2, const __grid_constant__ CUtensorMap tmP2,
              const __grid_constant__ CUtensorMap tmX, const MoeParams p) {
   constexpr bool kPacked = kMode != kTableGather;   // activations by TMA
   using L = Lay<kTok, kCtas>;
@@ -361,14 +367,19 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
   // most experts receive pairs they are fetched while the routing or packing
   // grid may still run.  (The routing grid is an ordinary stream-ordered
   // launch, so whatever wrote the tiles before it has completed.)
-  int e_first, n0_first;
-  unit_rows(p, (int)blockIdx.x, e_first, n0_first);
+  int set_first, e_first, n0_first;
+  unit_rows(p, (int)blockIdx.x, set_first, e_first, n0_first);
   const int pre = p.npairs >= p.n_expert ? min(kRawStages, TC) : 0;
   if (warp == kWProd && lane == 0) {
     tma_prefetch_desc(&tmC);
     tma_prefetch_desc(&tmP);
+    if (p.Y2 != nullptr) {
+      tma_prefetch_desc(&tmC2);
+      tma_prefetch_desc(&tmP2);
+    }
     for (int tc = 0; tc < pre; ++tc)
-      produce_weights<kRawStages>(&tmC, &tmP, p, e_first, n0_first, tc, tc, raw0, w_full, w_empty, abort_flag);
+      produce_weights<kRawStages>(set_first ? &tmC2 : &tmC, set_first ? &tmP2 : &tmP, p, e_first, n0_first, tc, tc,
+                                  raw0, w_full, w_empty, abort_flag);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // When the first unit has no pairs, its prefetched stages are consumed and dropped.
@@ -613,7 +624,8 @@ q4_tc_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CU
         const int tc0 = (first && !first_empty) ? pre : 0;   // the first job is then the first unit's pass 0
         first = false;
         for (int tc = tc0; tc < TC && ok; ++tc, ++gws)
-          ok = produce_weights<kRawStages>(&tmC, &tmP, p, jb.e, jb.n0, tc, gws, raw0, w_full, w_empty, abort_flag);
+          ok = produce_weights<kRawStages>(jb.set ? &tmC2 : &tmC, jb.set ? &tmP2 : &tmP, p, jb.e, jb.n0, tc, gws, raw0,
+                                           w_full, w_empty, abort_flag);
       }
     }
     __syncwarp();
@@ -814,8 +826,8 @@ moe_pack_kernel(const int32_t* __restrict__ pairs, const int32_t* __restrict__ o
 }
 
 template <int kMode, int kTok, int kCtas>
-cudaError_t launch_tc(const CUtensorMap& tmC, const CUtensorMap& tmP, const CUtensorMap& tmX, const MoeParams& p,
-                      cudaStream_t stream) {
+cudaError_t launch_tc(const CUtensorMap& tmC, const CUtensorMap& tmP, const CUtensorMap& tmC2, const CUtensorMap& tmP2,
+                      const CUtensorMap& tmX, const MoeParams& p, cudaStream_t stream) {
   using L = Lay<kTok, kCtas>;
   auto kern = q4_tc_kernel<kMode, kTok, kCtas>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kSmemBytes);
@@ -832,7 +844,7 @@ cudaError_t launch_tc(const CUtensorMap& tmC, const CUtensorMap& tmP, const CUte
   attr[0].val.programmaticStreamSerializationAllowed = 1;   // overlap the packing or conversion grid
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmC, tmP, tmX, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmC, tmP, tmC2, tmP2, tmX, p);
 }
 
 }  // namespace
@@ -858,8 +870,10 @@ cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream) {
   p.n_expert = a.n_expert;
   p.npairs = a.T * a.n_used;
   p.nrb = (a.N + kRows - 1) / kRows;
-  p.n_units = a.n_expert * p.nrb;
+  p.units_per_set = a.n_expert * p.nrb;
+  p.n_units = (a.tiles2 != nullptr ? 2 : 1) * p.units_per_set;
   p.Y = a.Y;
+  p.Y2 = a.tiles2 != nullptr ? a.Y2 : nullptr;
   p.ldy_token = a.ldy_token;
   p.ldy_slot = a.ldy_slot;
   p.offsets = a.offsets;
@@ -867,11 +881,16 @@ cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream) {
   p.xup = a.xup;
   p.dev_status = a.dev_status;
   const uint64_t n_tiles = (uint64_t)a.n_expert * (uint64_t)p.tiles_per_expert;
-  if (n_tiles > (uint64_t)INT32_MAX || (int64_t)a.n_expert * p.nrb > INT32_MAX) return cudaErrorInvalidValue;
-  CUtensorMap tmC, tmP, tmX;
+  if (n_tiles > (uint64_t)INT32_MAX || 2 * (int64_t)a.n_expert * p.nrb > INT32_MAX) return cudaErrorInvalidValue;
+  CUtensorMap tmC, tmP, tmC2, tmP2, tmX;
   const uint64_t tile_rows = (uint64_t)a.n_expert * (uint64_t)(a.N / 32);
   if (!make_tmap_q4_tiles(&tmC, a.tiles, (uint64_t)(a.K / 256), tile_rows, 32) ||
       !make_tmap_q4_tiles(&tmP, a.tiles, (uint64_t)(a.K / 256), tile_rows, 8))
+    return cudaErrorInvalidValue;
+  tmC2 = tmC;
+  tmP2 = tmP;
+  if (a.tiles2 != nullptr && (!make_tmap_q4_tiles(&tmC2, a.tiles2, (uint64_t)(a.K / 256), tile_rows, 32) ||
+                              !make_tmap_q4_tiles(&tmP2, a.tiles2, (uint64_t)(a.K / 256), tile_rows, 8)))
     return cudaErrorInvalidValue;
   const int npairs = a.T * a.n_used;
   // 256 pairs per routing block, more when the batch is large enough that
@@ -899,10 +918,10 @@ cudaError_t launch_q4_moe(const Q4MoEArgs& a, cudaStream_t stream) {
                      a.xup);
     if (err != cudaSuccess) return err;
   }
-  if (a.xperm == nullptr) return launch_tc<kTableGather, 64, 2>(tmC, tmP, tmC, p, stream);
+  if (a.xperm == nullptr) return launch_tc<kTableGather, 64, 2>(tmC, tmP, tmC2, tmP2, tmC, p, stream);
   if (!make_tmap_2d(&tmX, true, a.xperm, (uint64_t)a.K, (uint64_t)npairs, (uint64_t)a.K * 2, 64, 64))
     return cudaErrorInvalidValue;
-  return launch_tc<kTablePacked, 64, 2>(tmC, tmP, tmX, p, stream);
+  return launch_tc<kTablePacked, 64, 2>(tmC, tmP, tmC2, tmP2, tmX, p, stream);
 }
 
 bool q4_umma_eligible(int64_t M, int64_t N, int64_t K) {
@@ -924,6 +943,7 @@ cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaS
   p.npairs = a.M;
   p.nrb = (a.N + kRows - 1) / kRows;
   p.n_units = p.nrb;
+  p.units_per_set = p.nrb;
   p.Y = a.Y;
   p.ldy_token = a.ldy;
   p.dense_rows = a.M;
@@ -949,9 +969,9 @@ cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaS
   p.n_units = p.nrb * p.dense_chunks;
   const cudaError_t err = launch_act_to_f16(a.X, a.ldx, a.M, a.K, a.act16, stream);
   if (err != cudaSuccess) return err;
-  if (tok == 64) return launch_tc<kDense, 64, 1>(tmC, tmP, tmX, p, stream);
-  if (tok == 192) return launch_tc<kDense, 192, 1>(tmC, tmP, tmX, p, stream);
-  return launch_tc<kDense, 128, 1>(tmC, tmP, tmX, p, stream);
+  if (tok == 64) return launch_tc<kDense, 64, 1>(tmC, tmP, tmC, tmP, tmX, p, stream);
+  if (tok == 192) return launch_tc<kDense, 192, 1>(tmC, tmP, tmC, tmP, tmX, p, stream);
+  return launch_tc<kDense, 128, 1>(tmC, tmP, tmC, tmP, tmX, p, stream);
 }
 
 }  // namespace qmm

@@ -158,6 +158,8 @@ cudaError_t launch_q4_gemm_umma(const Q4DenseArgs& a, int32_t* dev_status, cudaS
 
 struct Q4MoEArgs {
   const uint8_t* tiles;
+  const uint8_t* tiles2;   // the gate/up pair: a second weight set read with the same routing, or null
+  float* Y2;               // its output
   int n_expert, N, K;
   const __nv_bfloat16* X;
   int64_t ldx_token, ldx_slot;

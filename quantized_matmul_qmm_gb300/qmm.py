@@ -66,6 +66,8 @@ SIGNATURES = {
     "qmm_q4_gemm_id_workspace_size": (_c.c_int, [_i64, _i64, _i64, _i64, _szp]),
     "qmm_q4_gemm_id": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64, _i64,
                                   _vp, _i64, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_q4_gemm_id_pair": (_c.c_int, [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp,
+                                       _i64, _i64, _vp, _sz, _vp, _vp]),
     "qmm_q4_gemm_id_noalloc": (_c.c_int, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
                                           _i64, _vp, _i64, _i64, _vp, _vp]),
     "qmm_pack_w8_size": (_c.c_int, [_i64, _i64, _szp, _szp]),
@@ -318,6 +320,26 @@ def q4_gemm_id(tiles: torch.Tensor, n_expert: int, N: int, K: int, X: torch.Tens
         _ptr(Y), Y.stride(0), Y.stride(1), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
     return Y
+
+
+def q4_gemm_id_pair(tiles_gate: torch.Tensor, tiles_up: torch.Tensor, n_expert: int, N: int, K: int,
+                    X: torch.Tensor, ids: torch.Tensor, ld_ids: int, n_used: int, T: int, Y_gate=None, Y_up=None,
+                    workspace=None, dev_status=None):
+    """The gate/up pair: both MUL_MAT_IDs over the shared src1 X [T][K] in one
+    call.  Returns (Y_gate, Y_up), each [T][n_used][N]."""
+    if Y_gate is None:
+        Y_gate = torch.empty((T, n_used, N), dtype=torch.float32, device=X.device)
+    if Y_up is None:
+        Y_up = torch.empty((T, n_used, N), dtype=torch.float32, device=X.device)
+    assert Y_gate.stride() == Y_up.stride()
+    if workspace is None:
+        workspace = torch.empty(q4_gemm_id_workspace_size(n_expert, n_used, T, K), dtype=torch.uint8,
+                                device=X.device)
+    _check("qmm_q4_gemm_id_pair", lib.qmm_q4_gemm_id_pair(
+        _ptr(tiles_gate), _ptr(tiles_up), n_expert, N, K, _ptr(X), X.stride(0), _ptr(ids), ld_ids, n_used, T,
+        _ptr(Y_gate), _ptr(Y_up), Y_gate.stride(0), Y_gate.stride(1), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream()))
+    return Y_gate, Y_up
 
 
 def q4_gemm_id_noalloc(tiles: torch.Tensor, n_expert: int, N: int, K: int, X: torch.Tensor,

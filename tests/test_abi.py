@@ -269,3 +269,19 @@ def test_int8_gemm_group_host_validation(qmm):
     assert call(prob(ldo=31)) == qmm.QMM_ERR_INVALID_ARG                  # ldo < N
     assert call(prob(K=70000, lda=70016)) == qmm.QMM_ERR_OVERFLOW_BOUND
     assert call(prob(out=P + 2)) == qmm.QMM_ERR_INVALID_ARG               # int32 output misaligned
+
+
+def test_q4_gemm_id_pair_host_validation(qmm):
+    L = qmm.lib
+    P = ctypes.c_void_p(1 << 20)
+    # a missing or misaligned second weight set / output, then the single call's checks
+    assert L.qmm_q4_gemm_id_pair(P, None, 4, 32, 256, P, 256, P, 3, 2, 5, P, P, 64, 32, P, 1 << 20, None,
+                                 None) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_q4_gemm_id_pair(P, P, 4, 32, 256, P, 256, P, 3, 2, 5, P, None, 64, 32, P, 1 << 20, None,
+                                 None) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_q4_gemm_id_pair(P, ctypes.c_void_p((1 << 20) + 8), 4, 32, 256, P, 256, P, 3, 2, 5, P, P, 64, 32, P,
+                                 1 << 20, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_q4_gemm_id_pair(P, P, 4, 32, 256, P, 256, P, 1, 2, 5, P, P, 64, 32, P, 1 << 20, None,
+                                 None) == qmm.QMM_ERR_INVALID_ARG   # ld_ids < n_used
+    assert L.qmm_q4_gemm_id_pair(P, P, 4, 32, 256, P, 256, P, 3, 2, 5, P, P, 64, 32, None, 0, None,
+                                 None) == qmm.QMM_ERR_WORKSPACE

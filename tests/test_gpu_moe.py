@@ -163,3 +163,55 @@ def test_workload_moe_tables_only_workspace(qmm, cuda, kind):
     y, norm = O.q4_gemm_id(tiles, c.n_expert, c.N, c.K, c.X.float().double().numpy(), c.shared_src1,
                            c.ids_buf.numpy(), c.ld_ids, c.n_used, c.T)
     assert O.normalized_error(Y, y, norm) <= TOL
+
+
+# ---------------------------------------------------------------------------
+# the gate/up pair in one call (qmm_q4_gemm_id_pair)
+# ---------------------------------------------------------------------------
+def run_pair(qmm, dev, Wg, Wu, X, ids_buf, ld_ids, n_used, T, ws_bytes=None, status=None):
+    E, N, K = Wg.shape
+    tg = torch.cat([qmm.pack_q4(Wg[e].to(dev)) for e in range(E)])
+    tu = torch.cat([qmm.pack_q4(Wu[e].to(dev)) for e in range(E)])
+    fg = torch.full((T, n_used, N + 4), float("nan"), dtype=torch.float32, device=dev)
+    fu = torch.full((T, n_used, N + 4), float("nan"), dtype=torch.float32, device=dev)
+    ws = None if ws_bytes is None else torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    qmm.q4_gemm_id_pair(tg, tu, E, N, K, X.to(dev), ids_buf.to(dev), ld_ids, n_used, T, Y_gate=fg[:, :, :N],
+                        Y_up=fu[:, :, :N], workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    out = []
+    for f, W, t in ((fg, Wg, tg), (fu, Wu, tu)):
+        h = f.cpu()
+        assert torch.isnan(h[:, :, N:]).all(), "canary overwritten"
+        ref = np.concatenate([O.pack_q4(W[e].numpy()) for e in range(E)])
+        assert np.array_equal(t.cpu().numpy(), ref)
+        y, norm = O.q4_gemm_id(ref, E, N, K, X.float().double().numpy(), True, ids_buf.numpy(), ld_ids, n_used, T)
+        out.append((h[:, :, :N].numpy(), y, norm))
+    return out
+
+
+def test_moe_pair_small(qmm, cuda):
+    g = torch.Generator().manual_seed(21)
+    E, N, K, T, n_used, ld = 8, 96, 512, 45, 3, 5
+    Wg = torch.randn((E, N, K), generator=g) * 0.02
+    Wu = torch.randn((E, N, K), generator=g) * 0.02
+    ids_buf = torch.randint(0, E, (T, ld), generator=g, dtype=torch.int32)
+    X = torch.randn((T, K), generator=g).to(torch.bfloat16)
+    for Y, y, norm in run_pair(qmm, cuda, Wg, Wu, X, ids_buf, ld, n_used, T):
+        assert O.normalized_error(Y, y, norm) <= TOL
+
+
+@pytest.mark.parametrize("tables_only", [False, True])
+def test_workload_moe_pair_full(qmm, cuda, tables_only):
+    """The C5 gate and up matrices (128 experts, top-8 of 17, 512 tokens) in
+    one call, with the packed activations and with the gather mode; every
+    pair of both outputs against the oracle, and bit-identical to two
+    separate qmm_q4_gemm_id calls."""
+    cg, cu = I.moe_case("gate"), I.moe_case("up")
+    ws = table_bytes(cg.n_expert, cg.n_used, cg.T) if tables_only else None
+    res = run_pair(qmm, cuda, cg.W, cu.W, cg.X, cg.ids_buf, cg.ld_ids, cg.n_used, cg.T, ws_bytes=ws)
+    for Y, y, norm in res:
+        assert O.normalized_error(Y, y, norm) <= TOL
+    # same bits as the separate calls (same kernels, same per-output order)
+    _, Yg = run_moe(qmm, cuda, cg.W, cg.X, cg.ids_buf, cg.ld_ids, cg.n_used, cg.T, ws_bytes=ws)
+    _, Yu = run_moe(qmm, cuda, cu.W, cg.X, cg.ids_buf, cg.ld_ids, cg.n_used, cg.T, ws_bytes=ws)
+    assert np.array_equal(res[0][0], Yg) and np.array_equal(res[1][0], Yu)
