@@ -155,7 +155,7 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
   if (int8_umma_eligible(M, K, N)) {
     // tensor-core route: needs the caller's workspace (never a silent switch)
     const size_t need = int8_umma_workspace_bytes(M, K, N);
-    if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256)) return QMM_ERR_WORKSPACE;
+    if (need > 0 && (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256))) return QMM_ERR_WORKSPACE;
     if ((M + 127) / 128 > INT32_MAX || (N + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;
     return cuda_status(launch_int8_gemm_umma(a, workspace, dev_status, stream));
   }

@@ -285,14 +285,20 @@ def test_umma_fp32_accumulation_is_exact(qmm, cuda, pattern):
     assert_same(got, oracle_out(A, "u8", 128, B, "s8", 0, "s32"), "s32")
 
 
-def test_umma_route_needs_workspace(qmm, cuda):
-    M, K, N = 256, 128, 64
-    A = torch.zeros((M, K), dtype=torch.uint8, device=cuda)
-    packed, _, col_sum = qmm.pack_b_int8(torch.zeros((K, N), dtype=torch.int8, device=cuda), "s8")
-    with pytest.raises(qmm.QmmError) as e:
-        qmm.int8_gemm(A, "u8", 0, packed, col_sum, N, "s8", 0, "s32",
-                      workspace=torch.empty(16, dtype=torch.uint8, device=cuda))
-    assert e.value.status == qmm.QMM_ERR_WORKSPACE
+def test_umma_route_tail_and_edge_rows_exact(qmm, cuda):
+    """The tensor-core route widens the weight tiles in shared memory and the
+    activations in a pass before the GEMM: K not a multiple of 64 (the bytes
+    past K count as 0), M and N past the last full tile, extreme codes, row
+    sums over a ragged K."""
+    for (M, K, N, zA, zB) in [(257, 65, 300, 255, -8), (300, 4607, 130, 0, 8), (513, 1, 257, 7, 3)]:
+        g = torch.Generator().manual_seed(M + K + N)
+        A = rand_codes(g, "u8", (M, K))
+        A[0] = 0
+        A[1] = 255
+        B = rand_codes(g, "s8", (K, N))
+        B[:, 0] = -128
+        got, _ = gpu_gemm(qmm, cuda, A, "u8", zA, B, "s8", zB, "s32")
+        assert_same(got, oracle_out(A, "u8", zA, B, "s8", zB, "s32"), "s32")
 
 
 # ---------------------------------------------------------------------------
