@@ -990,7 +990,7 @@ def main():
                                                     "traffic": None}
     rooflines["q4_gemv_projection_set_m1_group_graph"] = {
         "bound": "hbm", "achieved": st_pg["GBs"], "peak": hbm_peak, "unit": "GB/s", "frac": st_pg["GBs"] / hbm_peak,
-        "traffic": None, "note": "the 7 projections as one qmm_q4_gemv_group launch per set, sets in one CUDA graph"}
+        "traffic": traffic.get("q4_gemv_projection_set_m1_group_graph"), "note": "the 7 projections as one qmm_q4_gemv_group launch per set, sets in one CUDA graph"}
     w8 = streams["w8"]
     for name in ("w8_gemv_lm_head_m1_stream", "w8_gemv_lm_head_m1"):
         d = w8[name]
@@ -1031,7 +1031,7 @@ def main():
     rooflines["int8_qwen3_projections_m32_group_graph"] = {
         "bound": "hbm", "achieved": pgg["weight_GBs"], "peak": hbm_peak, "unit": "GB/s",
         "frac": pgg["weight_GBs"] / hbm_peak, "peak_probe": probe["GBs"], "frac_probe": pgg["weight_GBs"] / probe["GBs"],
-        "traffic": None, "note": "weight bytes only; one grouped launch per set in one CUDA graph, rotating copies"}
+        "traffic": traffic.get("int8_qwen3_projections_m32_group_graph"), "note": "weight bytes only; one grouped launch per set in one CUDA graph, rotating copies"}
     for name, d in streams["q4_small_batch"].items():
         rooflines[name] = {"bound": "hbm", "achieved": d["GBs"], "peak": hbm_peak, "unit": "GB/s",
                            "frac": d["GBs"] / hbm_peak, "peak_probe": probe["GBs"],
