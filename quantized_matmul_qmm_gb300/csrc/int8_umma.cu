@@ -58,7 +58,8 @@ constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kTmemCols = 512;       // two 256-column fp32 accumulators
 constexpr int kColConstBytes = kEpiWarps * 2 * 128 * 12;   // per warp: two sets of c1 / s_w / Mq, 128 columns
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kColConstBytes + 256;
-constexpr int kMinM = 256;           // below this the legacy-MMA route is used
+constexpr int kMinM = 65;            // up to 64 rows the small-M route is used (a pair tile is 256
+                                     // rows: from 65 rows on, partly empty tiles still beat the integer MMA)
 constexpr uint16_t kBothCtas = 0x3;
 constexpr int kMaxDevices = 64;
 constexpr int kWidenMaxSmem = 160 * 1024;   // >= 2 rows of the largest padded K (2 x 65792 bytes) + alignment

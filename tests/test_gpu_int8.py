@@ -210,10 +210,10 @@ def test_workload_large_sampled(qmm, cuda):
 
 
 # ---------------------------------------------------------------------------
-# tensor-core route (M >= 256): same function, bit-exact
+# tensor-core route (M >= 65): same function, bit-exact
 # ---------------------------------------------------------------------------
-UMMA_SHAPES = [(256, 64, 256), (300, 1000, 300), (257, 4608, 130), (512, 2048, 520), (520, 130, 64),
-               (1300, 2050, 1000)]
+UMMA_SHAPES = [(65, 300, 200), (96, 1088, 64), (128, 4608, 300), (200, 1000, 257), (256, 64, 256), (300, 1000, 300), (257, 4608, 130),
+               (512, 2048, 520), (520, 130, 64), (1300, 2050, 1000)]
 
 
 @pytest.mark.parametrize("a_type,b_type", [("u8", "s8"), ("s8", "u8"), ("u8", "f32")])

@@ -72,7 +72,7 @@ def test_projection_chain_per_tensor(qmm, cuda, idx):
 
 
 def test_large_chain_per_row_requant(qmm, cuda):
-    """Per-row scales into the tensor-core route (M >= 256) with int8 output."""
+    """Per-row scales into the tensor-core route (M >= 65) with int8 output."""
     M, K, N = 384, 1000, 520
     g = torch.Generator().manual_seed(77)
     X = (torch.randn((M, K), generator=g) * torch.exp(torch.randn((M, 1), generator=g))).to(torch.bfloat16)
