@@ -130,9 +130,9 @@ qmm_status qmm_int8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t*
  *
  * A        [M][K] uint8 or int8 (a_type), row stride lda bytes: lda >= K,
  *          lda % 16 == 0, base 16-byte aligned.  zA in A's own domain.  The
- *          tensor-core route (M >= 65) reads whole 16-byte groups, so A must
- *          be readable for (M - 1) * lda + roundup(K, 16) bytes, as an
- *          [M][lda] tensor is; the bytes past K do not change the result.
+ *          kernels read whole 16-byte groups, so A must be readable for
+ *          (M - 1) * lda + roundup(K, 16) bytes, as an [M][lda] tensor is;
+ *          the bytes past K do not change the result.
  * packedB  from qmm_pack_b_int8 with the same K and N; col_sum from the same call.
  * b_orig_type  the b_type given to packB (QMM_U8, QMM_S8 or QMM_F32); zB is in
  *          that domain and must be 0 for QMM_F32 weights (symmetric).

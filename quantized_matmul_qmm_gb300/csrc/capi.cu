@@ -159,14 +159,13 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
     if ((M + 127) / 128 > INT32_MAX || (N + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;
     return cuda_status(launch_int8_gemm_umma(a, workspace, dev_status, stream));
   }
-  if (int8_small_eligible(M, K, N)) return cuda_status(launch_int8_small(a, stream));
+  if (int8_small_eligible(M, K, N)) return cuda_status(launch_int8_small(a, dev_status, stream));
   if ((M + 31) / 32 > 65535) return QMM_ERR_UNSUPPORTED;
   return cuda_status(launch_int8_gemm_mma(a, stream));
 }
 
 qmm_status qmm_int8_gemm_group(const qmm_int8_problem* problems, int64_t count, int32_t* dev_status,
                                cudaStream_t stream) {
-  (void)dev_status;   // the small-M kernel has no device-side error
   if (problems == nullptr || count < 1 || count > INT32_MAX) return QMM_ERR_INVALID_ARG;
   std::vector<Int8GemmArgs> args((size_t)count);
   for (int64_t i = 0; i < count; ++i) {
@@ -176,7 +175,7 @@ qmm_status qmm_int8_gemm_group(const qmm_int8_problem* problems, int64_t count, 
     if (st != QMM_OK) return st;
     if (!int8_small_eligible(q.M, q.K, q.N)) return QMM_ERR_UNSUPPORTED;
   }
-  return cuda_status(launch_int8_small_group(args.data(), (int)count, stream));
+  return cuda_status(launch_int8_small_group(args.data(), (int)count, dev_status, stream));
 }
 
 namespace {

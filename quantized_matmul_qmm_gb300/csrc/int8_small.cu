@@ -23,6 +23,7 @@
 // cluster barrier every CTA adds its 8 slots and applies the zero-point
 // correction, bias and output conversion to its own 8 columns.
 #include <mutex>
+#include <vector>
 
 #include "qmm_internal.h"
 #include "umma.cuh"
@@ -296,41 +297,83 @@ bool int8_small_eligible(int64_t M, int64_t K, int64_t N) {
          small_smem((int)(M + 15) / 16, padded_k(K)) <= kSmemBudget;
 }
 
-cudaError_t launch_int8_small_group(const Int8GemmArgs* probs, int n, cudaStream_t stream) {
-  // consecutive problems share a launch, up to kMaxGroup of them
-  for (int b = 0; b < n; b += kMaxGroup) {
-    const int cnt = n - b < kMaxGroup ? n - b : kMaxGroup;
-    static SmallGroup gp;   // host staging copy; the launch copies it into the parameter space
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lk(mu);
-    gp = SmallGroup{};
-    int MT = 1;
-    int64_t clusters = 0, kp_max = 0;
-    for (int i = 0; i < cnt; ++i) {
-      const Int8GemmArgs& a = probs[b + i];
-      gp.prob[i] = small_params(a);
-      gp.cluster_begin[i] = (int32_t)clusters;
-      clusters += (a.N + kCols - 1) / kCols;
-      MT = MT > (a.M + 15) / 16 ? MT : (a.M + 15) / 16;
-      kp_max = kp_max > a.Kp ? kp_max : a.Kp;
-    }
-    gp.cluster_begin[cnt] = (int32_t)clusters;
-    gp.nprob = cnt;
-    if (clusters * kCluster > INT32_MAX) return cudaErrorInvalidConfiguration;
-    const size_t smem = small_smem(MT, kp_max);
-    if (smem > kSmemBudget) return cudaErrorInvalidConfiguration;
-    cudaError_t e;
-    if (MT == 1) e = launch_mt<1>(gp, smem, stream);
-    else if (MT == 2) e = launch_mt<2>(gp, smem, stream);
-    else if (MT == 3) e = launch_mt<3>(gp, smem, stream);
-    else e = launch_mt<4>(gp, smem, stream);
-    if (e != cudaSuccess) return e;
+namespace {
+
+// The cluster form on up to kMaxGroup problems in one launch.
+cudaError_t launch_cluster_batch(const std::vector<Int8GemmArgs>& probs, cudaStream_t stream) {
+  const int cnt = (int)probs.size();
+  static SmallGroup gp;   // host staging copy; the launch copies it into the parameter space
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  gp = SmallGroup{};
+  int MT = 1;
+  int64_t clusters = 0, kp_max = 0;
+  for (int i = 0; i < cnt; ++i) {
+    const Int8GemmArgs& a = probs[i];
+    gp.prob[i] = small_params(a);
+    gp.cluster_begin[i] = (int32_t)clusters;
+    clusters += (a.N + kCols - 1) / kCols;
+    MT = MT > (a.M + 15) / 16 ? MT : (a.M + 15) / 16;
+    kp_max = kp_max > a.Kp ? kp_max : a.Kp;
   }
-  return cudaSuccess;
+  gp.cluster_begin[cnt] = (int32_t)clusters;
+  gp.nprob = cnt;
+  if (clusters * kCluster > INT32_MAX) return cudaErrorInvalidConfiguration;
+  const size_t smem = small_smem(MT, kp_max);
+  if (smem > kSmemBudget) return cudaErrorInvalidConfiguration;
+  if (MT == 1) return launch_mt<1>(gp, smem, stream);
+  if (MT == 2) return launch_mt<2>(gp, smem, stream);
+  if (MT == 3) return launch_mt<3>(gp, smem, stream);
+  return launch_mt<4>(gp, smem, stream);
 }
 
-cudaError_t launch_int8_small(const Int8GemmArgs& a, cudaStream_t stream) {
-  return launch_int8_small_group(&a, 1, stream);
+}  // namespace
+
+cudaError_t launch_int8_small_group(const Int8GemmArgs* probs, int n, int32_t* dev_status, cudaStream_t stream) {
+  // Problems whose rows fit the streaming form's shared memory are gathered
+  // into batches that fit together; a batch with at least one item (16
+  // columns) per SM streams, a smaller one (too few items to fill the GPU
+  // without splitting K) joins the rest in the cluster form, up to kMaxGroup
+  // problems per launch.  The problems are independent, so launch order is free.
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  std::vector<Int8GemmArgs> st, cl;
+  cudaError_t e = cudaSuccess;
+  auto to_cluster = [&](const Int8GemmArgs& a) {
+    cl.push_back(a);
+    if ((int)cl.size() == kMaxGroup) {
+      if (e == cudaSuccess) e = launch_cluster_batch(cl, stream);
+      cl.clear();
+    }
+  };
+  auto flush_stream = [&]() {
+    if (st.empty()) return;
+    if (int8_stream_items(st.data(), (int)st.size()) >= sms) {
+      if (e == cudaSuccess) e = launch_int8_stream_group(st.data(), (int)st.size(), dev_status, stream);
+    } else {
+      for (const Int8GemmArgs& a : st) to_cluster(a);
+    }
+    st.clear();
+  };
+  for (int i = 0; i < n && e == cudaSuccess; ++i) {
+    if (!int8_stream_fits(&probs[i], 1)) {
+      to_cluster(probs[i]);
+      continue;
+    }
+    st.push_back(probs[i]);
+    if (!int8_stream_fits(st.data(), (int)st.size())) {
+      st.pop_back();
+      flush_stream();
+      st.push_back(probs[i]);
+    }
+  }
+  flush_stream();
+  if (e == cudaSuccess && !cl.empty()) e = launch_cluster_batch(cl, stream);
+  return e;
+}
+
+cudaError_t launch_int8_small(const Int8GemmArgs& a, int32_t* dev_status, cudaStream_t stream) {
+  return launch_int8_small_group(&a, 1, dev_status, stream);
 }
 
 }  // namespace qmm

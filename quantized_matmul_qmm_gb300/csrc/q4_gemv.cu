@@ -652,7 +652,7 @@ __global__ void __launch_bounds__(kGThreads, 2) q4_gemv_group_kernel(const __gri
     // copies nobody waited for may still be landing: let them land first
     if (threadIdx.x == 0)
       for (int c = 0; c < ncopies; ++c)
-        mbar_wait(&bars[c], 0, abort_flag, nullptr, 50000000ull) || mbar_try_wait(&bars[c], 0);
+        mbar_drain(&bars[c], 0);
     return;
   }
   // each output: its slab's items summed in tile-column order

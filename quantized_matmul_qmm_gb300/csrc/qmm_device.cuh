@@ -87,9 +87,11 @@ QMM_DEV void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, ui
 }
 
 // D = A(16x16 f16, row) * B(16x8 f16, col) + D with fp32 accumulation.
+// No side effects beyond d: not volatile, so independent MMAs may be
+// interleaved by the compiler to hide each one's latency.
 QMM_DEV void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                            uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -144,15 +146,15 @@ QMM_DEV int32_t zp_correct(int32_t S, int32_t colsum, int32_t rowsum, const Int8
   return (int32_t)y;
 }
 
-// Output conversion of one element (fp32 steps with explicit IEEE rounding).
-QMM_DEV void int8_store(const Int8Epi& e, int m, int n, int32_t Y) {
-  const int32_t yb = (int32_t)((uint32_t)Y + (uint32_t)(e.bias ? e.bias[n] : 0));
+// Output conversion of one element (fp32 steps with explicit IEEE rounding),
+// given the element's bias, activation scale and weight scale (0, 1 and 1
+// where the epilogue has none).
+QMM_DEV void int8_store_vals(const Int8Epi& e, int m, int n, int32_t Y, int32_t bias, float sx, float sw) {
+  const int32_t yb = (int32_t)((uint32_t)Y + (uint32_t)bias);
   if (e.out_type == QMM_S32) {
     reinterpret_cast<int32_t*>(e.out)[(int64_t)m * e.ldo + n] = yb;
     return;
   }
-  const float sx = e.s_x ? e.s_x[e.s_x_stride ? m : 0] : 1.0f;
-  const float sw = e.s_w ? e.s_w[n] : 1.0f;
   const float yf = __int2float_rn(yb);
   if (e.out_type == QMM_F32) {
     reinterpret_cast<float*>(e.out)[(int64_t)m * e.ldo + n] = __fmul_rn(__fmul_rn(yf, sx), sw);
@@ -169,6 +171,11 @@ QMM_DEV void int8_store(const Int8Epi& e, int m, int n, int32_t Y) {
     q = min(max(q, 0), 255);
     reinterpret_cast<uint8_t*>(e.out)[(int64_t)m * e.ldo + n] = (uint8_t)q;
   }
+}
+
+QMM_DEV void int8_store(const Int8Epi& e, int m, int n, int32_t Y) {
+  int8_store_vals(e, m, n, Y, e.bias ? e.bias[n] : 0, e.s_x ? e.s_x[e.s_x_stride ? m : 0] : 1.0f,
+                  e.s_w ? e.s_w[n] : 1.0f);
 }
 
 }  // namespace qmm

@@ -51,6 +51,13 @@ bool make_tmap_2d(CUtensorMap* map, bool is_bf16_or_f16, void* base, uint64_t in
 bool make_tmap_q4_tiles(CUtensorMap* map, const void* tiles, uint64_t tile_cols, uint64_t tile_rows,
                         uint32_t box_rows);
 
+// A row-major byte matrix [rows][row_stride] as {64 bytes, rows, k-blocks}
+// (k-block stride 64 bytes), no swizzle, box {64, box_rows, box_kblocks}: a
+// box lands as [k-block][row][64 bytes]; rows and k-blocks past the extents
+// read as zero.
+bool make_tmap_kblocks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_stride, uint64_t kblocks,
+                       uint32_t box_rows, uint32_t box_kblocks);
+
 // ---- packs (pack.cu) ----
 cudaError_t launch_pack_b_int8(const void* B, qmm_dtype b_type, int64_t K, int64_t N, int64_t ldb,
                                int8_t* packed, int64_t Kp, float* col_scale, int32_t* col_sum,
@@ -73,9 +80,14 @@ struct Int8GemmArgs {
 cudaError_t launch_int8_gemm_mma(const Int8GemmArgs& a, cudaStream_t stream);
 // small-M route (int8_small.cu): clusters of 8 CTAs, f16 MMA on exact integer codes
 bool int8_small_eligible(int64_t M, int64_t K, int64_t N);
-cudaError_t launch_int8_small(const Int8GemmArgs& a, cudaStream_t stream);
+cudaError_t launch_int8_small(const Int8GemmArgs& a, int32_t* dev_status, cudaStream_t stream);
 // several small-M problems, one launch per 16 (each must be int8_small_eligible)
-cudaError_t launch_int8_small_group(const Int8GemmArgs* probs, int n, cudaStream_t stream);
+cudaError_t launch_int8_small_group(const Int8GemmArgs* probs, int n, int32_t* dev_status, cudaStream_t stream);
+// the streaming form (int8_stream.cu): one CTA per SM, no clusters; for up to
+// 16 problems whose rows fit its shared memory together
+bool int8_stream_fits(const Int8GemmArgs* probs, int n);
+int64_t int8_stream_items(const Int8GemmArgs* probs, int n);   // 16-column items
+cudaError_t launch_int8_stream_group(const Int8GemmArgs* probs, int n, int32_t* dev_status, cudaStream_t stream);
 // tcgen05 route (int8_umma.cu)
 bool int8_umma_eligible(int64_t M, int64_t K, int64_t N);
 size_t int8_umma_workspace_bytes(int64_t M, int64_t K, int64_t N);

@@ -82,6 +82,17 @@ QMM_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
   }
 }
 
+// Wait for a phase that copies already issued will complete, whether or not
+// the CTA's abort flag is up (a CTA leaves only after its copies land); still
+// bounded by limit_ns.
+QMM_DEV bool mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns = 50000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 <= limit_ns)
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+  return false;
+}
+
 // ---- TMA ---------------------------------------------------------------------
 // 2-D tiled load into shared memory; c0 is the innermost (contiguous) coordinate.
 QMM_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
@@ -132,6 +143,15 @@ QMM_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
 // is visible (a no-op when the launch carries no programmatic dependency).
 QMM_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 QMM_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Warm L2 with the line holding one global address.
+QMM_DEV void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory"); }
+// Warm L2 with one 3-D box of a tensor map; nothing lands in shared memory.
+QMM_DEV void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
 QMM_DEV void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -302,7 +302,9 @@ def test_umma_route_tail_and_edge_rows_exact(qmm, cuda):
 
 
 # ---------------------------------------------------------------------------
-# small-M route (M <= 64): f16 MMA on exact integer codes, clusters of 8 CTAs
+# small-M routes (M <= 64): f16 MMA on exact integer codes; the streaming
+# form (one CTA per SM, weight rows through a shared-memory ring) when the
+# rows fit its shared memory, else clusters of 8 CTAs
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("M,K", [(16, 1024), (32, 2048), (48, 4608), (64, 4608), (16, 20000)])
 def test_small_route_extreme_codes_exact(qmm, cuda, M, K):
@@ -318,8 +320,49 @@ def test_small_route_extreme_codes_exact(qmm, cuda, M, K):
     assert_same(got, oracle_out(A, "u8", 128, B, "s8", 0, "s32"), "s32")
 
 
+@pytest.mark.parametrize("M,K,N", [(64, 2200, 2500), (64, 2300, 2500), (1, 10500, 2500), (1, 10600, 2500),
+                                   (17, 3300, 2500), (33, 17, 2500), (48, 1000, 4099)])
+def test_small_route_form_boundaries_exact(qmm, cuda, M, K, N):
+    """Enough columns for the streaming form (at least one 16-column item per
+    SM), on both sides of its shared-memory limit (the largest padded K for 64
+    rows and for one row, and just past each: those take the cluster form), a
+    K of one 64-step (seven of the eight warps idle), a ragged last item;
+    extreme codes in a row and a column, zero points on both sides."""
+    g = torch.Generator().manual_seed(3 * M + K + N)
+    A = rand_codes(g, "u8", (M, K))
+    A[0] = 255
+    B = rand_codes(g, "s8", (K, N))
+    B[:, 0] = -128
+    got, _ = gpu_gemm(qmm, cuda, A, "u8", 201, B, "s8", -7, "s32")
+    assert_same(got, oracle_out(A, "u8", 201, B, "s8", -7, "s32"), "s32")
+
+
+@pytest.mark.parametrize("K", [3000, 1000])
 @pytest.mark.parametrize("a_type,b_type,out_type", [("u8", "s8", "s8"), ("s8", "u8", "f32"), ("u8", "f32", "u8")])
-@pytest.mark.parametrize("M,K,N", [(64, 4608, 200), (48, 3000, 65), (2, 130, 1), (31, 20000, 100)])
+def test_small_route_stream_epilogues_exact(qmm, cuda, a_type, b_type, out_type, K):
+    """The streaming form with every operand type, both zero points (row sums),
+    bias, per-row s_x and each output type: M = 32, N = 2600; K = 3000 keeps
+    A as int8 codes (three chunks of the ring, the last one ragged), K = 1000
+    widens A to f16 once (a ragged last 64-k block)."""
+    M, N = 32, 2600
+    g = torch.Generator().manual_seed(91)
+    A = rand_codes(g, a_type, (M, K))
+    B = torch.randn((K, N), generator=g) * 0.02 if b_type == "f32" else rand_codes(g, b_type, (K, N))
+    zA = 37 if a_type == "u8" else -21
+    zB = 0 if b_type == "f32" else (200 if b_type == "u8" else 5)
+    bias = torch.randint(-5000, 5000, (N,), generator=g, dtype=torch.int32)
+    s_x = (torch.rand(M, generator=g) * 0.01 + 0.001).numpy()
+    s_w = (torch.rand(N, generator=g) * 9e-3 + 1e-3).float()
+    s_y = 40.0 if out_type in ("s8", "u8") else 1.0
+    got, _ = gpu_gemm(qmm, cuda, A, a_type, zA, B, b_type, zB, out_type, bias=bias, s_x=s_x, s_x_stride=1,
+                      s_w=s_w, s_y=s_y, zp_y=3 if out_type == "u8" else -2)
+    ref = oracle_out(A, a_type, zA, B, b_type, zB, out_type, bias=bias, s_x=s_x, s_w=s_w.numpy(), s_y=s_y,
+                     zp_y=3 if out_type == "u8" else -2)
+    assert_same(got, ref, out_type)
+
+
+@pytest.mark.parametrize("a_type,b_type,out_type", [("u8", "s8", "s8"), ("s8", "u8", "f32"), ("u8", "f32", "u8")])
+@pytest.mark.parametrize("M,K,N", [(64, 4608, 200), (48, 3000, 65), (2, 130, 1), (31, 20000, 100), (40, 1000, 130)])
 def test_small_route_epilogues_exact(qmm, cuda, a_type, b_type, out_type, M, K, N):
     """Zero points on both sides (row sums needed), bias, per-row s_x, every
     output type; K not a multiple of 64 and N not a multiple of 64."""

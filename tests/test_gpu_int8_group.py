@@ -102,3 +102,31 @@ def test_group_mixed_problems(qmm, cuda):
         assert_same(got, ref, ot)
     for got, ref, ot in run_group(qmm, cuda, cases):
         assert_same(got, ref, ot)
+
+
+def test_group_stream_and_cluster_forms(qmm, cuda):
+    """A group that splits into a streaming batch (the first two problems:
+    158 items of 16 columns) and a cluster batch (the next three do not fit
+    the streaming form together with them, and have too few items alone):
+    operand types, zero points with row sums, every output type."""
+    g = torch.Generator().manual_seed(5)
+    specs = [(5, 700, 1500, "u8", "s8", "s32"), (32, 3072, 1024, "s8", "u8", "f32"), (64, 1500, 900, "u8", "u8", "u8"),
+             (1, 64, 40, "s8", "f32", "f32"), (20, 2000, 777, "u8", "s8", "s8")]
+    cases = []
+    for (M, K, N, at, bt, ot) in specs:
+        A = rand_codes(g, at, (M, K))
+        B = torch.randn((K, N), generator=g) * 0.02 if bt == "f32" else rand_codes(g, bt, (K, N))
+        zA = int(torch.randint(0, 256, (1,), generator=g)) if at == "u8" else int(torch.randint(-128, 128, (1,), generator=g))
+        zB = 0 if bt == "f32" else (int(torch.randint(0, 256, (1,), generator=g)) if bt == "u8" else -4)
+        c = dict(A=A, a_type=at, zA=zA, B=B, b_type=bt, zB=zB, out_type=ot,
+                 bias=torch.randint(-3000, 3000, (N,), generator=g, dtype=torch.int32))
+        if ot != "s32":
+            c["s_x"] = (torch.rand(M, generator=g) * 0.01 + 0.001).numpy()
+            c["s_x_stride"] = 1
+            if bt != "f32":
+                c["s_w"] = (torch.rand(N, generator=g) * 9e-3 + 1e-3).float()
+        if ot in ("s8", "u8"):
+            c["s_y"], c["zp_y"] = 40.0, 3
+        cases.append(c)
+    for got, ref, ot in run_group(qmm, cuda, cases):
+        assert_same(got, ref, ot)
