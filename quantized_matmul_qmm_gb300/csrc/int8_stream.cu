@@ -322,13 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
 #pragma unroll
         for (int k = 0; k < R / kRowStep; ++k) rs[k] = rowsum[min(r0 + kRowStep * k, R - 1)];
       }
-      const int32_t* rb = red + b * kCW * R * kItem;
+      const uint32_t rb = smem_u32(red) + (uint32_t)((b * kCW * R * kItem + r0 * kItem + c) * 4);
       uint32_t S[R / kRowStep];
 #pragma unroll
       for (int k = 0; k < R / kRowStep; ++k) {
         S[k] = 0u;
 #pragma unroll
-        for (int w = 0; w < kCW; ++w) S[k] += (uint32_t)rb[(w * R + r0 + kRowStep * k) * kItem + c];
+        for (int w = 0; w < kCW; ++w) S[k] += lds32(rb + (uint32_t)((w * R + kRowStep * k) * kItem * 4));
       }
 #pragma unroll
       for (int k = 0; k < R / kRowStep; ++k) {
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
     // buffer j & 1 is free once the epilogue is done with item j - 2
     const int b = j & 1;
     ok = __all_sync(0xffffffffu, mbar_wait(&red_empty[b], (uint32_t)(((j >> 1) & 1) ^ 1), abort_flag, p.dev_status)) && ok;
-    int32_t* rb = red + b * kCW * R * kItem;
+    const uint32_t rb = smem_u32(red) + (uint32_t)(b * kCW * R * kItem * 4);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -504,11 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
           for (int pp = 0; pp < NP; ++pp) v[e] += __float2int_rn(accf[mt][nb][pp][e]);
         }
         // D fragment: (row g, columns 2t, 2t+1) and (row g + 8, same columns)
-        int32_t* r0 = rb + (warp * R + 16 * mt + g) * kItem + 8 * nb + 2 * t;
-        r0[0] = v[0];
-        r0[1] = v[1];
-        r0[8 * kItem] = v[2];
-        r0[8 * kItem + 1] = v[3];
+        const uint32_t r0 = rb + (uint32_t)(((warp * R + 16 * mt + g) * kItem + 8 * nb + 2 * t) * 4);
+        sts64(r0, (uint32_t)v[0], (uint32_t)v[1]);
+        sts64(r0 + 8 * kItem * 4, (uint32_t)v[2], (uint32_t)v[3]);
       }
     __syncwarp();
     if (lane == 0) mbar_arrive(&red_full[b]);
