@@ -158,6 +158,35 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
                          int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
                          cudaStream_t stream);
 
+/* Static weights widened once ("int8 inference", "Product kernel (Int8Gemm)":
+ * packB is a one-time weight transform, and so is this).  The tensor-core
+ * route (M >= 65) multiplies f16 copies of the codes, exact for every int8
+ * value; qmm_int8_gemm widens the packed weights on every call, while
+ * qmm_int8_gemm_b16 reads a copy made here once, so a call only widens A.
+ *
+ * qmm_widen_b_int8_size: bytes of that copy, N * roundup(K, 64) * 2.
+ * qmm_widen_b_int8: packedB (from qmm_pack_b_int8 with the same K and N,
+ *          16-byte aligned) -> b16, f16 [N][roundup(K, 64)] of the packed
+ *          codes B' (the padding columns are zeros), device, 16-byte aligned,
+ *          b16_bytes at least the size above; owned by the caller and valid as
+ *          long as packedB is unchanged.  Asynchronous on `stream`.
+ * qmm_int8_gemm_b16_workspace_size: workspace of qmm_int8_gemm_b16 (smaller
+ *          than qmm_int8_gemm's: no room for the widened weights).
+ * qmm_int8_gemm_b16: exactly qmm_int8_gemm (same arguments, checks, routes
+ *          and results, bit for bit), with b16 (non-NULL) the copy of
+ *          packedB.  M <= 64 routes read packedB and ignore b16.
+ * Errors: QMM_ERR_INVALID_ARG for a NULL or misaligned b16 or a short
+ *          b16_bytes, else as qmm_int8_gemm / qmm_pack_b_int8.
+ */
+qmm_status qmm_widen_b_int8_size(int64_t K, int64_t N, size_t* b16_bytes);
+qmm_status qmm_widen_b_int8(const void* packedB, int64_t K, int64_t N, void* b16, size_t b16_bytes,
+                            int32_t* dev_status, cudaStream_t stream);
+qmm_status qmm_int8_gemm_b16_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes);
+qmm_status qmm_int8_gemm_b16(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int64_t lda, int32_t zA,
+                             const void* packedB, const void* b16, const int32_t* col_sum, int64_t N,
+                             qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out, int64_t ldo,
+                             void* workspace, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream);
+
 /* One int8 GEMM of a grouped call: the arguments of qmm_int8_gemm, with the
  * epilogue held by value. */
 typedef struct qmm_int8_problem {

@@ -140,6 +140,26 @@ qmm_status int8_args(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int6
   return QMM_OK;
 }
 
+qmm_status int8_gemm_impl(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int64_t lda, int32_t zA,
+                          const void* packedB, const void* b16, const int32_t* col_sum, int64_t N,
+                          qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out, int64_t ldo,
+                          void* workspace, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  Int8GemmArgs a;
+  const qmm_status st = int8_args(A, a_type, M, K, lda, zA, packedB, col_sum, N, b_orig_type, zB, ep, out, ldo, a);
+  if (st != QMM_OK) return st;
+  if (b16 != nullptr && !aligned(b16, 16)) return QMM_ERR_INVALID_ARG;
+  if (int8_umma_eligible(M, K, N)) {
+    // tensor-core route: needs the caller's workspace (never a silent switch)
+    const size_t need = int8_umma_workspace_bytes(M, K, N, b16 != nullptr);
+    if (need > 0 && (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256))) return QMM_ERR_WORKSPACE;
+    if ((M + 127) / 128 > INT32_MAX || (N + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;
+    return cuda_status(launch_int8_gemm_umma(a, workspace, dev_status, stream, static_cast<const __half*>(b16)));
+  }
+  if (int8_small_eligible(M, K, N)) return cuda_status(launch_int8_small(a, dev_status, stream));
+  if ((M + 31) / 32 > 65535) return QMM_ERR_UNSUPPORTED;
+  return cuda_status(launch_int8_gemm_mma(a, stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -149,19 +169,42 @@ qmm_status qmm_int8_gemm(const void* A, qmm_dtype a_type, int64_t M, int64_t K, 
                          qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out,
                          int64_t ldo, void* workspace, size_t ws_bytes, int32_t* dev_status,
                          cudaStream_t stream) {
-  Int8GemmArgs a;
-  const qmm_status st = int8_args(A, a_type, M, K, lda, zA, packedB, col_sum, N, b_orig_type, zB, ep, out, ldo, a);
-  if (st != QMM_OK) return st;
-  if (int8_umma_eligible(M, K, N)) {
-    // tensor-core route: needs the caller's workspace (never a silent switch)
-    const size_t need = int8_umma_workspace_bytes(M, K, N);
-    if (need > 0 && (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256))) return QMM_ERR_WORKSPACE;
-    if ((M + 127) / 128 > INT32_MAX || (N + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;
-    return cuda_status(launch_int8_gemm_umma(a, workspace, dev_status, stream));
-  }
-  if (int8_small_eligible(M, K, N)) return cuda_status(launch_int8_small(a, dev_status, stream));
-  if ((M + 31) / 32 > 65535) return QMM_ERR_UNSUPPORTED;
-  return cuda_status(launch_int8_gemm_mma(a, stream));
+  return int8_gemm_impl(A, a_type, M, K, lda, zA, packedB, nullptr, col_sum, N, b_orig_type, zB, ep, out, ldo,
+                        workspace, ws_bytes, dev_status, stream);
+}
+
+qmm_status qmm_widen_b_int8_size(int64_t K, int64_t N, size_t* b16_bytes) {
+  if (b16_bytes == nullptr || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (!k_bound_ok(K)) return QMM_ERR_OVERFLOW_BOUND;
+  *b16_bytes = (size_t)(N * padded_k(K) * 2);
+  return QMM_OK;
+}
+
+qmm_status qmm_widen_b_int8(const void* packedB, int64_t K, int64_t N, void* b16, size_t b16_bytes,
+                            int32_t* dev_status, cudaStream_t stream) {
+  if (packedB == nullptr || b16 == nullptr || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (!k_bound_ok(K)) return QMM_ERR_OVERFLOW_BOUND;
+  if (!aligned(packedB, 16) || !aligned(b16, 16)) return QMM_ERR_INVALID_ARG;
+  if (b16_bytes < (size_t)(N * padded_k(K) * 2)) return QMM_ERR_INVALID_ARG;
+  if (N > INT32_MAX) return QMM_ERR_UNSUPPORTED;
+  return cuda_status(launch_widen_b_int8(static_cast<const int8_t*>(packedB), (int)K, (int)N,
+                                         static_cast<__half*>(b16), dev_status, stream));
+}
+
+qmm_status qmm_int8_gemm_b16_workspace_size(int64_t M, int64_t K, int64_t N, size_t* ws_bytes) {
+  if (ws_bytes == nullptr || M < 1 || K < 1 || N < 1) return QMM_ERR_INVALID_ARG;
+  if (!k_bound_ok(K)) return QMM_ERR_OVERFLOW_BOUND;
+  *ws_bytes = int8_umma_workspace_bytes(M, K, N, true);
+  return QMM_OK;
+}
+
+qmm_status qmm_int8_gemm_b16(const void* A, qmm_dtype a_type, int64_t M, int64_t K, int64_t lda, int32_t zA,
+                             const void* packedB, const void* b16, const int32_t* col_sum, int64_t N,
+                             qmm_dtype b_orig_type, int32_t zB, const qmm_epilogue* ep, void* out, int64_t ldo,
+                             void* workspace, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  if (b16 == nullptr) return QMM_ERR_INVALID_ARG;
+  return int8_gemm_impl(A, a_type, M, K, lda, zA, packedB, b16, col_sum, N, b_orig_type, zB, ep, out, ldo,
+                        workspace, ws_bytes, dev_status, stream);
 }
 
 qmm_status qmm_int8_gemm_group(const qmm_int8_problem* problems, int64_t count, int32_t* dev_status,

@@ -70,16 +70,6 @@ struct StreamParams {
   int32_t* dev_status;
 };
 
-// Four biased bytes (code + 128) as two f16x2 pairs of the codes, exactly:
-// each byte becomes the low mantissa byte of 1024 (f16 0x6400), and
-// 1024 + 128 is subtracted.
-QMM_DEV void biased4_to_f16(uint32_t u, uint32_t& lo, uint32_t& hi) {
-  const uint32_t l = __byte_perm(u, 0x64646464u, 0x4140u);
-  const uint32_t h = __byte_perm(u, 0x64646464u, 0x4342u);
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(0x64806480u));
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(0x64806480u));
-}
-
 QMM_DEV void bar_compute() { asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "memory"); }
 
 // Shared memory: A (int8 as [k-block][R][64 bytes], or f16 as [k-block][R]

@@ -559,14 +559,14 @@ __global__ void __launch_bounds__(kWidenThreads) int8_widen_kernel(const WidenPa
           *reinterpret_cast<uint4*>(dst + k) = *reinterpret_cast<const uint4*>(h);
           continue;
         }
-        __half h[8];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          sum = __dp4a((int)w[q], 0x01010101, sum);
-#pragma unroll
-          for (int b = 0; b < 4; ++b) h[4 * q + b] = __int2half_rn((int)(int8_t)(w[q] >> (8 * b)));
-        }
-        *reinterpret_cast<uint4*>(dst + k) = *reinterpret_cast<const uint4*>(h);
+        // the codes (exact in f16) through their biased bytes: two byte
+        // permutes and two f16x2 subtractions per four codes
+        uint4 h;
+        sum = __dp4a((int)w[0], 0x01010101, sum);
+        sum = __dp4a((int)w[1], 0x01010101, sum);
+        biased4_to_f16(w[0] ^ 0x80808080u, h.x, h.y);
+        biased4_to_f16(w[1] ^ 0x80808080u, h.z, h.w);
+        *reinterpret_cast<uint4*>(dst + k) = h;
       }
       if (is_a) {
 #pragma unroll
@@ -599,11 +599,13 @@ struct WsLayout {
 WsLayout ws_layout(int64_t M, int64_t K, int64_t N) {
   const int64_t Kp = padded_k(K);
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  // A16, the row sums, then B16 last: a call with weights widened beforehand
+  // needs the workspace only up to b16
   WsLayout w{};
   w.a16 = 0;
-  w.b16 = up((size_t)M * Kp * 2);
-  w.rs = w.b16 + up((size_t)N * Kp * 2);
-  w.total = w.rs + up((size_t)M * 4);
+  w.rs = up((size_t)M * Kp * 2);
+  w.b16 = w.rs + up((size_t)M * 4);
+  w.total = w.b16 + up((size_t)N * Kp * 2);
   return w;
 }
 
@@ -660,16 +662,19 @@ bool int8_umma_eligible(int64_t M, int64_t K, int64_t N) {
   return M >= kMinM;
 }
 
-size_t int8_umma_workspace_bytes(int64_t M, int64_t K, int64_t N) {
-  return int8_umma_eligible(M, K, N) ? ws_layout(M, K, N).total : 0;
+size_t int8_umma_workspace_bytes(int64_t M, int64_t K, int64_t N, bool b16_given) {
+  if (!int8_umma_eligible(M, K, N)) return 0;
+  const WsLayout w = ws_layout(M, K, N);
+  return b16_given ? w.b16 : w.total;
 }
 
 cudaError_t launch_int8_gemm_umma(const Int8GemmArgs& a, void* workspace, int32_t* dev_status,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, const __half* b16) {
   const WsLayout w = ws_layout(a.M, a.K, a.N);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   __half* A16 = reinterpret_cast<__half*>(ws + w.a16);
-  __half* B16 = reinterpret_cast<__half*>(ws + w.b16);
+  // weights widened once beforehand (launch_widen_b_int8), or here on every call
+  __half* B16 = b16 != nullptr ? const_cast<__half*>(b16) : reinterpret_cast<__half*>(ws + w.b16);
   int32_t* rs = a.need_rowsum ? reinterpret_cast<int32_t*>(ws + w.rs) : nullptr;
   const int Kp = (int)a.Kp;
   WidenParams wp{};
@@ -682,12 +687,12 @@ cudaError_t launch_int8_gemm_umma(const Int8GemmArgs& a, void* workspace, int32_
   wp.dev_status = dev_status;
   wp.M = a.M;
   wp.K = a.K;
-  wp.N = a.N;
+  wp.N = b16 != nullptr ? 0 : a.N;   // the widen pass takes A's rows, and B's unless they come widened
   wp.Kp = Kp;
   wp.a_u8 = a.a_u8;
   wp.R = std::max(1, std::min(kWidenMaxRows, kWidenGroupBytes / Kp));
   const size_t wsmem = 128 + (size_t)2 * wp.R * Kp;
-  const int ngroups = (a.M + a.N + wp.R - 1) / wp.R;
+  const int ngroups = (wp.M + wp.N + wp.R - 1) / wp.R;
   int pairs = 0;
   cudaError_t err = resident_pairs(&pairs);
   if (err != cudaSuccess) return err;
@@ -726,6 +731,27 @@ cudaError_t launch_int8_gemm_umma(const Int8GemmArgs& a, void* workspace, int32_
   const bool per_row_mq = (ot == QMM_S8 || ot == QMM_U8) && a.epi.s_x != nullptr && a.epi.s_x_stride != 0;
   const int which = ot == QMM_S32 ? 0 : ot == QMM_F32 ? 1 : (ot == QMM_S8 ? 2 : 3) + (per_row_mq ? 2 : 0);
   return cudaLaunchKernelEx(&cfg, kUmmaKernels[which], tmA, tmB, p);
+}
+
+cudaError_t launch_widen_b_int8(const int8_t* packed, int K, int N, __half* b16, int32_t* dev_status,
+                                cudaStream_t stream) {
+  WidenParams wp{};
+  wp.B = packed;
+  wp.B16 = b16;
+  wp.dev_status = dev_status;
+  wp.M = 0;
+  wp.K = K;
+  wp.N = N;
+  wp.Kp = (int)padded_k(K);
+  wp.R = std::max(1, std::min(kWidenMaxRows, kWidenGroupBytes / wp.Kp));
+  const size_t wsmem = 128 + (size_t)2 * wp.R * wp.Kp;
+  int pairs = 0;
+  cudaError_t err = resident_pairs(&pairs);
+  if (err != cudaSuccess) return err;
+  const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(8, (200u << 10) / wsmem));
+  const int wgrid = std::min((N + wp.R - 1) / wp.R, 2 * pairs * per_sm);
+  int8_widen_kernel<<<wgrid, kWidenThreads, wsmem, stream>>>(wp);
+  return cudaGetLastError();
 }
 
 size_t w8_umma_workspace_bytes(int64_t K, int64_t N) { return (size_t)N * padded_k(K) * 2; }

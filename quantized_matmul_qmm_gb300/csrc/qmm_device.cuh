@@ -87,6 +87,16 @@ QMM_DEV void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, ui
 }
 
 // D = A(16x16 f16, row) * B(16x8 f16, col) + D with fp32 accumulation.
+// Four biased bytes (code + 128 each) as two f16x2 pairs of the codes,
+// exactly: each byte becomes the low mantissa byte of 1024 (f16 0x6400), and
+// 1024 + 128 is subtracted.  lo holds bytes 0 and 1 (byte 0 in the low half).
+QMM_DEV void biased4_to_f16(uint32_t u, uint32_t& lo, uint32_t& hi) {
+  const uint32_t l = __byte_perm(u, 0x64646464u, 0x4140u);
+  const uint32_t h = __byte_perm(u, 0x64646464u, 0x4342u);
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(0x64806480u));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(0x64806480u));
+}
+
 // No side effects beyond d: not volatile, so independent MMAs may be
 // interleaved by the compiler to hide each one's latency.
 QMM_DEV void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,

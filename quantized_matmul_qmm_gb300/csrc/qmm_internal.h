@@ -90,9 +90,13 @@ int64_t int8_stream_items(const Int8GemmArgs* probs, int n);   // 16-column item
 cudaError_t launch_int8_stream_group(const Int8GemmArgs* probs, int n, int32_t* dev_status, cudaStream_t stream);
 // tcgen05 route (int8_umma.cu)
 bool int8_umma_eligible(int64_t M, int64_t K, int64_t N);
-size_t int8_umma_workspace_bytes(int64_t M, int64_t K, int64_t N);
+size_t int8_umma_workspace_bytes(int64_t M, int64_t K, int64_t N, bool b16_given = false);
+// b16: the weights as f16 [N][Kp] from launch_widen_b_int8, or null (widened on every call)
 cudaError_t launch_int8_gemm_umma(const Int8GemmArgs& a, void* workspace, int32_t* dev_status,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, const __half* b16 = nullptr);
+// packed B' [N][Kp] widened once to f16 [N][Kp] (exact)
+cudaError_t launch_widen_b_int8(const int8_t* packed, int K, int N, __half* b16, int32_t* dev_status,
+                                cudaStream_t stream);
 // activation quantisation (quant_act.cu); the per-tensor path uses 4 bytes of workspace
 cudaError_t launch_quantize_act(const void* X, bool x_bf16, int M, int K, int64_t ldx, bool per_row, int8_t* A,
                                 int64_t lda, float* s_x, void* workspace, cudaStream_t stream);

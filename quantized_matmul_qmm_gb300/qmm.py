@@ -51,6 +51,11 @@ SIGNATURES = {
     "qmm_int8_gemm_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
     "qmm_int8_gemm": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _i32, _vp, _vp, _i64, _c.c_int,
                                  _i32, _c.POINTER(QmmEpilogue), _vp, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_widen_b_int8_size": (_c.c_int, [_i64, _i64, _szp]),
+    "qmm_widen_b_int8": (_c.c_int, [_vp, _i64, _i64, _vp, _sz, _vp, _vp]),
+    "qmm_int8_gemm_b16_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
+    "qmm_int8_gemm_b16": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _i64, _c.c_int,
+                                     _i32, _c.POINTER(QmmEpilogue), _vp, _i64, _vp, _sz, _vp, _vp]),
     "qmm_int8_gemm_group": (_c.c_int, [_c.POINTER(QmmInt8Problem), _i64, _vp, _vp]),
     "qmm_int8_gemm_axis_zp_workspace_size": (_c.c_int, [_i64, _i64, _i64, _szp]),
     "qmm_int8_gemm_axis_zp": (_c.c_int, [_vp, _c.c_int, _i64, _i64, _i64, _vp, _vp, _vp, _i64, _c.c_int,
@@ -155,23 +160,41 @@ def int8_gemm_workspace_size(M: int, K: int, N: int) -> int:
     return _size("qmm_int8_gemm_workspace_size", M, K, N)
 
 
+def widen_b_int8(packed: torch.Tensor, K: int, N: int, dev_status=None) -> torch.Tensor:
+    """packed [N][Kp] int8 from pack_b_int8 -> its f16 copy [N][Kp] through
+    qmm_widen_b_int8 (done once, like the pack)."""
+    nbytes = _size("qmm_widen_b_int8_size", K, N)
+    b16 = torch.empty(nbytes // 2, dtype=torch.float16, device=packed.device).view(N, nbytes // (2 * N))
+    _check("qmm_widen_b_int8", lib.qmm_widen_b_int8(_ptr(packed), K, N, _ptr(b16), nbytes, _ptr(dev_status),
+                                                    _stream()))
+    return b16
+
+
 def int8_gemm(A: torch.Tensor, a_type: str, zA: int, packed: torch.Tensor, col_sum: torch.Tensor,
               N: int, b_orig_type: str, zB: int, out_type: str = "s32", bias=None, s_x=None,
               s_x_stride: int = 0, s_w=None, s_y: float = 1.0, zp_y: int = 0, out=None,
-              workspace=None, dev_status=None):
-    """Y = A (x) packB through qmm_int8_gemm.  Returns the output tensor."""
+              workspace=None, dev_status=None, b16=None):
+    """Y = A (x) packB through qmm_int8_gemm, or qmm_int8_gemm_b16 when b16
+    (from widen_b_int8) is given.  Returns the output tensor."""
     M, K = A.shape
     if out is None:
         out = torch.empty((M, N), dtype=TORCH_OUT[out_type], device=A.device)
-    ws_need = int8_gemm_workspace_size(M, K, N)
+    ws_need = (_size("qmm_int8_gemm_b16_workspace_size", M, K, N) if b16 is not None
+               else int8_gemm_workspace_size(M, K, N))
     if workspace is None and ws_need > 0:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=A.device)
     ep = QmmEpilogue(DTYPES[out_type], _ptr(bias), _ptr(s_x), s_x_stride, _ptr(s_w),
                      float(s_y), int(zp_y))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if b16 is not None:
+        _check("qmm_int8_gemm_b16", lib.qmm_int8_gemm_b16(
+            _ptr(A), DTYPES[a_type], M, K, A.stride(0), int(zA), _ptr(packed), _ptr(b16), _ptr(col_sum), N,
+            DTYPES[b_orig_type], int(zB), ctypes.byref(ep), _ptr(out), out.stride(0), _ptr(workspace), ws_bytes,
+            _ptr(dev_status), _stream()))
+        return out
     _check("qmm_int8_gemm", lib.qmm_int8_gemm(
         _ptr(A), DTYPES[a_type], M, K, A.stride(0), int(zA), _ptr(packed), _ptr(col_sum), N,
-        DTYPES[b_orig_type], int(zB), ctypes.byref(ep), _ptr(out), out.stride(0), _ptr(workspace),
-        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        DTYPES[b_orig_type], int(zB), ctypes.byref(ep), _ptr(out), out.stride(0), _ptr(workspace), ws_bytes,
         _ptr(dev_status), _stream()))
     return out
 

@@ -285,3 +285,31 @@ def test_q4_gemm_id_pair_host_validation(qmm):
                                  None) == qmm.QMM_ERR_INVALID_ARG   # ld_ids < n_used
     assert L.qmm_q4_gemm_id_pair(P, P, 4, 32, 256, P, 256, P, 3, 2, 5, P, P, 64, 32, None, 0, None,
                                  None) == qmm.QMM_ERR_WORKSPACE
+
+
+def test_widen_b_sizes_and_host_validation(qmm):
+    """The one-time f16 copy of packed int8 weights and the GEMM that reads
+    it: sizes, and bad arguments rejected on the host."""
+    L = qmm.lib
+    sz = ctypes.c_size_t(0)
+    assert L.qmm_widen_b_int8_size(100, 7, ctypes.byref(sz)) == qmm.QMM_OK and sz.value == 7 * 128 * 2
+    assert L.qmm_widen_b_int8_size(0, 7, ctypes.byref(sz)) == qmm.QMM_ERR_INVALID_ARG
+    kmax = (2 ** 31 - 1) // (255 * 128)
+    assert L.qmm_widen_b_int8_size(kmax + 1, 7, ctypes.byref(sz)) == qmm.QMM_ERR_OVERFLOW_BOUND
+    # the b16 call needs less workspace: no room for the widened weights
+    full, b16ws = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert L.qmm_int8_gemm_workspace_size(4096, 4608, 4608, ctypes.byref(full)) == qmm.QMM_OK
+    assert L.qmm_int8_gemm_b16_workspace_size(4096, 4608, 4608, ctypes.byref(b16ws)) == qmm.QMM_OK
+    assert full.value - b16ws.value >= 4608 * 4608 * 2
+    assert L.qmm_int8_gemm_b16_workspace_size(16, 1024, 1024, ctypes.byref(b16ws)) == qmm.QMM_OK and b16ws.value == 0
+    p16 = 1 << 20   # a 16-byte aligned, never dereferenced address
+    assert L.qmm_widen_b_int8(None, 64, 8, p16, 1024, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_widen_b_int8(p16, 64, 8, None, 1024, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_widen_b_int8(p16 + 4, 64, 8, p16, 1024, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_widen_b_int8(p16, 64, 8, p16 + 8, 1024, None, None) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_widen_b_int8(p16, 64, 8, p16, 1023, None, None) == qmm.QMM_ERR_INVALID_ARG
+    ep = qmm.QmmEpilogue(qmm.DTYPES["s32"], None, None, 0, None, 1.0, 0)
+    args = lambda b16: (p16, qmm.DTYPES["u8"], 128, 64, 64, 0, p16, b16, p16, 8, qmm.DTYPES["s8"], 0,
+                        ctypes.byref(ep), p16, 8, p16, 1 << 30, None, None)
+    assert L.qmm_int8_gemm_b16(*args(None)) == qmm.QMM_ERR_INVALID_ARG
+    assert L.qmm_int8_gemm_b16(*args(p16 + 2)) == qmm.QMM_ERR_INVALID_ARG

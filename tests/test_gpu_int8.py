@@ -207,6 +207,12 @@ def test_workload_large_sampled(qmm, cuda):
     # the workload exercises rounding and both clamps
     assert (got == 127).mean() > 0.001 and (got == -128).mean() > 0.001
     assert np.array_equal(col_sum.cpu().numpy().astype(np.int64), c.B.numpy().astype(np.int64).sum(0))
+    # the same call with the weights widened once beforehand: the whole output identical
+    b16 = qmm.widen_b_int8(packed, c.K, c.N)
+    out2 = qmm.int8_gemm(c.A.to(dev), c.a_type, c.zA, packed, col_sum, c.N, c.b_type, c.zB,
+                         "s8", bias=c.bias.to(dev), s_x=torch.tensor([c.s_x], device=dev),
+                         s_w=c.s_w.to(dev), s_y=c.s_y, zp_y=c.zp_y, b16=b16)
+    assert torch.equal(out2, out)
 
 
 # ---------------------------------------------------------------------------
@@ -283,6 +289,44 @@ def test_umma_fp32_accumulation_is_exact(qmm, cuda, pattern):
         B = B.to(torch.int8)
     got, _ = gpu_gemm(qmm, cuda, A, "u8", 128, B, "s8", 0, "s32")
     assert_same(got, oracle_out(A, "u8", 128, B, "s8", 0, "s32"), "s32")
+
+
+@pytest.mark.parametrize("K,N", [(100, 37), (4608, 300), (1, 5)])
+def test_widen_b_int8_bytes(qmm, cuda, K, N):
+    """The one-time f16 copy of the packed weights holds every packed code
+    exactly, the padding columns as zeros."""
+    g = torch.Generator().manual_seed(K + N)
+    B = rand_codes(g, "s8", (K, N))
+    packed, _, _ = qmm.pack_b_int8(B.to(cuda), "s8")
+    b16 = qmm.widen_b_int8(packed, K, N)
+    torch.cuda.synchronize()
+    assert b16.shape == packed.shape
+    assert torch.equal(b16.cpu(), packed.cpu().to(torch.float16))
+
+
+@pytest.mark.parametrize("M,K,N,out_type", [(65, 300, 200, "s32"), (257, 4607, 130, "s8"), (512, 2048, 520, "f32"),
+                                            (2560, 1088, 2816, "u8"), (16, 1024, 64, "s32")])
+def test_gemm_with_widened_weights_exact(qmm, cuda, M, K, N, out_type):
+    """qmm_int8_gemm_b16 (weights widened once beforehand) against the oracle,
+    bit-exact: tensor-core shapes with ragged K and N, more tiles than CTA
+    pairs, every output type, and one small-M call (which ignores the copy)."""
+    g = torch.Generator().manual_seed(3 * M + K + N)
+    A = rand_codes(g, "u8", (M, K))
+    B = rand_codes(g, "s8", (K, N))
+    bias = torch.randint(-20000, 20000, (N,), generator=g, dtype=torch.int32)
+    s_w = (torch.rand(N, generator=g) * 9e-3 + 1e-3).float()
+    s_y = 0.1 if out_type in ("s8", "u8") else 1.0
+    packed, _, col_sum = qmm.pack_b_int8(B.to(cuda), "s8")
+    b16 = qmm.widen_b_int8(packed, K, N)
+    sx = torch.tensor([1.0 / 64], device=cuda)
+    Ad = torch.zeros((M, (K + 15) // 16 * 16), dtype=torch.uint8, device=cuda)   # row stride a multiple of 16
+    Ad[:, :K] = A.to(cuda)
+    out = qmm.int8_gemm(Ad[:, :K], "u8", 131, packed, col_sum, N, "s8", -4, out_type, bias=bias.to(cuda), s_x=sx,
+                        s_w=s_w.to(cuda), s_y=s_y, zp_y=3 if out_type == "u8" else 0, b16=b16)
+    torch.cuda.synchronize()
+    ref = oracle_out(A, "u8", 131, B, "s8", -4, out_type, bias=bias, s_x=1.0 / 64, s_w=s_w.numpy(), s_y=s_y,
+                     zp_y=3 if out_type == "u8" else 0)
+    assert_same(out.cpu().numpy(), ref, out_type)
 
 
 def test_umma_route_tail_and_edge_rows_exact(qmm, cuda):
