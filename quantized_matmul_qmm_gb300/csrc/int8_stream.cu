@@ -34,6 +34,8 @@ namespace qmm {
 namespace {
 
 constexpr int kCW = 8;                         // compute warps
+constexpr int kGroups = 2;                     // compute groups: group g takes items i0 + g, i0 + g + 2, ...
+constexpr int kGW = kCW / kGroups;             // warps of a group, splitting each chunk's K
 constexpr int kEW = 2;                         // epilogue warps
 constexpr int kLoaderWarp = kCW, kEpiWarp0 = kCW + 1;
 constexpr int kThreads = 32 * (kCW + 1 + kEW);
@@ -75,18 +77,18 @@ QMM_DEV void bar_compute() { asm volatile("bar.sync 1, %0;" ::"n"(kCW * 32) : "m
 // Shared memory: A (int8 as [k-block][R][64 bytes], or f16 as [k-block][R]
 // [128 bytes] with the 16-byte units of odd rows swapped in pairs), the ring
 // [slots][16][16][64],
-// the compute warps' partial sums [2 items][kCW][R][16] int32, the row sums [R], the CTA's
+// the compute warps' partial sums [group][2 items][kGW][R][16] int32, the row sums [R], the CTA's
 // problem, then the barriers and the abort flag.
 struct Layout {
   uint32_t a, ring, red, rowsum, prob, bars, end;
-  static constexpr int kBars = 1 + 2 * kMaxSlots + 4;   // a_full, full[], empty[], red_full[2], red_empty[2]
+  static constexpr int kBars = 1 + 2 * kMaxSlots + 4 * kGroups;   // a_full, full[], empty[], red_full[g][2], red_empty[g][2]
 };
 __host__ __device__ inline Layout stream_layout(int R, int a_bytes, int slots) {
   Layout l;
   l.a = 0;
   l.ring = l.a + (uint32_t)a_bytes;
   l.red = l.ring + (uint32_t)(slots * kSlotBytes);
-  l.rowsum = l.red + (uint32_t)(2 * kCW * R * kItem * 4);
+  l.rowsum = l.red + (uint32_t)(kGroups * 2 * kGW * R * kItem * 4);
   l.prob = l.rowsum + (uint32_t)(R * 4);
   l.bars = l.prob + (uint32_t)sizeof(StreamProb);
   l.end = l.bars + (uint32_t)(Layout::kBars * 8 + 16);
@@ -167,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
   uint64_t* a_full = bars;                       // the A boxes landed
   uint64_t* full = bars + 1;                     // [slots] a chunk landed
   uint64_t* empty = bars + 1 + kMaxSlots;        // [slots] the compute warps are done with a chunk
-  uint64_t* red_full = bars + 1 + 2 * kMaxSlots; // [2] an item's partial sums are written
-  uint64_t* red_empty = red_full + 2;            // [2] the epilogue is done with them
+  uint64_t* red_full = bars + 1 + 2 * kMaxSlots; // [group][2] an item's partial sums are written
+  uint64_t* red_empty = red_full + 2 * kGroups;  // [group][2] the epilogue is done with them
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + Layout::kBars);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -187,10 +189,10 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
     mbar_init(a_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kCW);
+      mbar_init(&empty[s], kGW);   // a chunk is consumed by its item's group
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&red_full[b], kCW);
+    for (int b = 0; b < 2 * kGroups; ++b) {
+      mbar_init(&red_full[b], kGW);
       mbar_init(&red_empty[b], kEW);
     }
     *abort_flag = 0;
@@ -298,27 +300,28 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
     };
     Col c0 = load_col(i0), c1 = load_col(i0 + 1);
     for (int i = i0, j = 0; i < i1; ++i, ++j) {
-      const int b = j & 1;
+      const int grp = j % kGroups, jj = j / kGroups;   // the item's group, and its index there
+      const int b = grp * 2 + (jj & 1);
       const int n = (i - ib) * kItem + c;
       const Col c2 = load_col(i + 2);
       const int32_t e_cs = c0.cs, e_bias = c0.bias;
       const float e_sw = c0.sw;
       c0 = c1;
       c1 = c2;
-      if (!__all_sync(0xffffffffu, mbar_wait(&red_full[b], (uint32_t)((j >> 1) & 1), abort_flag, p.dev_status)))
+      if (!__all_sync(0xffffffffu, mbar_wait(&red_full[b], (uint32_t)((jj >> 1) & 1), abort_flag, p.dev_status)))
         break;
       if (*abort_flag) break;   // the compute warps gave up on this item
       if (j == 0) {
 #pragma unroll
         for (int k = 0; k < R / kRowStep; ++k) rs[k] = rowsum[min(r0 + kRowStep * k, R - 1)];
       }
-      const uint32_t rb = smem_u32(red) + (uint32_t)((b * kCW * R * kItem + r0 * kItem + c) * 4);
+      const uint32_t rb = smem_u32(red) + (uint32_t)((b * kGW * R * kItem + r0 * kItem + c) * 4);
       uint32_t S[R / kRowStep];
 #pragma unroll
       for (int k = 0; k < R / kRowStep; ++k) {
         S[k] = 0u;
 #pragma unroll
-        for (int w = 0; w < kCW; ++w) S[k] += lds32(rb + (uint32_t)((w * R + kRowStep * k) * kItem * 4));
+        for (int w = 0; w < kGW; ++w) S[k] += lds32(rb + (uint32_t)((w * R + kRowStep * k) * kItem * 4));
       }
 #pragma unroll
       for (int k = 0; k < R / kRowStep; ++k) {
@@ -425,8 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
   const uint32_t a16_lane = smem_u32(sA) + (uint32_t)(g * 128);
   const uint32_t a16_off0 = 16u * (uint32_t)((2 * t) ^ (g & 1)), a16_off1 = 16u * (uint32_t)((2 * t + 1) ^ (g & 1));
   const uint32_t b_lane = smem_u32(ring) + (uint32_t)(g * 64 + 16 * t);
-  int slot = 0, ph = 0;
-  for (int i = i0, j = 0; i < i1; ++i, ++j) {
+  const int grp = warp / kGW, wg = warp % kGW;
+  const int nch = (nkb + kChunkKb - 1) / kChunkKb;   // chunks per item
+  for (int i = i0 + grp, j = 0; i < i1; i += kGroups, ++j) {
+    // the item's chunks are numbers (i - i0) * nch + c of the CTA's sequence
+    int seq = (i - i0) * nch;
+    int slot = seq % NS, ph = (seq / NS) & 1;
     // fp32 accumulators per (row tile, column block, k parity): with one row
     // tile, the k parity doubles the independent MMA chains
     constexpr int NP = MT == 1 ? 2 : 1;
@@ -448,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
       ok = __all_sync(0xffffffffu, ok && mbar_wait(&full[slot], (uint32_t)ph, abort_flag, p.dev_status));
       if (ok) {
         const int cs = min(kChunkKb, nkb - kb0);
-        const int s0 = warp * cs / kCW, s1 = (warp + 1) * cs / kCW;
+        const int s0 = wg * cs / kGW, s1 = (wg + 1) * cs / kGW;
         if (nst + (s1 - s0) > 16) {
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
@@ -479,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
       }
     }
     // buffer j & 1 is free once the epilogue is done with item j - 2
-    const int b = j & 1;
+    const int b = grp * 2 + (j & 1);
     ok = __all_sync(0xffffffffu, mbar_wait(&red_empty[b], (uint32_t)(((j >> 1) & 1) ^ 1), abort_flag, p.dev_status)) && ok;
-    const uint32_t rb = smem_u32(red) + (uint32_t)(b * kCW * R * kItem * 4);
+    const uint32_t rb = smem_u32(red) + (uint32_t)(b * kGW * R * kItem * 4);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -494,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
           for (int pp = 0; pp < NP; ++pp) v[e] += __float2int_rn(accf[mt][nb][pp][e]);
         }
         // D fragment: (row g, columns 2t, 2t+1) and (row g + 8, same columns)
-        const uint32_t r0 = rb + (uint32_t)(((warp * R + 16 * mt + g) * kItem + 8 * nb + 2 * t) * 4);
+        const uint32_t r0 = rb + (uint32_t)(((wg * R + 16 * mt + g) * kItem + 8 * nb + 2 * t) * 4);
         sts64(r0, (uint32_t)v[0], (uint32_t)v[1]);
         sts64(r0 + 8 * kItem * 4, (uint32_t)v[2], (uint32_t)v[3]);
       }
