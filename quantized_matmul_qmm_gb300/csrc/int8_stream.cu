@@ -13,7 +13,9 @@
 // time whatever its size, so row-sized copies would cap the stream).  Both
 // operands are viewed as {64 bytes, rows, k-blocks} and land as [k-block]
 // [row][64 bytes], which the MMA fragments read without bank conflicts.
-// Eight warps split each chunk's K range; each widens its codes to f16
+// Eight compute warps in two groups take alternate items (two items in
+// flight), the four warps of a group splitting each chunk's K range; each
+// widens its codes to f16
 // (exact for |code| <= 128) and multiplies them with mma.sync m16n8k16 (fp32
 // accumulate): every product is an integer of at most 2^14, so a sum of up
 // to 1024 of them is exact in fp32, and the accumulators are drained into
@@ -34,7 +36,7 @@ namespace qmm {
 namespace {
 
 constexpr int kCW = 8;                         // compute warps
-constexpr int kGroups = 2;                     // compute groups: group g takes items i0 + g, i0 + g + 2, ...
+constexpr int kGroups = 2;                     // compute groups: group g takes items i0 + g, i0 + g + kGroups, ...
 constexpr int kGW = kCW / kGroups;             // warps of a group, splitting each chunk's K
 constexpr int kEW = 2;                         // epilogue warps
 constexpr int kLoaderWarp = kCW, kEpiWarp0 = kCW + 1;
