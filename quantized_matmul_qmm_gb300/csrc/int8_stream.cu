@@ -227,10 +227,12 @@ __global__ void __launch_bounds__(kThreads, 1) int8_stream_kernel(const __grid_c
     tma_prefetch_desc(tmA);
     tma_prefetch_desc(tmB);
     // Warm A in L2 while the previous grid finishes (L2 is where global
-    // memory is coherent; the copies come after the wait).  The weights are
-    // not warmed: a GPU-wide burst of them would queue ahead of A and of
-    // every CTA's first chunk.
+    // memory is coherent; the copies come after the wait).  Of the weights
+    // only the first chunk: a GPU-wide burst of all of them would queue ahead
+    // of A and of every CTA's first chunk.
     for (int j = 0; j < (kb_full + kChunkKb - 1) / kChunkKb; ++j) tma_prefetch_l2_3d(tmA, 0, 0, j * kChunkKb);
+    // and only the first chunk of weights (16 KB a CTA)
+    tma_prefetch_l2_3d(tmB, 0, (i0 - ib) * kItem, 0);
     pdl_wait();
     // the A boxes go first in this SM's copy queue
     mbar_arrive_expect_tx(a_full, (uint32_t)(na * kChunkKb) * kKbBytes);
