@@ -17,7 +17,10 @@
 // of the block (columns 32b + 8t .. 32b + 8t + 7) and the matching 16 bytes
 // of x.  The logical k order inside the MMA is a permutation of these, the
 // same for A and B.
+#include <algorithm>
+
 #include "qmm_internal.h"
+#include "umma.cuh"
 
 namespace qmm {
 namespace {
@@ -62,9 +65,12 @@ __device__ __forceinline__ void slab_load(SlabTile& d, const uint8_t* tile, int 
 
 // One block of 32 columns for the two rows of this thread: MMA on the biased
 // codes, then the block's scale and min.  kOneCol: only column 0 is real.
-template <int NG, bool kOneCol>
-__device__ __forceinline__ void gemv_block(const SlabTile& cur, int b, int lane, int t, int blk_x, const float* xs,
-                                           const __nv_bfloat16* const (&xrow)[NG], float (&y)[NG][4]) {
+// xload(ng) gives this thread's 16 bytes of x (token 8 ng + g, the block's
+// elements 8t .. 8t + 7).
+template <int NG, bool kOneCol, typename XLoad>
+__device__ __forceinline__ void gemv_block_x(const SlabTile& cur, int b, int lane, const float* xs, XLoad xload,
+                                             float (&y)[NG][4]) {
+  const int t = lane & 3;
   const int src = (lane & ~3) | (b >> 1);
   const uint32_t pA = __shfl_sync(0xffffffffu, (b & 1) ? cur.p[0].y : cur.p[0].x, src);
   const uint32_t pB = __shfl_sync(0xffffffffu, (b & 1) ? cur.p[1].y : cur.p[1].x, src);
@@ -79,7 +85,7 @@ __device__ __forceinline__ void gemv_block(const SlabTile& cur, int b, int lane,
   const uint32_t a12 = q4_pair_biased(wA, 3), a13 = q4_pair_biased(wB, 3);
 #pragma unroll
   for (int ng = 0; ng < NG; ++ng) {
-    const uint4 xv = xrow[ng] ? ldg128(xrow[ng] + blk_x + 8 * t) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 xv = xload(ng);
     float c[4] = {0.f, 0.f, 0.f, 0.f};
     mma_bf16_16816(c, a00, a01, a02, a03, xv.x, xv.y);
     mma_bf16_16816(c, a10, a11, a12, a13, xv.z, xv.w);
@@ -95,6 +101,14 @@ __device__ __forceinline__ void gemv_block(const SlabTile& cur, int b, int lane,
       y[ng][3] = fmaf(sB, c[3], fmaf(mB, xsv.y, y[ng][3]));
     }
   }
+}
+
+template <int NG, bool kOneCol>
+__device__ __forceinline__ void gemv_block(const SlabTile& cur, int b, int lane, int t, int blk_x, const float* xs,
+                                           const __nv_bfloat16* const (&xrow)[NG], float (&y)[NG][4]) {
+  gemv_block_x<NG, kOneCol>(cur, b, lane, xs, [&](int ng) {
+    return xrow[ng] ? ldg128(xrow[ng] + blk_x + 8 * t) : make_uint4(0u, 0u, 0u, 0u);
+  }, y);
 }
 
 template <int NG>
@@ -199,6 +213,196 @@ __global__ void __launch_bounds__(kGemvWarps * 32) q4_gemv_kernel(const Q4GemvPa
   gemv_store<NG, false>(p, y, nrow0, g, t);
 }
 
+// ---------------------------------------------------------------------------
+// Streaming decode GEMV for 2 <= M <= 16 over many tile rows (the lm_head
+// shape).  One producer thread fills a ring in shared memory with whole tile
+// rows, as TMA boxes of up to six tiles seen as lines of 128 bytes with the
+// 128-byte swizzle: 16-byte unit u of line l lands at unit u ^ (l & 7), so
+// the eight rows a warp reads in one step sit in eight different bank
+// groups.  x of every token is staged once in shared memory, each token's
+// row padded by 64 bytes so that the two tokens of a quarter-warp read
+// different banks.  Pairs of warps take the tile rows, one 16-row slab each,
+// with the block step of the kernel above; the ring slot is released as soon
+// as the pair has read it.
+// ---------------------------------------------------------------------------
+constexpr int kRWarps = 8;                        // consumer warps, in pairs
+constexpr int kRThreads = 32 * (kRWarps + 1);     // + the producer warp
+constexpr int kRMaxSlots = 16;
+constexpr int kRBoxTiles = 6;                     // a box is at most 240 lines
+constexpr size_t kRSmemCap = 227 * 1024;
+
+struct Q4GemvRingParams {
+  CUtensorMap tm;                                 // the tiles as lines of 128 bytes
+  const uint8_t* tiles;
+  int N, K, M;
+  const __nv_bfloat16* X;
+  int64_t ldx;
+  float* Y;
+  int64_t ldy;
+  int slots;                                      // ring slots of one tile row each
+  int box_tiles;                                  // tiles per TMA box (divides K / 256)
+  int32_t* dev_status;
+};
+
+__host__ __device__ inline uint32_t ring_x_stride(int K) { return (uint32_t)K * 2 + 64; }
+
+// Shared-memory bytes past the ring: x of 8 NG tokens, their block sums, the
+// barriers and the abort flag.
+__host__ __device__ inline size_t ring_tail_bytes(int K, int NG) {
+  return (size_t)8 * NG * ring_x_stride(K) + (size_t)(K / 32) * 8 * NG * 4 + 2 * kRMaxSlots * 8 + 16;
+}
+
+// Fragment data of thread (g, t) from a swizzled tile (1024-byte aligned) in
+// shared memory: word t of blocks 0..7 of rows r0 and r0 + 8 (r0 & 7 == g),
+// and the (scale, min) pairs of blocks 2t, 2t + 1, which sit at byte
+// 4096 + 32 r + 8 t of the tile.
+QMM_DEV void slab_lds_swizzled(SlabTile& d, uint32_t tile, int r0, int t) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = r0 + 8 * h;
+    const uint32_t line = tile + (uint32_t)r * 128u;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) d.c[h][b] = umma::lds32(line + (uint32_t)(((b ^ (r & 7)) << 4) | (4 * t)));
+    const int L = 32 + (r >> 2);                         // the pairs' line
+    const int u = ((r & 3) << 1) | (t >> 1);             // their 16-byte unit in it
+    uint2 pv;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(pv.x), "=r"(pv.y)
+                 : "r"(tile + (uint32_t)L * 128u + (uint32_t)((u ^ (L & 7)) << 4) + 8u * (uint32_t)(t & 1)));
+    d.p[h] = pv;
+  }
+}
+
+template <int NG>
+__global__ void __launch_bounds__(kRThreads, 1) q4_gemv_ring_kernel(const __grid_constant__ Q4GemvRingParams p) {
+  using namespace umma;
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = smem_align(sm_raw, 1024);
+  const int TC = p.K / 256;
+  const uint32_t row_bytes = (uint32_t)TC * (uint32_t)kTileBytes;
+  const uint32_t xstride = ring_x_stride(p.K);
+  uint8_t* ring = sm;                                                          // [slots][row_bytes]
+  uint8_t* xs = ring + (size_t)p.slots * row_bytes;                            // [8 NG][xstride]
+  float* xsum = reinterpret_cast<float*>(xs + (size_t)8 * NG * xstride);       // [K / 32][8 NG]
+  uint64_t* full = reinterpret_cast<uint64_t*>(xsum + (p.K / 32) * 8 * NG);    // [kRMaxSlots]
+  uint64_t* empty = full + kRMaxSlots;                                         // [kRMaxSlots]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kRMaxSlots);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int nrows = p.N / 32;
+  const int my_rows = (int)blockIdx.x < nrows ? (nrows - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&p.tm);
+    for (int s = 0; s < p.slots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 2);   // the two warps of a pair
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kRWarps) {
+    // ---- producer: tile rows blockIdx.x, blockIdx.x + gridDim.x, ... ----
+    if (lane == 0) {
+      // the first two rows into L2 while the previous grid finishes (the
+      // copies into shared memory only start after the wait)
+      for (int j = 0; j < my_rows && j < 2; ++j)
+        bulk_prefetch_l2(p.tiles + (int64_t)((int)blockIdx.x + j * (int)gridDim.x) * row_bytes, row_bytes);
+      pdl_wait();
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < my_rows; ++j) {
+        const int s = j % p.slots;
+        if (!mbar_wait(&empty[s], (uint32_t)(((j / p.slots) & 1) ^ 1), abort_flag, p.dev_status)) {
+          ok = false;
+          break;
+        }
+        const int tr = (int)blockIdx.x + j * (int)gridDim.x;
+        mbar_arrive_expect_tx(&full[s], row_bytes);
+        const uint32_t dst = smem_u32(ring) + (uint32_t)s * row_bytes;
+        for (int tc = 0; tc < TC; tc += p.box_tiles)
+          tma_load_2d_u32(dst + (uint32_t)tc * (uint32_t)kTileBytes, &p.tm, &full[s], 0, (tr * TC + tc) * 40);
+        ++issued;
+      }
+      if (!ok) {
+        // the rows already issued land before the CTA leaves: each slot's
+        // last issued phase, whether or not it was consumed
+        for (int s = 0; s < p.slots && s < issued; ++s) {
+          const int last = issued - 1 - ((issued - 1 - s) % p.slots);
+          mbar_drain(&full[s], (uint32_t)((last / p.slots) & 1));
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- consumers: x of every token into shared memory (tokens M .. 8 NG - 1
+  // as zeros), the block sums of x, then the tile rows ----
+  pdl_wait();   // x and y may belong to the previous grid
+  const int xunits = p.K / 8;   // 16-byte units of one token's x
+  for (int i = threadIdx.x; i < 8 * NG * xunits; i += kRWarps * 32) {
+    const int m = i / xunits, u = i - m * xunits;
+    const uint4 v = m < p.M ? ldg128(p.X + (int64_t)m * p.ldx + 8 * u) : make_uint4(0u, 0u, 0u, 0u);
+    sts128(smem_u32(xs) + (uint32_t)m * xstride + 16u * (uint32_t)u, v);
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kRWarps * 32) : "memory");
+  for (int idx = threadIdx.x; idx < (p.K / 32) * 8 * NG; idx += kRWarps * 32) {
+    const int blk = idx / (8 * NG), m = idx - blk * 8 * NG;
+    const uint32_t xa = smem_u32(xs) + (uint32_t)m * xstride + 64u * (uint32_t)blk;
+    float sum = 0.f;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 w = lds128(xa + 16u * v);
+      sum += bf16lo_to_f32(w.x) + bf16hi_to_f32(w.x) + bf16lo_to_f32(w.y) + bf16hi_to_f32(w.y) +
+             bf16lo_to_f32(w.z) + bf16hi_to_f32(w.z) + bf16lo_to_f32(w.w) + bf16hi_to_f32(w.w);
+    }
+    xsum[idx] = sum;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kRWarps * 32) : "memory");
+
+  // Pair q takes this CTA's rows q, q + P, ... (P = min(4, slots) pairs; the
+  // launcher makes the slot count a multiple of P, so the rows sharing a slot
+  // all belong to one pair and are consumed in order).
+  const int pair = warp >> 1, slab = warp & 1;
+  const int npairs = min(kRWarps / 2, p.slots);
+  const uint32_t xthr = smem_u32(xs) + (uint32_t)g * xstride + 16u * (uint32_t)t;   // token g, elements 8t ..
+  for (int j = pair < npairs ? pair : my_rows; j < my_rows; j += npairs) {
+    const int s = j % p.slots;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (uint32_t)((j / p.slots) & 1), abort_flag, p.dev_status)))
+      break;
+    const uint32_t rowbase = smem_u32(ring) + (uint32_t)s * row_bytes;
+    float y[NG][4];
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) y[ng][c] = 0.f;
+    for (int tc = 0; tc < TC; ++tc) {
+      SlabTile d;
+      slab_lds_swizzled(d, rowbase + (uint32_t)tc * (uint32_t)kTileBytes, 16 * slab + g, t);
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const uint32_t xb = xthr + (uint32_t)(tc * 256 + 32 * b) * 2u;
+        gemv_block_x<NG, false>(d, b, lane, xsum + (tc * 8 + b) * 8 * NG,
+                                [&](int ng) { return lds128(xb + (uint32_t)(8 * ng) * xstride); }, y);
+      }
+    }
+    // every lane's shared-memory reads of this slot are done
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    const int nrow0 = ((int)blockIdx.x + j * (int)gridDim.x) * 32 + 16 * slab;
+#pragma unroll
+    for (int ng = 0; ng < NG; ++ng)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int m = 8 * ng + 2 * t + (c & 1);
+        if (m < p.M) p.Y[(int64_t)m * p.ldy + nrow0 + g + 8 * (c >> 1)] = y[ng][c];
+      }
+  }
+}
+
 }  // namespace
 
 template <typename Kern>
@@ -214,6 +418,43 @@ cudaError_t launch_q4_gemv(const Q4DenseArgs& a, int32_t* dev_status, cudaStream
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (a.M == 1) return launch_q4_gemv1(a, sms, dev_status, stream);
+  const int NG = a.M <= 8 ? 1 : 2;
+  if (a.N / 32 >= 2 * sms) {
+    // many tile rows: the streaming ring kernel, where x and at least three
+    // tile rows fit in shared memory
+    const int TC = a.K / 256;
+    const size_t row_bytes = (size_t)TC * kTileBytes;
+    const size_t fixed = 1024 + ring_tail_bytes(a.K, NG);
+    int slots = 0;
+    if (fixed + 3 * row_bytes <= kRSmemCap) {
+      slots = (int)std::min<size_t>((kRSmemCap - fixed) / row_bytes, kRMaxSlots);
+      if (slots >= kRWarps / 2) slots -= slots % (kRWarps / 2);   // a multiple of the active pairs
+    }
+    if (slots >= 3) {
+      Q4GemvRingParams p{};
+      int bt = std::min(TC, kRBoxTiles);
+      while (TC % bt != 0) --bt;   // boxes never cross a tile row
+      if (!make_tmap_2d(&p.tm, false, const_cast<uint8_t*>(a.tiles), 64, (uint64_t)(a.N / 32) * TC * 40, 128, 64,
+                        (uint32_t)(40 * bt)))
+        return cudaErrorInvalidValue;
+      p.tiles = a.tiles;
+      p.N = a.N;
+      p.K = a.K;
+      p.M = a.M;
+      p.X = a.X;
+      p.ldx = a.ldx;
+      p.Y = a.Y;
+      p.ldy = a.ldy;
+      p.slots = slots;
+      p.box_tiles = bt;
+      p.dev_status = dev_status;
+      const size_t smem = fixed + (size_t)slots * row_bytes;
+      auto kern = NG == 1 ? q4_gemv_ring_kernel<1> : q4_gemv_ring_kernel<2>;
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      return launch_pdl(kern, dim3((unsigned)sms), dim3(kRThreads), smem, stream, p);
+    }
+  }
   Q4GemvParams p{};
   p.tiles = a.tiles;
   p.N = a.N;
@@ -225,7 +466,6 @@ cudaError_t launch_q4_gemv(const Q4DenseArgs& a, int32_t* dev_status, cudaStream
   p.ldy = a.ldy;
   const int TC = a.K / 256;
   const int slabs = a.N / 16;
-  const int NG = a.M <= 8 ? 1 : 2;
   const size_t xs_bytes = (size_t)(a.K / 32) * 8 * NG * sizeof(float);
   // split K across the warps of a CTA until the grid fills the GPU
   int S = 1;

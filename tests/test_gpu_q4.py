@@ -137,6 +137,34 @@ def test_q4_gemv_ring_slot_reuse(qmm, cuda, K, rows_per_sm):
     assert err <= 2e-5, err
 
 
+@pytest.mark.parametrize("M,K,rows_per_sm", [(2, 1024, 9), (5, 1280, 3), (8, 2048, 5), (9, 1792, 6),
+                                           (16, 1024, 11), (16, 2048, 4)])
+def test_q4_gemv_small_batch_ring(qmm, cuda, M, K, rows_per_sm):
+    """2 <= M <= 16 over many tile rows: the streaming ring kernel, with every
+    slot refilled.  The shapes cover one TMA box per tile row (K=1024, 1280),
+    two (K=2048 at four tiles a box) and one box per tile (K=1792, seven tiles),
+    one and two 8-token MMA column groups, and 3 to 8 ring slots."""
+    sms = torch.cuda.get_device_properties(cuda).multi_processor_count
+    N = 32 * sms * rows_per_sm
+    g = torch.Generator().manual_seed(M * 1000 + K + rows_per_sm)
+    W = torch.randn((N, K), generator=g) * 0.02
+    X = torch.randn((M, K), generator=g).to(torch.bfloat16)
+    tiles, Y = gpu_q4(qmm, cuda, W, X, pad=0)
+    assert np.isfinite(Y).all()
+    rng = np.random.default_rng(M + K)
+    ntr = N // 32
+    trs = np.unique(np.concatenate([np.arange(0, ntr, sms), np.arange(ntr - 8, ntr),
+                                    rng.choice(ntr, 24, replace=False)]))
+    per = (K // 256) * 5120
+    rows = np.concatenate([np.arange(32 * tr, 32 * tr + 32) for tr in trs])
+    Wn = W.numpy()
+    for tr in trs:   # packing of the sampled tile rows, byte for byte
+        assert np.array_equal(tiles[tr * per:(tr + 1) * per], O.pack_q4(Wn[32 * tr:32 * tr + 32]))
+    y, norm = O.q4_gemm_rows(tiles, N, K, xnp(X), rows)
+    err = O.normalized_error(Y[:, rows], y, norm)
+    assert err <= 2e-5, err
+
+
 @pytest.mark.parametrize("M,N,K", [(577, 8192, 256), (300, 12288, 256)])
 def test_q4_prefill_192_token_chunks(qmm, cuda, M, N, K):
     """Prefill GEMMs large enough in N to take 192-token jobs (the MMA's N),
