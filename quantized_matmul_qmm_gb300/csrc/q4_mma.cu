@@ -2,8 +2,11 @@
 //
 // The weights are 32x256 q4_1 tiles ("NPU engine: full ELFs, no xclbin", "Q4NX
 // chunks"; w = q*scale + min, "Zaya 8B Q4NX on the AMD NPU", round 26).  At
-// decode sizes the work is bound by the weight stream, so each warp streams
-// whole tiles with 16-byte loads and never expands them in memory.
+// decode sizes the work is bound by the weight stream, and the tiles are
+// never expanded in memory.  Two kernels: over many tile rows, a producer
+// thread streams whole tile rows into a shared ring (q4_gemv_ring_kernel);
+// for fewer rows, each warp walks its slab's tiles with loads prefetched in
+// registers and the warps of a CTA split K (q4_gemv_kernel).
 //
 // The factored form keeps the per-weight work to one logic op per two codes.
 // For one block (32 columns of one row):
