@@ -1052,7 +1052,7 @@ def main():
     for name, d in streams["q4_small_batch"].items():
         rooflines[name] = {"bound": "hbm", "achieved": d["GBs"], "peak": hbm_peak, "unit": "GB/s",
                            "frac": d["GBs"] / hbm_peak, "peak_probe": probe["GBs"],
-                           "frac_probe": d["GBs"] / probe["GBs"], "traffic": None}
+                           "frac_probe": d["GBs"] / probe["GBs"], "traffic": traffic.get(name)}
     c = hp.int8
     launches = sum(l for (_, _, l, _) in hp.calls) * args.steps
     line = {
