@@ -228,8 +228,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32) q4_gemv_kernel(const Q4GemvPa
 // with the block step of the kernel above; the ring slot is released as soon
 // as the pair has read it.
 // ---------------------------------------------------------------------------
-constexpr int kRWarps = 8;                        // consumer warps, in pairs
-constexpr int kRThreads = 32 * (kRWarps + 1);     // + the producer warp
+// Consumer warps, in pairs: 8 for one 8-token column group, 16 for two (the
+// second group doubles the issue work per byte; measured on lm_head, 16 warps
+// took M = 9..16 from 29.3-29.7 to 27.0-28.0 us, and 8 warps stayed faster at
+// M = 8: 21.8 against 22.5-22.9 us).  The producer warp comes after them.
+__host__ __device__ constexpr int ring_warps(int NG) { return NG == 1 ? 8 : 16; }
 constexpr int kRMaxSlots = 16;
 constexpr int kRBoxTiles = 6;                     // a box is at most 240 lines
 constexpr size_t kRSmemCap = 227 * 1024;
@@ -277,8 +280,10 @@ QMM_DEV void slab_lds_swizzled(SlabTile& d, uint32_t tile, int r0, int t) {
 }
 
 template <int NG>
-__global__ void __launch_bounds__(kRThreads, 1) q4_gemv_ring_kernel(const __grid_constant__ Q4GemvRingParams p) {
+__global__ void __launch_bounds__(32 * (ring_warps(NG) + 1), 1)
+    q4_gemv_ring_kernel(const __grid_constant__ Q4GemvRingParams p) {
   using namespace umma;
+  constexpr int kRWarps = ring_warps(NG);
   extern __shared__ uint8_t sm_raw[];
   uint8_t* sm = smem_align(sm_raw, 1024);
   const int TC = p.K / 256;
@@ -431,7 +436,7 @@ cudaError_t launch_q4_gemv(const Q4DenseArgs& a, int32_t* dev_status, cudaStream
     int slots = 0;
     if (fixed + 3 * row_bytes <= kRSmemCap) {
       slots = (int)std::min<size_t>((kRSmemCap - fixed) / row_bytes, kRMaxSlots);
-      if (slots >= kRWarps / 2) slots -= slots % (kRWarps / 2);   // a multiple of the active pairs
+      if (slots >= ring_warps(NG) / 2) slots -= slots % (ring_warps(NG) / 2);   // a multiple of the active pairs
     }
     if (slots >= 3) {
       Q4GemvRingParams p{};
@@ -455,7 +460,7 @@ cudaError_t launch_q4_gemv(const Q4DenseArgs& a, int32_t* dev_status, cudaStream
       auto kern = NG == 1 ? q4_gemv_ring_kernel<1> : q4_gemv_ring_kernel<2>;
       const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
-      return launch_pdl(kern, dim3((unsigned)sms), dim3(kRThreads), smem, stream, p);
+      return launch_pdl(kern, dim3((unsigned)sms), dim3(32 * (ring_warps(NG) + 1)), smem, stream, p);
     }
   }
   Q4GemvParams p{};
