@@ -356,7 +356,8 @@ qmm_status qmm_w8_gemm(const void* codes, const float* scales, int64_t N, int64_
   if (M > INT32_MAX || N > INT32_MAX || K > kW8MaxK) return QMM_ERR_UNSUPPORTED;
   const int8_t* c = static_cast<const int8_t*>(codes);
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
-  if (M <= kW8GemvMaxM) return cuda_status(launch_w8_gemv(c, scales, (int)N, (int)K, x, ldx, (int)M, Y, ldy, stream));
+  if (M <= kW8GemvMaxM)
+    return cuda_status(launch_w8_gemv(c, scales, (int)N, (int)K, x, ldx, (int)M, Y, ldy, dev_status, stream));
   const size_t need = w8_umma_workspace_bytes(K, N);
   if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256)) return QMM_ERR_WORKSPACE;
   if ((N + 255) / 256 > 65535) return QMM_ERR_UNSUPPORTED;

@@ -57,6 +57,10 @@ bool make_tmap_q4_tiles(CUtensorMap* map, const void* tiles, uint64_t tile_cols,
 // read as zero.
 bool make_tmap_kblocks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_stride, uint64_t kblocks,
                        uint32_t box_rows, uint32_t box_kblocks);
+// The same with 128-byte k-blocks and the 128-byte swizzle (row_stride a
+// multiple of 128, so no k-block reaches past its row).
+bool make_tmap_kblocks128_sw(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_stride,
+                             uint64_t kblocks, uint32_t box_rows, uint32_t box_kblocks);
 
 // ---- packs (pack.cu) ----
 cudaError_t launch_pack_b_int8(const void* B, qmm_dtype b_type, int64_t K, int64_t N, int64_t ldb,
@@ -109,7 +113,7 @@ int64_t w8_blocks(int64_t K);     // scales per row: ceil(K / 1024)
 cudaError_t launch_pack_w8(const float* W, int N, int K, int64_t ldw, int8_t* codes, float* scales,
                            cudaStream_t stream);
 cudaError_t launch_w8_gemv(const int8_t* codes, const float* scales, int N, int K, const __nv_bfloat16* X,
-                           int64_t ldx, int M, float* Y, int64_t ldy, cudaStream_t stream);
+                           int64_t ldx, int M, float* Y, int64_t ldy, int32_t* dev_status, cudaStream_t stream);
 size_t w8_umma_workspace_bytes(int64_t K, int64_t N);
 cudaError_t launch_w8_gemm_umma(const int8_t* codes, const float* scales, int N, int K,
                                 const __nv_bfloat16* X, int64_t ldx, int M, float* Y, int64_t ldy,

@@ -76,4 +76,22 @@ bool make_tmap_kblocks(CUtensorMap* map, const void* base, uint64_t rows, uint64
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_kblocks128_sw(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_stride,
+                             uint64_t kblocks, uint32_t box_rows, uint32_t box_kblocks) {
+  std::call_once(g_once, resolve);
+  if (g_encode == nullptr) return false;
+  // Bytes of a row-major [rows][row_stride] matrix seen as {128 bytes, rows,
+  // k-blocks} (k-block stride 128 outermost): a box lands as [k-block][row]
+  // [128 bytes] with the 128-byte swizzle (16-byte unit u of line l at
+  // u ^ (l & 7)).
+  const cuuint64_t dims[3] = {128, rows, kblocks};
+  const cuuint64_t strides[2] = {row_stride, 128};
+  const cuuint32_t box[3] = {128, box_rows, box_kblocks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace qmm

@@ -21,6 +21,7 @@
 #include <algorithm>
 
 #include "qmm_internal.h"
+#include "umma.cuh"
 
 namespace qmm {
 namespace {
@@ -143,6 +144,189 @@ w8_gemv_kernel(const int8_t* __restrict__ codes, const float* __restrict__ scale
   }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming decode GEMV for one token over many rows.  One producer thread
+// brings 32-row items of whole rows into a ring in shared memory, one TMA box
+// per item, seen as {128 bytes, 32 rows, Kp / 128 k-blocks} with the 128-byte
+// swizzle: the box lands as [k-block][row][128 bytes] with 16-byte unit u of
+// row r at u ^ (r & 7), so the eight rows a quarter-warp reads sit in eight
+// different bank groups.  Each consumer warp owns one ring slot and takes the
+// items of that slot in order.  Lane (r, h) of a warp works on rows r and
+// r + 16 over half h of the k-blocks, so every x value read from shared
+// memory serves two rows; the halves are added with one shuffle.
+// ---------------------------------------------------------------------------
+constexpr int kW8RItemRows = 32;
+constexpr int kW8RMaxWarps = 12;              // consumer warps = ring slots
+constexpr size_t kW8RSmemCap = 227 * 1024;
+constexpr int kW8RMaxKp = 2048;               // at most 3 scale blocks per lane
+
+struct W8RingParams {
+  CUtensorMap tm;                             // the codes as {128 bytes, rows, k-blocks}
+  const int8_t* codes;
+  const float* scales;
+  int N, K, Kp, nb;
+  const __nv_bfloat16* X;
+  float* Y;
+  int32_t* dev_status;
+};
+
+// 4 codes of a word (already XORed with 0x80808080) as two f32 pairs, exact.
+__device__ __forceinline__ void w8_word_pairs(uint32_t w, uint64_t& p01, uint64_t& p23) {
+  const uint64_t nbias = f2_pack(-8388736.0f, -8388736.0f);   // -(2^23 + 128)
+  p01 = f2_add(f2_pack(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u)),
+                       __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541u))), nbias);
+  p23 = f2_add(f2_pack(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7542u)),
+                       __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7543u))), nbias);
+}
+
+// 16 codes of one row times x (16 f32 in four 16-byte vectors) into the pair
+// accumulator acc (even and odd k in its two halves).
+__device__ __forceinline__ uint64_t w8_dot16(const uint4 c, const uint4 (&x)[4], uint64_t acc) {
+  const uint32_t w[4] = {c.x ^ 0x80808080u, c.y ^ 0x80808080u, c.z ^ 0x80808080u, c.w ^ 0x80808080u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint64_t p01, p23;
+    w8_word_pairs(w[i], p01, p23);
+    acc = f2_fma(p01, f2_pack(__uint_as_float(x[i].x), __uint_as_float(x[i].y)), acc);
+    acc = f2_fma(p23, f2_pack(__uint_as_float(x[i].z), __uint_as_float(x[i].w)), acc);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float f2_sum(uint64_t v) {
+  float lo, hi;
+  f2_unpack(v, lo, hi);
+  return lo + hi;
+}
+
+__global__ void __launch_bounds__(32 * (kW8RMaxWarps + 1), 1) w8_gemv_ring_kernel(const __grid_constant__ W8RingParams p) {
+  using namespace umma;
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = smem_align(sm_raw, 1024);
+  const int W = (int)blockDim.x / 32 - 1;                 // consumer warps, one ring slot each
+  const uint32_t slot_bytes = (uint32_t)kW8RItemRows * (uint32_t)p.Kp;
+  uint8_t* ring = sm;                                      // [W][Kp / 128][32][128], swizzled
+  float* xs = reinterpret_cast<float*>(ring + (size_t)W * slot_bytes);   // [Kp], zeros past K
+  uint64_t* full = reinterpret_cast<uint64_t*>(xs + p.Kp);
+  uint64_t* empty = full + kW8RMaxWarps;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kW8RMaxWarps);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int items = (p.N + kW8RItemRows - 1) / kW8RItemRows;
+  const int my_items = (int)blockIdx.x < items ? (items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  const int nkb = p.Kp / 128;
+
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&p.tm);
+    for (int s = 0; s < W; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+
+  if (warp == W) {
+    // ---- producer: items blockIdx.x, blockIdx.x + gridDim.x, ... ----
+    if (lane == 0) {
+      // the first two items into L2 while the previous grid finishes (the
+      // copies into shared memory only start after the wait)
+      for (int j = 0; j < my_items && j < 2; ++j) {
+        const int row0 = ((int)blockIdx.x + j * (int)gridDim.x) * kW8RItemRows;
+        const int rows = min(kW8RItemRows, p.N - row0);
+        bulk_prefetch_l2(p.codes + (int64_t)row0 * p.Kp, (uint32_t)rows * (uint32_t)p.Kp);
+      }
+      pdl_wait();
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < my_items; ++j) {
+        const int s = j % W;
+        if (!mbar_wait(&empty[s], (uint32_t)(((j / W) & 1) ^ 1), abort_flag, p.dev_status)) {
+          ok = false;
+          break;
+        }
+        const int row0 = ((int)blockIdx.x + j * (int)gridDim.x) * kW8RItemRows;
+        mbar_arrive_expect_tx(&full[s], slot_bytes);
+        tma_load_3d(smem_u32(ring) + (uint32_t)s * slot_bytes, &p.tm, &full[s], 0, row0, 0);
+        ++issued;
+      }
+      if (!ok) {
+        // the items already issued land before the CTA leaves: each slot's
+        // last issued phase, whether or not it was consumed
+        for (int s = 0; s < W && s < issued; ++s) {
+          const int last = issued - 1 - ((issued - 1 - s) % W);
+          mbar_drain(&full[s], (uint32_t)((last / W) & 1));
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- consumers: x as f32 into shared memory, then the items of this
+  // warp's slot ----
+  pdl_wait();   // x and y may belong to the previous grid
+  for (int k = threadIdx.x; k < p.Kp; k += W * 32) xs[k] = k < p.K ? __bfloat162float(p.X[k]) : 0.f;
+  asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
+  const int r = lane & 15, h = lane >> 4;
+  const int kb0 = h ? (nkb + 1) / 2 : 0, kb1 = h ? nkb : (nkb + 1) / 2;   // this lane's k-blocks
+  const int b0 = (kb0 * 128) >> 10;                                       // its first scale block
+  const uint32_t xsa = smem_u32(xs);
+  for (int j = warp; j < my_items; j += W) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[warp], (uint32_t)((j / W) & 1), abort_flag, p.dev_status)))
+      break;
+    const int n0 = ((int)blockIdx.x + j * (int)gridDim.x) * kW8RItemRows + r, n1 = n0 + 16;
+    // the scales of (at most) three blocks from b0 for both rows, read ahead
+    float sA[3], sB[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int b = b0 + q;
+      sA[q] = (n0 < p.N && b < p.nb) ? __ldg(p.scales + (int64_t)n0 * p.nb + b) : 0.f;
+      sB[q] = (n1 < p.N && b < p.nb) ? __ldg(p.scales + (int64_t)n1 * p.nb + b) : 0.f;
+    }
+    const uint32_t rowA = smem_u32(ring) + (uint32_t)warp * slot_bytes + (uint32_t)r * 128u;
+    const uint32_t rowB = rowA + 16u * 128u;
+    float yA = 0.f, yB = 0.f;
+    uint64_t accA = 0ull, accB = 0ull;   // pair sums of the current scale block
+    int q = 0;                           // current block, relative to b0
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int bq = ((kb * 128) >> 10) - b0;
+      if (bq != q) {   // a new scale block: close the previous one
+        yA = fmaf(f2_sum(accA), q == 0 ? sA[0] : (q == 1 ? sA[1] : sA[2]), yA);
+        yB = fmaf(f2_sum(accB), q == 0 ? sB[0] : (q == 1 ? sB[1] : sB[2]), yB);
+        accA = 0ull;
+        accB = 0ull;
+        q = bq;
+      }
+      const uint32_t off = (uint32_t)kb * (uint32_t)(kW8RItemRows * 128);
+#pragma unroll 4
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t sw = (uint32_t)((u ^ (r & 7)) << 4);
+        const uint4 cA = lds128(rowA + off + sw);
+        const uint4 cB = lds128(rowB + off + sw);
+        const uint32_t xa = xsa + (uint32_t)(kb * 128 + 16 * u) * 4u;
+        const uint4 xv[4] = {lds128(xa), lds128(xa + 16u), lds128(xa + 32u), lds128(xa + 48u)};
+        accA = w8_dot16(cA, xv, accA);
+        accB = w8_dot16(cB, xv, accB);
+      }
+    }
+    if (kb1 > kb0) {
+      yA = fmaf(f2_sum(accA), q == 0 ? sA[0] : (q == 1 ? sA[1] : sA[2]), yA);
+      yB = fmaf(f2_sum(accB), q == 0 ? sB[0] : (q == 1 ? sB[1] : sB[2]), yB);
+    }
+    // every lane's reads of this slot are done
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[warp]);
+    yA += __shfl_xor_sync(0xffffffffu, yA, 16);
+    yB += __shfl_xor_sync(0xffffffffu, yB, 16);
+    if (h == 0) {
+      if (n0 < p.N) p.Y[n0] = yA;
+      if (n1 < p.N) p.Y[n1] = yB;
+    }
+  }
+}
+
 }  // namespace
 
 int64_t w8_padded_k(int64_t K) { return (K + 63) / 64 * 64; }
@@ -155,10 +339,37 @@ cudaError_t launch_pack_w8(const float* W, int N, int K, int64_t ldw, int8_t* co
 }
 
 cudaError_t launch_w8_gemv(const int8_t* codes, const float* scales, int N, int K, const __nv_bfloat16* X,
-                           int64_t ldx, int M, float* Y, int64_t ldy, cudaStream_t stream) {
+                           int64_t ldx, int M, float* Y, int64_t ldy, int32_t* dev_status, cudaStream_t stream) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int Kp = (int)w8_padded_k(K), nb = (int)w8_blocks(K);
+  if (M == 1 && Kp % 128 == 0 && Kp <= kW8RMaxKp && N / kW8RItemRows >= 2 * sms) {
+    // one token over many rows: the streaming ring kernel, with at least
+    // three 32-row items in flight per SM
+    const size_t slot_bytes = (size_t)kW8RItemRows * Kp;
+    const size_t fixed = 1024 + (size_t)Kp * 4 + 2 * kW8RMaxWarps * 8 + 16;
+    const int W = (int)std::min<size_t>((kW8RSmemCap - fixed) / slot_bytes, kW8RMaxWarps);
+    if (W >= 3) {
+      W8RingParams p{};
+      if (!make_tmap_kblocks128_sw(&p.tm, codes, (uint64_t)N, (uint64_t)Kp, (uint64_t)(Kp / 128), kW8RItemRows,
+                                   (uint32_t)(Kp / 128)))
+        return cudaErrorInvalidValue;
+      p.codes = codes;
+      p.scales = scales;
+      p.N = N;
+      p.K = K;
+      p.Kp = Kp;
+      p.nb = nb;
+      p.X = X;
+      p.Y = Y;
+      p.dev_status = dev_status;
+      const size_t smem = fixed + (size_t)W * slot_bytes;
+      const cudaError_t e =
+          cudaFuncSetAttribute(w8_gemv_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      return launch_pdl(w8_gemv_ring_kernel, dim3((unsigned)sms), dim3(32 * (W + 1)), smem, stream, p);
+    }
+  }
   // lanes per row: about kGvSteps groups each, at least 4 lanes, at most 32
   int G = 32;
   while (G > 4 && G * kGvSteps > Kp / 16) G >>= 1;

@@ -126,6 +126,28 @@ def test_w8_lm_head_decode_full_size(qmm, cuda):
     check(Y, ref, norm)
 
 
+@pytest.mark.parametrize("K,items_per_sm,extra", [(128, 2, 0), (1000, 3, 17), (1100, 2, 5), (1536, 3, 0),
+                                                 (2048, 4, 31)])
+def test_w8_gemv_streaming_ring(qmm, cuda, K, items_per_sm, extra):
+    """M = 1 over many rows: the streaming ring kernel.  K = 128 (one k-block,
+    the second half-warp idle, 12 slots), 1000 and 1536 (one scale block),
+    1100 (nine k-blocks split 5 + 4, the second half crossing into the second
+    scale block) and 2048 (two scale blocks, 3 slots); N past a multiple of 32
+    leaves the last item partly outside the matrix; every slot is refilled."""
+    sms = torch.cuda.get_device_properties(cuda).multi_processor_count
+    N = 32 * sms * items_per_sm + extra
+    g = torch.Generator().manual_seed(K + extra)
+    W = torch.randn((N, K), generator=g) * 0.02
+    W[7] = 0.0
+    X = torch.randn((1, K), generator=g).to(torch.bfloat16)
+    codes, scales = O.pack_w8(W.numpy())
+    cd, sd = upload_w8(qmm, cuda, codes, scales)
+    Y = gpu_w8(qmm, cuda, cd, sd, N, K, X)
+    ref, norm = O.w8_gemm(codes, scales, X.float().double().numpy())
+    check(Y, ref, norm)
+    assert (Y[0, 7] == 0.0)
+
+
 def test_w8_large_gemm_sampled_rows(qmm, cuda):
     """M = 4096, K = N = 4608 on the tensor-core route, checked on 48 sampled
     rows (rows are independent, so the oracle runs on those rows alone)."""
