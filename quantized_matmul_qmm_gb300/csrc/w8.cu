@@ -8,13 +8,15 @@
 // q = clamp(rint_even(fl(w / s)), -127, 127), 0 where s == 0.  Codes are
 // [N][Kp] (Kp = K rounded up to 64, zero padding), scales [N][ceil(K/1024)].
 //
-// Decode GEMV (M <= 16): a warp streams 32/G rows at once with G lanes per
-// row, G sized so that every lane has about eight 16-byte groups of its row
-// (a K = 1024 row is 1 KB: four rows per warp, 4 KB in flight per warp).  Each
-// lane converts its codes exactly with a byte permute and one add (the
-// int-to-float unit runs at a quarter of the fma rate) and multiplies them
-// with x read through the read-only cache, even and odd columns as the two
-// lanes of packed f32x2 fmas.  Sixteen codes never straddle a 1,024 block, so
+// Decode GEMV for one token over many rows: the streaming ring kernel
+// (w8_gemv_ring_kernel, below).  Otherwise (M <= 16, or few rows): a warp
+// streams 32/G rows at once with G lanes per row, G sized so that every lane
+// has about eight 16-byte groups of its row (a K = 1024 row is 1 KB: four
+// rows per warp, 4 KB in flight per warp).  Each lane converts its codes
+// exactly with a byte permute and one add (the int-to-float unit runs at a
+// quarter of the fma rate) and multiplies them with x read through the
+// read-only cache, even and odd columns as the two lanes of packed f32x2
+// fmas.  Sixteen codes never straddle a 1,024 block, so
 // each group's partial sum is scaled by its own block's scale.
 #include <cuda_bf16.h>
 
