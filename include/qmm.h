@@ -511,8 +511,9 @@ qmm_status qmm_w8_gemm_workspace_size(int64_t M, int64_t K, int64_t N, size_t* w
  * Y      fp32 [M][N], row stride ldy elements (ldy >= N), 4-byte aligned.
  * workspace / ws_bytes  qmm_w8_gemm_workspace_size bytes, 256-byte aligned
  *        (NULL when that size is 0), rewritten by the call.
- * M <= 16 runs the decode GEMV (codes streamed once, one warp per row);
- * larger M the tensor-core GEMM (the codes widened to bf16, which is exact;
+ * M <= 16 runs the decode GEMV (codes streamed once; M = 1 over many rows
+ * streams 32-row items through a shared-memory ring with bounded waits, which
+ * report QMM_ERR_TIMEOUT into dev_status); larger M the tensor-core GEMM (the codes widened to bf16, which is exact;
  * each 1,024-k block summed in the tensor cores' fp32 accumulator, then
  * scaled).  Both compute the same function, within
  * max |y - y_exact| <= 2e-4 * sum_k |x| |w|: the products code * x are exact
